@@ -1,0 +1,170 @@
+"""CPU oracle for paged KV-cache decode (fp64).
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the package's ``smoke()`` check
+and the bench's CPU-baseline leg may import this package.  The product path
+(the CUDA library and its binding) never imports, links or runs it, and the
+oracle imports nothing from the product.
+
+Parts:
+
+* ``pa_oracle.c`` -- cache write, block-table gather and textbook softmax
+  attention in fp64 (built to ``liboracle.so`` by :func:`build`).
+* :mod:`oracle.allocator` -- the block allocator model (free queue, ref
+  counts, copy-on-write).
+* :func:`kv_bytes_per_token` -- the pages' KV size formula.
+
+Every function cites the passage it follows in its own docstring or in the
+header of ``pa_oracle.c``.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+DTYPE_CODES = {"f16": 0, "bf16": 1}
+
+
+def kv_bytes_per_token(num_layers, num_kv_heads, head_dim, bytes_per_elem):
+    """KV bytes per token = 2 x layers x KV heads x head_dim x bytes/element.
+
+    The leading 2 counts K and V.  Defined in "Yerel LLM sistemlerinde
+    backpressure ve olcekleme", section "KV butcesi", and restated with a
+    worked example in "vLLM Nedir? PagedAttention ile Production LLM
+    Serving", section "Asil sisen sey agirlik degil, KV cache".  Both
+    insist on the KV-head count (not the attention-head count); the other
+    page's version with attention heads lost its formula in extraction.
+    """
+    return 2 * num_layers * num_kv_heads * head_dim * bytes_per_elem
+
+
+def build(force=False):
+    """Compile pa_oracle.c with gcc (OpenMP, no FP contraction) if stale."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
+
+
+class OracleLib:
+    """ctypes handle on one build of pa_oracle.c (the default one, or a
+    variant a test compiled from a modified copy of the source)."""
+
+    def __init__(self, path):
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i32, i64 = ctypes.c_int32, ctypes.c_int64
+        lib.oracle_bits_to_double.argtypes = [P, i64, ctypes.c_int, P]
+        lib.oracle_bits_to_double.restype = None
+        lib.oracle_cache_write.argtypes = [P, P, P, i64, i32, i32, i32, P, P, i64]
+        lib.oracle_cache_write.restype = i64
+        lib.oracle_gather.argtypes = [P, ctypes.c_int, P, i32, i32, i32, i32, i32, P]
+        lib.oracle_gather.restype = None
+        lib.oracle_decode.argtypes = [P, P, P, ctypes.c_int, P, i32, P, i32, i32, i32, i32, i32,
+                                      ctypes.c_double, P, ctypes.c_int]
+        lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = path
+
+
+def compile_source(src, out_path):
+    """Compile a pa_oracle.c-like source file to a shared library."""
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def _load(handle=None):
+    global _lib
+    if handle is not None:
+        return handle.lib
+    if _lib is None:
+        build()
+        _lib = OracleLib(_LIB_PATH)
+    return _lib.lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {a.dtype}")
+    return a
+
+
+def max_threads(handle=None):
+    return _load(handle).oracle_max_threads()
+
+
+def bits_to_double(bits, dtype, handle=None):
+    """Exact fp64 value of each 16-bit pattern (dtype 'f16' or 'bf16')."""
+    bits = _c(np.asarray(bits), np.uint16)
+    out = np.empty(bits.shape, np.float64)
+    _load(handle).oracle_bits_to_double(_ptr(bits), bits.size, DTYPE_CODES[dtype], _ptr(out))
+    return out
+
+
+def cache_write(k, v, slot_mapping, k_cache, v_cache, block_size=16, handle=None):
+    """Scatter k/v [T, Hkv, D] (uint16 patterns) into copies of the caches.
+
+    Returns (k_cache', v_cache', n_out_of_range).  Slots < 0 are skipped; so
+    are slots past the pool (counted).
+    """
+    k, v = _c(k, np.uint16), _c(v, np.uint16)
+    slot_mapping = _c(slot_mapping, np.int64)
+    kc, vc = np.array(k_cache, np.uint16, copy=True), np.array(v_cache, np.uint16, copy=True)
+    T, Hkv, D = k.shape
+    nb = kc.shape[0]
+    assert kc.shape == (nb, Hkv, block_size, D) and vc.shape == kc.shape
+    bad = _load(handle).oracle_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, block_size,
+                                     _ptr(kc), _ptr(vc), nb)
+    return kc, vc, int(bad)
+
+
+def gather(cache, dtype, table_row, seq_len, h, block_size=16, handle=None):
+    """Contiguous fp64 [seq_len, D] of KV head h read through one table row."""
+    cache = _c(cache, np.uint16)
+    table_row = _c(table_row, np.int32)
+    nb, Hkv, bs, D = cache.shape
+    assert bs == block_size
+    out = np.empty((seq_len, D), np.float64)
+    _load(handle).oracle_gather(_ptr(cache), DTYPE_CODES[dtype], _ptr(table_row), seq_len, Hkv, h, D,
+                          block_size, _ptr(out))
+    return out
+
+
+def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, dtype, block_size=16, threads=0,
+           handle=None):
+    """fp64 attention of each query against its sequence's paged K/V.
+
+    q [B, Hq, D] and the caches [NB, Hkv, bs, D] are uint16 patterns of
+    ``dtype``; block_tables [B, max_blocks] int32; seq_lens [B] int32.
+    Returns out [B, Hq, D] float64.  threads=0 lets OpenMP choose.
+    """
+    q = _c(q, np.uint16)
+    k_cache, v_cache = _c(k_cache, np.uint16), _c(v_cache, np.uint16)
+    block_tables, seq_lens = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    B, Hq, D = q.shape
+    nb, Hkv, bs, D2 = k_cache.shape
+    assert D2 == D and bs == block_size and v_cache.shape == k_cache.shape
+    assert Hq % Hkv == 0 and block_tables.shape[0] == B and seq_lens.shape == (B,)
+    out = np.empty((B, Hq, D), np.float64)
+    rc = _load(handle).oracle_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), DTYPE_CODES[dtype],
+                               _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq,
+                               Hkv, D, block_size, float(scale), _ptr(out), int(threads))
+    if rc != 0:
+        raise MemoryError("oracle_decode could not allocate its gather buffers")
+    return out

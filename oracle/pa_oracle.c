@@ -1,0 +1,233 @@
+/*
+ * Oracle for paged KV-cache decode: plain, slow, fp64 C.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * under paged_kv_cache_blocks_gb300/) includes, links or calls this file; only
+ * the tests, the package's smoke check and the CPU-baseline leg of the bench
+ * use it.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes, and where that is defined:
+ *
+ *   - KV layout.  The cache is cut into fixed blocks of `block_size` (16)
+ *     tokens; a per-sequence block table maps logical block j to a physical
+ *     block id, like a page table maps virtual pages to frames.
+ *       "vLLM Nedir? PagedAttention ile Production LLM Serving", section
+ *       "PagedAttention"; "vLLM ve Triton ile maliyet optimizasyonu",
+ *       section 03 ("Yontem"), steps 1 and 2.
+ *     Physical layout (the pages leave it open; our reading): one array per
+ *     K and per V of shape [num_blocks][num_kv_heads][block_size][head_dim].
+ *
+ *   - Cache write: the new token's key/value rows are copied to the slot the
+ *     allocator handed out, slot = block_id * block_size + offset.
+ *       "vLLM Nedir?", section "Bir istek motorun icinde", step 2
+ *       (allocate_slots); "vLLM ve Triton", section 03, step 3.
+ *
+ *   - Attention: the maths of scaled dot-product attention is unchanged by
+ *     paging, only where K and V are read from changes:
+ *       out = softmax(q K^T / sqrt(d_k)) V  over the sequence's tokens.
+ *       "vLLM ve Triton", section 03, the paragraph on scaled dot-product
+ *       attention (its formula was lost in extraction; this is the standard
+ *       definition it names).
+ *     Grouped-query attention: several query heads share one KV head.
+ *       "Yerel LLM sistemlerinde backpressure ve olcekleme", section
+ *       "KV butcesi" (64 attention heads, 8 KV heads).
+ *     Our reading: query head i uses KV head i / G, G = Hq / Hkv (contiguous
+ *     groups).
+ *
+ * Method: gather every sequence's blocks into a contiguous fp64 K and V
+ * (exact conversion from fp16/bf16), then textbook softmax attention in fp64:
+ * scores, subtract the maximum, exp (libm), normalise, weighted sum of V.
+ * No online softmax, no partitions, no blocking.
+ *
+ * Element types are passed as raw 16-bit patterns: dtype 0 = IEEE binary16,
+ * dtype 1 = bfloat16.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- 16-bit float decoding, written from the IEEE 754 / bfloat16 layouts ---- */
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double mag;
+    if (e == 0) {
+        mag = ldexp((double)f, -24);           /* subnormal: f * 2^-14 * 2^-10 */
+    } else if (e == 31) {
+        mag = (f == 0) ? INFINITY : NAN;
+    } else {
+        mag = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+    }
+    return sign ? -mag : mag;
+}
+
+/* bfloat16: the top 16 bits of an IEEE binary32 (1, 8 bits bias 127, 7). */
+static double bf16_bits_to_double(uint16_t b) {
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xff;
+    int f = b & 0x7f;
+    double mag;
+    if (e == 0) {
+        mag = ldexp((double)f, -133);          /* subnormal: f * 2^-126 * 2^-7 */
+    } else if (e == 255) {
+        mag = (f == 0) ? INFINITY : NAN;
+    } else {
+        mag = ldexp((double)(128 + f), e - 134); /* (1 + f/128) * 2^(e-127) */
+    }
+    return sign ? -mag : mag;
+}
+
+static double to_double(uint16_t bits, int dtype) {
+    return dtype == 0 ? half_bits_to_double(bits) : bf16_bits_to_double(bits);
+}
+
+/* Exposed so the tests can check the decoding against numpy / torch. */
+void oracle_bits_to_double(const uint16_t* bits, int64_t n, int dtype, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = to_double(bits[i], dtype);
+}
+
+/* ---- cache write ---- */
+
+/*
+ * For every token t with slot s = slot_mapping[t] >= 0: copy the head_dim
+ * 16-bit values of k[t][h] to k_cache[s / block_size][h][s % block_size] and
+ * likewise for v, for every KV head h.  Negative slots are padding and are
+ * skipped.  Returns the number of tokens whose slot lies past the pool
+ * (those are skipped too).
+ */
+int64_t oracle_cache_write(const uint16_t* k, const uint16_t* v, const int64_t* slot_mapping,
+                           int64_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, uint16_t* k_cache, uint16_t* v_cache,
+                           int64_t num_blocks) {
+    int64_t out_of_range = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        int64_t blk = s / block_size;
+        int64_t off = s % block_size;
+        if (blk >= num_blocks) { ++out_of_range; continue; }
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            int64_t src = (t * num_kv_heads + h) * (int64_t)head_dim;
+            int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * (int64_t)head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                k_cache[dst + d] = k[src + d];
+                v_cache[dst + d] = v[src + d];
+            }
+        }
+    }
+    return out_of_range;
+}
+
+/* ---- gather ---- */
+
+/*
+ * Logical token t of a sequence lives in physical block table_row[t / bs] at
+ * row t % bs.  Writes the seq_len x head_dim values of KV head h, converted
+ * to fp64, to `dst` in token order.
+ */
+void oracle_gather(const uint16_t* cache, int dtype, const int32_t* table_row, int32_t seq_len,
+                   int32_t num_kv_heads, int32_t h, int32_t head_dim, int32_t block_size,
+                   double* dst) {
+    for (int32_t t = 0; t < seq_len; ++t) {
+        int64_t phys = table_row[t / block_size];
+        int64_t row = ((phys * num_kv_heads + h) * block_size + (t % block_size)) * (int64_t)head_dim;
+        for (int32_t d = 0; d < head_dim; ++d)
+            dst[(int64_t)t * head_dim + d] = to_double(cache[row + d], dtype);
+    }
+}
+
+/* ---- decode attention ---- */
+
+/*
+ * q:            [num_seqs][num_q_heads][head_dim] 16-bit patterns
+ * k/v_cache:    [num_blocks][num_kv_heads][block_size][head_dim]
+ * block_tables: [num_seqs][max_blocks]; only the first ceil(len/bs) entries
+ *               of a row are read
+ * seq_lens:     [num_seqs], tokens to attend over (the new one included)
+ * out:          [num_seqs][num_q_heads][head_dim] fp64
+ * A sequence of length 0 has an empty softmax; our reading defines its
+ * output as 0.
+ * Returns 0, or -1 if scratch memory could not be allocated.
+ */
+int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, int dtype,
+                  const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                  int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t block_size, double scale, double* out, int num_threads) {
+    const int32_t G = num_q_heads / num_kv_heads;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+    int64_t n_pairs = (int64_t)num_seqs * num_kv_heads;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t pair = 0; pair < n_pairs; ++pair) {
+        int32_t b = (int32_t)(pair / num_kv_heads);
+        int32_t h = (int32_t)(pair % num_kv_heads);
+        int32_t L = seq_lens[b];
+        if (L <= 0) {
+            for (int32_t g = 0; g < G; ++g) {
+                double* o = out + ((int64_t)b * num_q_heads + (int64_t)h * G + g) * head_dim;
+                for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+            }
+            continue;
+        }
+        double* K = (double*)malloc(sizeof(double) * (size_t)L * head_dim);
+        double* V = (double*)malloc(sizeof(double) * (size_t)L * head_dim);
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        if (!K || !V || !s || !qd) {
+            free(K); free(V); free(s); free(qd);
+            failed |= 1;
+            continue;
+        }
+        const int32_t* row = block_tables + (int64_t)b * max_blocks;
+        oracle_gather(k_cache, dtype, row, L, num_kv_heads, h, head_dim, block_size, K);
+        oracle_gather(v_cache, dtype, row, L, num_kv_heads, h, head_dim, block_size, V);
+        for (int32_t g = 0; g < G; ++g) {
+            int32_t i = h * G + g; /* query head i reads KV head i / G */
+            const uint16_t* qi = q + ((int64_t)b * num_q_heads + i) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) qd[d] = to_double(qi[d], dtype);
+            /* scores */
+            double smax = -INFINITY;
+            for (int32_t t = 0; t < L; ++t) {
+                double acc = 0.0;
+                for (int32_t d = 0; d < head_dim; ++d) acc += qd[d] * K[(int64_t)t * head_dim + d];
+                s[t] = scale * acc;
+                if (s[t] > smax) smax = s[t];
+            }
+            /* softmax weights */
+            double denom = 0.0;
+            for (int32_t t = 0; t < L; ++t) {
+                s[t] = exp(s[t] - smax);
+                denom += s[t];
+            }
+            /* weighted sum of values */
+            double* o = out + ((int64_t)b * num_q_heads + i) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                double acc = 0.0;
+                for (int32_t t = 0; t < L; ++t) acc += s[t] * V[(int64_t)t * head_dim + d];
+                o[d] = acc / denom;
+            }
+        }
+        free(K); free(V); free(s); free(qd);
+    }
+    return failed ? -1 : 0;
+}
+
+/* Threads the OpenMP runtime would use (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

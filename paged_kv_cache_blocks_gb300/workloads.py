@@ -1,0 +1,316 @@
+"""Seeded synthetic decode batches for paged KV-cache attention.
+
+This module only draws random numbers and lays them out: sequence lengths,
+a permutation of physical block ids, query/key/value values and the pool
+placement that a block table implies.  It holds no attention arithmetic and
+no allocator policy, and it imports neither the CUDA binding nor the oracle,
+so both sides can be fed from it.
+
+Workloads (all values ~N(0,1) drawn in fp32 and rounded to the storage type
+with round-to-nearest-even; block size 16):
+
+=============  =======================================================
+tiny           1 layer, 4 sequences of lengths {1,17,33,100}, 4 query /
+               2 KV heads, head_dim 64, fp16, scale 1/8, 24-block pool
+llama8b        Llama-3-8B-shaped layer: 32 q / 8 KV heads, head_dim 128,
+               bf16, 64 sequences with lengths U{128..2048}
+llama70b       Llama-3-70B-shaped layer: 64 q / 8 KV heads, head_dim 128,
+               bf16, 256 sequences: 90% of 300+U{1..100} tokens, 10% of
+               30000+U{1..4000} tokens (capped at 34000)
+long           32 q / 8 KV heads, head_dim 128, bf16, 8 sequences of
+               32768 tokens (long-context partitioned decode)
+fullstep       32 layers of the 8B shape, 128 sequences in 4 groups of 32;
+               each group shares a 1024-token prefix (64 full blocks);
+               lengths 1024+U{256..7168}
+=============  =======================================================
+
+Pools hold the needed blocks plus 25% (the tiny one holds 24 blocks); the
+physical id of each logical block comes from a seeded permutation.  One
+extra "poison" block pads the block tables past each sequence's last block.
+With ``poison=True`` every pool slot that holds no token (unused blocks,
+the poison block, tails of last blocks, and the slot the new token will be
+written to) is NaN, so a stray read shows up as NaN in the output.
+
+Draw order (one torch.Generator seeded from the workload seed): lengths,
+permutation, then per layer q, contiguous K, contiguous V, new k, new v.
+
+Each sequence of length L holds L-1 tokens in the pool before the step; the
+step writes the new token (position L-1) and attends over all L.
+"""
+from dataclasses import dataclass, field
+import math
+
+import numpy as np
+import torch
+
+BLOCK_SIZE = 16
+
+_NAN_BITS = {"f16": 0x7E00, "bf16": 0x7FC0}
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    dtype: str
+    num_layers: int
+    scale: float
+    description: str
+
+    @property
+    def group_size(self):
+        return self.num_q_heads // self.num_kv_heads
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 4, 4, 2, 64, "f16", 1, 1.0 / 8.0,
+                     "1 layer, 4 seqs lens {1,17,33,100}, 4q/2kv heads, d64, fp16, 24-block pool"),
+    "llama8b": Workload("llama8b", 64, 32, 8, 128, "bf16", 1, 1.0 / math.sqrt(128),
+                        "Llama-3-8B-shaped layer, 64 seqs lens U{128..2048}, 32q/8kv, d128, bf16"),
+    "llama70b": Workload("llama70b", 256, 64, 8, 128, "bf16", 1, 1.0 / math.sqrt(128),
+                         "Llama-3-70B-shaped layer, 256 seqs: 230 x ~400 + 26 x ~34000 tokens, "
+                         "64q/8kv, d128, bf16"),
+    "long": Workload("long", 8, 32, 8, 128, "bf16", 1, 1.0 / math.sqrt(128),
+                     "8 seqs x 32768 tokens, 32q/8kv, d128, bf16, 512-token partitions"),
+    "fullstep": Workload("fullstep", 128, 32, 8, 128, "bf16", 32, 1.0 / math.sqrt(128),
+                         "32 layers of the 8B shape, 128 seqs in 4 groups of 32 sharing a "
+                         "1024-token prefix, lens 1024+U{256..7168}"),
+}
+
+_SEED_SALT = {"tiny": 11, "llama8b": 22, "llama70b": 33, "long": 44, "fullstep": 55}
+PREFIX_TOKENS = 1024
+PREFIX_GROUPS = 4
+
+
+def _draw_lengths(w, g):
+    if w.name == "tiny":
+        return torch.tensor([1, 17, 33, 100], dtype=torch.int64)
+    if w.name == "llama8b":
+        return torch.randint(128, 2049, (w.num_seqs,), generator=g)
+    if w.name == "llama70b":
+        n_long = round(0.1 * w.num_seqs)
+        n_short = w.num_seqs - n_long
+        short = 300 + torch.randint(1, 101, (n_short,), generator=g)
+        long = torch.clamp(30000 + torch.randint(1, 4001, (n_long,), generator=g), max=34000)
+        lens = torch.cat([short, long])
+        return lens[torch.randperm(w.num_seqs, generator=g)]
+    if w.name == "long":
+        return torch.full((w.num_seqs,), 32768, dtype=torch.int64)
+    if w.name == "fullstep":
+        return PREFIX_TOKENS + torch.randint(256, 7169, (w.num_seqs,), generator=g)
+    raise KeyError(w.name)
+
+
+def _bits(x, dtype):
+    """fp32 tensor -> int16 tensor holding the RNE-rounded 16-bit patterns."""
+    return x.to(_TORCH_DTYPE[dtype]).view(torch.int16)
+
+
+@dataclass
+class Layer:
+    q: torch.Tensor          # int16 [B, Hq, D] bit patterns
+    k_cache: torch.Tensor    # int16 [NB, Hkv, 16, D], the L-1 past tokens placed
+    v_cache: torch.Tensor
+    new_k: torch.Tensor      # int16 [B, Hkv, D], token L-1 of each sequence
+    new_v: torch.Tensor
+    k_past: torch.Tensor = None  # int16 [rows, Hkv, D] contiguous draw (keep_contig only)
+    v_past: torch.Tensor = None
+
+
+@dataclass
+class Batch:
+    workload: Workload
+    seq_lens: np.ndarray         # int32 [B], new token included
+    block_tables: np.ndarray     # int32 [B, max_blocks], padded with poison_block
+    num_blocks: int
+    poison_block: int
+    slot_mapping: np.ndarray     # int64 [B], slot of token L-1
+    layers: list = field(default_factory=list)
+    num_unique_blocks: int = 0
+    # contiguous-draw bookkeeping (keep_contig only): per sequence, the list
+    # of (row_start, row_count) ranges of the past draw that form it, in order
+    past_ranges: list = None
+    seed: int = 0
+
+    # numpy views (host tensors only)
+    def np_layer(self, i):
+        L = self.layers[i]
+        f = lambda t: t.numpy().view(np.uint16)
+        return f(L.q), f(L.k_cache), f(L.v_cache), f(L.new_k), f(L.new_v)
+
+    def contiguous_kv(self, layer, b):
+        """Contiguous [L_b, Hkv, D] uint16 K and V of sequence b (keep_contig)."""
+        Lr = self.layers[layer]
+        ks = [Lr.k_past[s:s + n] for s, n in self.past_ranges[b]] + [Lr.new_k[b:b + 1]]
+        vs = [Lr.v_past[s:s + n] for s, n in self.past_ranges[b]] + [Lr.new_v[b:b + 1]]
+        f = lambda t: torch.cat(t).numpy().view(np.uint16)
+        return f(ks), f(vs)
+
+    def logical_kv_bytes(self):
+        """Sum over sequences of L x Hkv x D x 2 (K,V) x 2 bytes, per layer."""
+        w = self.workload
+        return int(self.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * 2
+
+    def unique_kv_bytes(self):
+        """KV bytes counting a shared physical block once (tails as stored)."""
+        w = self.workload
+        per_block_row = w.num_kv_heads * w.head_dim * 2 * 2
+        nb = (self.seq_lens.astype(np.int64) + BLOCK_SIZE - 1) // BLOCK_SIZE
+        if w.name != "fullstep":
+            return int(self.seq_lens.astype(np.int64).sum()) * per_block_row
+        shared_tokens = (PREFIX_GROUPS * (self.workload.num_seqs // PREFIX_GROUPS - 1)) * PREFIX_TOKENS
+        del nb
+        return (int(self.seq_lens.astype(np.int64).sum()) - shared_tokens) * per_block_row
+
+
+def make_batch(name, seed=0, poison=True, num_layers=None, keep_contig=False, device="cpu",
+               lens_override=None):
+    """Build one decode batch.  ``device='cuda'`` draws values on the GPU
+    (timing runs; not comparable bit-for-bit with a CPU draw)."""
+    w = WORKLOADS[name]
+    layers_n = w.num_layers if num_layers is None else num_layers
+    gseed = int(seed) * 1000 + _SEED_SALT[name]
+    g = torch.Generator(device="cpu")
+    g.manual_seed(gseed)
+    lens = _draw_lengths(w, g) if lens_override is None else torch.as_tensor(lens_override, dtype=torch.int64)
+    B = int(lens.numel())
+    if B != w.num_seqs and lens_override is None:
+        raise AssertionError
+    nblk = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
+
+    # --- logical block -> unique block index ---------------------------------
+    grouped = name == "fullstep" and lens_override is None
+    n_groups = PREFIX_GROUPS if grouped else 0
+    pre_blocks = PREFIX_TOKENS // BLOCK_SIZE if grouped else 0
+    group_of = (np.arange(B) * n_groups // B) if grouped else None
+    uniq = []  # per sequence: list of unique block indices
+    n_unique = 0
+    group_prefix_idx = {}
+    for b in range(B):
+        row = []
+        for j in range(int(nblk[b])):
+            if grouped and j < pre_blocks:
+                key = (int(group_of[b]), j)
+                if key not in group_prefix_idx:
+                    group_prefix_idx[key] = n_unique
+                    n_unique += 1
+                row.append(group_prefix_idx[key])
+            else:
+                row.append(n_unique)
+                n_unique += 1
+        uniq.append(row)
+    if name == "tiny" and lens_override is None:
+        pool = 24
+    else:
+        pool = max(int(math.ceil(1.25 * n_unique)), n_unique + 1)
+    perm = torch.randperm(pool, generator=g).numpy().astype(np.int32)
+    poison_block = int(perm[n_unique])
+    max_nb = max(1, int(nblk.max()) if B else 1)
+    tables = np.full((B, max_nb), poison_block, np.int32)
+    for b in range(B):
+        if uniq[b]:
+            tables[b, :len(uniq[b])] = perm[np.asarray(uniq[b], np.int64)]
+    lens_np = lens.numpy().astype(np.int32)
+    pos = lens_np.astype(np.int64) - 1
+    slot = np.where(pos >= 0, tables[np.arange(B), np.maximum(pos, 0) // BLOCK_SIZE].astype(np.int64)
+                    * BLOCK_SIZE + np.maximum(pos, 0) % BLOCK_SIZE, -1).astype(np.int64)
+
+    # --- placement of the past tokens (layout only) ------------------------------
+    # Draw rows: ungrouped -> each sequence's L-1 past tokens in sequence order;
+    # grouped -> per group: the shared prefix once, then each member's private part.
+    ranges = [None] * B
+    dst_blk, dst_off = [], []
+    row = 0
+
+    def place(b, t0, t1):
+        nonlocal row
+        t = np.arange(t0, t1, dtype=np.int64)
+        dst_blk.append(tables[b, t // BLOCK_SIZE].astype(np.int64))
+        dst_off.append(t % BLOCK_SIZE)
+        start = row
+        row += t1 - t0
+        return (start, t1 - t0)
+
+    if grouped:
+        for gi in range(n_groups):
+            members = [b for b in range(B) if group_of[b] == gi]
+            pr = place(members[0], 0, PREFIX_TOKENS)
+            for b in members:
+                ranges[b] = [pr]
+            for b in members:
+                ranges[b] = ranges[b] + [place(b, PREFIX_TOKENS, int(lens_np[b]) - 1)]
+    else:
+        for b in range(B):
+            ranges[b] = [place(b, 0, max(int(lens_np[b]) - 1, 0))]
+    dst_blk = np.concatenate(dst_blk) if dst_blk else np.zeros(0, np.int64)
+    dst_off = np.concatenate(dst_off) if dst_off else np.zeros(0, np.int64)
+    n_rows = row
+
+    H, Hq, D = w.num_kv_heads, w.num_q_heads, w.head_dim
+    dev = torch.device(device)
+    gv = g
+    if dev.type == "cuda":
+        gv = torch.Generator(device=dev)
+        gv.manual_seed(gseed + 7)
+    fill = _NAN_BITS[w.dtype] if poison else 0
+    fill_i16 = fill - 65536 if fill >= 32768 else fill
+    t_blk = torch.from_numpy(dst_blk).to(dev)
+    t_off = torch.from_numpy(dst_off).to(dev)
+    layers = []
+    for _ in range(layers_n):
+        q = _bits(torch.randn((B, Hq, D), generator=gv, device=dev), w.dtype)
+        k_past = _bits(torch.randn((n_rows, H, D), generator=gv, device=dev), w.dtype)
+        v_past = _bits(torch.randn((n_rows, H, D), generator=gv, device=dev), w.dtype)
+        new_k = _bits(torch.randn((B, H, D), generator=gv, device=dev), w.dtype)
+        new_v = _bits(torch.randn((B, H, D), generator=gv, device=dev), w.dtype)
+        kc = torch.full((pool, H, BLOCK_SIZE, D), fill_i16, dtype=torch.int16, device=dev)
+        vc = torch.full((pool, H, BLOCK_SIZE, D), fill_i16, dtype=torch.int16, device=dev)
+        if n_rows:
+            kc[t_blk, :, t_off, :] = k_past
+            vc[t_blk, :, t_off, :] = v_past
+        Lr = Layer(q, kc, vc, new_k, new_v)
+        if keep_contig:
+            Lr.k_past, Lr.v_past = k_past, v_past
+        else:
+            del k_past, v_past
+        layers.append(Lr)
+    return Batch(w, lens_np, tables, pool, poison_block, slot, layers, n_unique,
+                 ranges if keep_contig else None, seed)
+
+
+def place_new_tokens(batch, layer):
+    """Pool copies with each sequence's new token placed at its slot (layout
+    only; used to build decode-only inputs without running a cache write)."""
+    Lr = batch.layers[layer]
+    kc, vc = Lr.k_cache.clone(), Lr.v_cache.clone()
+    s = torch.from_numpy(batch.slot_mapping).to(kc.device)
+    ok = s >= 0
+    kc[s[ok] // BLOCK_SIZE, :, s[ok] % BLOCK_SIZE, :] = Lr.new_k[ok]
+    vc[s[ok] // BLOCK_SIZE, :, s[ok] % BLOCK_SIZE, :] = Lr.new_v[ok]
+    return kc, vc
+
+
+def relabel_blocks(batch, seed):
+    """Same logical contents under another physical placement: a seeded
+    permutation of the pool ids applied to tables, slots and pools."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(10_000 + int(seed))
+    sigma = torch.randperm(batch.num_blocks, generator=g).numpy().astype(np.int32)
+    new = Batch(batch.workload, batch.seq_lens.copy(), sigma[batch.block_tables],
+                batch.num_blocks, int(sigma[batch.poison_block]), None, [],
+                batch.num_unique_blocks, batch.past_ranges, batch.seed)
+    s = batch.slot_mapping
+    new.slot_mapping = np.where(s >= 0, sigma[np.maximum(s, 0) // BLOCK_SIZE].astype(np.int64)
+                                * BLOCK_SIZE + np.maximum(s, 0) % BLOCK_SIZE, -1)
+    inv = np.empty_like(sigma)
+    inv[sigma] = np.arange(batch.num_blocks, dtype=np.int32)
+    idx = torch.from_numpy(inv.astype(np.int64))
+    for Lr in batch.layers:
+        ix = idx.to(Lr.k_cache.device)
+        n = Layer(Lr.q, Lr.k_cache[ix], Lr.v_cache[ix], Lr.new_k, Lr.new_v, Lr.k_past, Lr.v_past)
+        new.layers.append(n)
+    return new

@@ -1,0 +1,218 @@
+"""Pins that hold the oracle to something other than itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle (the default
+build, or the variant passed as ``handle``) disagrees with what the pages or
+the mathematics fix:
+
+* worked numbers printed on the pages (tests/golden/*.json, each cited);
+* library routines the definition reduces to (numpy / torch float decoding,
+  ``torch.nn.functional.scaled_dot_product_attention`` in fp64 with the KV
+  heads repeated for grouped-query attention);
+* closed forms (one token, constant values, identical keys, one dominant key);
+* invariants (the gather returns the contiguous source exactly; relabelling
+  the physical blocks leaves the output bit-identical).
+
+test_oracle.py runs every pin on the oracle; test_oracle_mutants.py plants
+mistakes in copies of the oracle's source and checks that some pin fails.
+"""
+import json
+import os
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+from paged_kv_cache_blocks_gb300 import workloads as W
+
+GOLD = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def lib_f64(bits, dtype):
+    """fp64 values of 16-bit patterns via numpy (fp16) / torch (bf16)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    if dtype == "f16":
+        return bits.view(np.float16).astype(np.float64)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def sdpa_reference(batch, layer=0):
+    """Per-sequence attention by the library routine, fp64, GQA by repeat."""
+    w = batch.workload
+    G = w.group_size
+    q = lib_f64(batch.layers[layer].q.numpy().view(np.uint16), w.dtype)
+    out = np.zeros((len(batch.seq_lens), w.num_q_heads, w.head_dim))
+    for b, L in enumerate(batch.seq_lens):
+        if L == 0:
+            continue
+        kb, vb = batch.contiguous_kv(layer, b)
+        K = torch.from_numpy(lib_f64(kb, w.dtype)).permute(1, 0, 2)   # [Hkv, L, D]
+        V = torch.from_numpy(lib_f64(vb, w.dtype)).permute(1, 0, 2)
+        K = K.repeat_interleave(G, dim=0)
+        V = V.repeat_interleave(G, dim=0)
+        qb = torch.from_numpy(q[b]).unsqueeze(1)                       # [Hq, 1, D]
+        o = F.scaled_dot_product_attention(qb, K, V, scale=w.scale)
+        out[b] = o[:, 0, :].numpy()
+    return out
+
+
+def small_batches():
+    """Batches the oracle and the pins finish quickly on (several shapes)."""
+    return [
+        W.make_batch("tiny", seed=0, keep_contig=True),
+        W.make_batch("llama8b", seed=1, keep_contig=True, lens_override=[5, 16, 31, 200, 1]),
+        W.make_batch("llama70b", seed=2, keep_contig=True, lens_override=[48, 3, 130]),
+    ]
+
+
+def _decode(oracle, batch, handle, layer=0, pools=None):
+    w = batch.workload
+    q, _, _, _, _ = batch.np_layer(layer)
+    if pools is None:
+        kc, vc = W.place_new_tokens(batch, layer)
+    else:
+        kc, vc = pools
+    return oracle.decode(q, kc.numpy().view(np.uint16), vc.numpy().view(np.uint16),
+                         batch.block_tables, batch.seq_lens, w.scale, w.dtype, handle=handle)
+
+
+# ----------------------------------------------------------------------------------
+
+def pin_kv_bytes(oracle, handle=None):
+    g = json.load(open(os.path.join(GOLD, "kv_bytes.json")))
+    for c in g["per_token"]:
+        assert oracle.kv_bytes_per_token(c["layers"], c["kv_heads"], c["head_dim"], c["bytes"]) \
+            == c["expect"], c["cite"]
+    for c in g["per_context"]:
+        tot = oracle.kv_bytes_per_token(c["layers"], c["kv_heads"], c["head_dim"], c["bytes"]) \
+            * c["tokens"]
+        assert tot == c["expect_gib"] * 2 ** 30, c["cite"]
+
+
+def pin_bits(oracle, handle=None):
+    bits = np.arange(65536, dtype=np.uint16)
+    for dt in ("f16", "bf16"):
+        got = oracle.bits_to_double(bits, dt, handle=handle)
+        ref = lib_f64(bits, dt)
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan), dt
+        assert np.array_equal(got[~nan], ref[~nan]), dt
+        assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan])), dt
+
+
+def pin_cache_write_golden(oracle, handle=None):
+    g = json.load(open(os.path.join(GOLD, "cache_write_example.json")))
+    bs, nb, H, D = g["block_size"], g["num_blocks"], g["num_kv_heads"], g["head_dim"]
+    # small integers as fp16 patterns, so any misplaced copy is visible
+    f = lambda x: np.asarray(x, np.float16).view(np.uint16)
+    k, v = f(g["k"]), f(g["v"])
+    kc0 = np.full((nb, H, bs, D), 0xFFFF, np.uint16)
+    vc0 = kc0.copy()
+    kc, vc, bad = oracle.cache_write(k, v, np.asarray(g["slots"], np.int64), kc0, vc0, bs,
+                                     handle=handle)
+    assert bad == g["expect_out_of_range"]
+    ek, ev = kc0.copy(), vc0.copy()
+    for e in g["expect_written"]:
+        ek[e["block"], e["head"], e["row"]] = f(e["k"])
+        ev[e["block"], e["head"], e["row"]] = f(e["v"])
+    assert np.array_equal(kc, ek), g["cite"]
+    assert np.array_equal(vc, ev), g["cite"]
+
+
+def pin_gather_is_contiguous_source(oracle, handle=None):
+    for batch in small_batches():
+        w = batch.workload
+        kc, vc = W.place_new_tokens(batch, 0)
+        kc, vc = kc.numpy().view(np.uint16), vc.numpy().view(np.uint16)
+        for b, L in enumerate(batch.seq_lens):
+            kb, vb = batch.contiguous_kv(0, b)
+            for h in range(w.num_kv_heads):
+                gk = oracle.gather(kc, w.dtype, batch.block_tables[b], int(L), h, handle=handle)
+                gv = oracle.gather(vc, w.dtype, batch.block_tables[b], int(L), h, handle=handle)
+                assert np.array_equal(gk, lib_f64(kb[:, h, :], w.dtype)), (w.name, b, h)
+                assert np.array_equal(gv, lib_f64(vb[:, h, :], w.dtype)), (w.name, b, h)
+
+
+def pin_matches_sdpa(oracle, handle=None):
+    for batch in small_batches():
+        got = _decode(oracle, batch, handle)
+        ref = sdpa_reference(batch)
+        err = np.max(np.abs(got - ref))
+        assert err <= 1e-12, (batch.workload.name, err)
+
+
+def pin_relabel_invariance(oracle, handle=None):
+    for batch in small_batches():
+        a = _decode(oracle, batch, handle)
+        for s in (1, 2):
+            r = W.relabel_blocks(batch, s)
+            bb = _decode(oracle, r, handle)
+            assert np.array_equal(a, bb), (batch.workload.name, s)
+
+
+def _hand_pool(L, D, H, G, kvals, vvals, qvals, dtype="f16"):
+    """One sequence stored in blocks laid out in reverse physical order."""
+    bs = 16
+    nblk = max(1, -(-L // bs))
+    nb = nblk + 2
+    table = np.arange(nb - 1, nb - 1 - nblk, -1, dtype=np.int32)[None, :]
+    to_bits = (lambda x: np.asarray(x, np.float16).view(np.uint16)) if dtype == "f16" else \
+        (lambda x: torch.tensor(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16)
+         .numpy().view(np.uint16))
+    kc = np.zeros((nb, H, bs, D), np.uint16)
+    vc = np.zeros((nb, H, bs, D), np.uint16)
+    for t in range(L):
+        kc[table[0, t // bs], :, t % bs, :] = to_bits(kvals[t])
+        vc[table[0, t // bs], :, t % bs, :] = to_bits(vvals[t])
+    q = to_bits(qvals)[None]
+    return q, kc, vc, table, np.asarray([L], np.int32)
+
+
+def pin_closed_forms(oracle, handle=None):
+    rng = np.random.default_rng(5)
+    D, H, G = 8, 2, 2
+    Hq = H * G
+    scale = 0.25
+    for dt in ("f16", "bf16"):
+        # (1) one token: softmax of one score is 1, out = v
+        kv = rng.integers(-8, 8, (1, H, D)).astype(np.float64) / 4
+        vv = rng.integers(-8, 8, (1, H, D)).astype(np.float64) / 4
+        qv = rng.integers(-8, 8, (Hq, D)).astype(np.float64) / 4
+        q, kc, vc, t, ln = _hand_pool(1, D, H, G, kv, vv, qv, dt)
+        o = oracle.decode(q, kc, vc, t, ln, scale, dt, handle=handle)
+        for i in range(Hq):
+            assert np.array_equal(o[0, i], vv[0, i // G]), ("one token", dt)
+        # (2) constant values: out = that constant whatever the scores
+        L = 37
+        kv = rng.integers(-8, 8, (L, H, D)).astype(np.float64) / 4
+        vv = np.full((L, H, D), 0.75)
+        q, kc, vc, t, ln = _hand_pool(L, D, H, G, kv, vv, qv, dt)
+        o = oracle.decode(q, kc, vc, t, ln, scale, dt, handle=handle)
+        assert np.allclose(o, 0.75, rtol=0, atol=1e-14), ("constant V", dt)
+        # (3) identical keys: uniform weights, out = mean of V over tokens
+        kv = np.repeat(rng.integers(-8, 8, (1, H, D)).astype(np.float64) / 4, L, axis=0)
+        vv = rng.integers(-8, 8, (L, H, D)).astype(np.float64) / 4
+        q, kc, vc, t, ln = _hand_pool(L, D, H, G, kv, vv, qv, dt)
+        o = oracle.decode(q, kc, vc, t, ln, scale, dt, handle=handle)
+        for i in range(Hq):
+            assert np.allclose(o[0, i], vv[:, i // G].mean(axis=0), rtol=0, atol=1e-13), \
+                ("identical keys", dt)
+        # (4) one key whose score leads all others by >= 50: out = its value
+        j = 21
+        kv = np.zeros((L, H, D))
+        kv[j, :, 0] = 30.0
+        qv = np.zeros((Hq, D))
+        qv[:, 0] = 30.0   # score of key j: 900 * 0.25 = 225; others 0
+        vv = rng.integers(-8, 8, (L, H, D)).astype(np.float64) / 4
+        q, kc, vc, t, ln = _hand_pool(L, D, H, G, kv, vv, qv, dt)
+        o = oracle.decode(q, kc, vc, t, ln, scale, dt, handle=handle)
+        for i in range(Hq):
+            assert np.allclose(o[0, i], vv[j, i // G], rtol=0, atol=1e-12), ("dominant key", dt)
+    # (5) empty sequence: output defined as 0
+    q, kc, vc, t, _ = _hand_pool(1, D, H, G, np.ones((1, H, D)), np.ones((1, H, D)),
+                                 np.ones((Hq, D)))
+    o = oracle.decode(q, kc, vc, t, np.asarray([0], np.int32), scale, "f16", handle=handle)
+    assert np.array_equal(o, np.zeros_like(o))
+
+
+ALL_PINS = [pin_kv_bytes, pin_bits, pin_cache_write_golden, pin_gather_is_contiguous_source,
+            pin_matches_sdpa, pin_relabel_invariance, pin_closed_forms]

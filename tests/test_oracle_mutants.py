@@ -1,0 +1,48 @@
+"""Plant plausible mistakes in copies of the oracle and check a pin fails.
+
+Each mutant is the oracle's C source with one textual change (a dropped
+term, a wrong index, a swapped operand...), compiled on the CPU into a
+temporary directory.  The committed oracle is never modified.
+"""
+import os
+
+import pytest
+
+import oracle_pins as P
+
+MUTANTS = {
+    "gqa_head_mapping": ("int32_t i = h * G + g;", "int32_t i = g * num_kv_heads + h;"),
+    "scale_dropped": ("s[t] = scale * acc;", "s[t] = acc;"),
+    "normalisation_dropped": ("o[d] = acc / denom;", "o[d] = acc;"),
+    "exp_sign": ("s[t] = exp(s[t] - smax);", "s[t] = exp(smax - s[t]);"),
+    "pv_reads_keys": ("acc += s[t] * V[", "acc += s[t] * K["),
+    "query_head_index": ("q + ((int64_t)b * num_q_heads + i) * head_dim",
+                         "q + ((int64_t)b * num_q_heads + h) * head_dim"),
+    "gather_row_offset": ("(t % block_size)) * (int64_t)head_dim",
+                          "((t + 1) % block_size)) * (int64_t)head_dim"),
+    "gather_block_index": ("table_row[t / block_size]", "table_row[(t / block_size) / 2]"),
+    "bf16_exponent_bias": ("e - 134);", "e - 133);"),
+    "f16_subnormal_scale": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "write_v_from_k": ("v_cache[dst + d] = v[src + d];", "v_cache[dst + d] = k[src + d];"),
+    "write_row_reversed": ("* block_size + off) * (int64_t)head_dim",
+                           "* block_size + (block_size - 1 - off)) * (int64_t)head_dim"),
+    "negative_slot_written": ("if (s < 0) continue;", "if (s < 0) s = 0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_some_pin_catches_mutant(oracle_mod, tmp_path, name):
+    src = open(os.path.join(os.path.dirname(oracle_mod.__file__), "pa_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique in the oracle source"
+    mpath = tmp_path / f"mut_{name}.c"
+    mpath.write_text(src.replace(old, new))
+    lib = oracle_mod.compile_source(str(mpath), str(tmp_path / f"mut_{name}.so"))
+    handle = oracle_mod.OracleLib(lib)
+    caught = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(oracle_mod, handle=handle)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin detects mutant {name}"
