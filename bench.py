@@ -1,0 +1,500 @@
+"""Benchmark: one batched paged-decode step on GB300, printed as one JSON line.
+
+A step is the whole hot path over one batch: pa_cache_write of every
+sequence's new token into the paged cache, then pa_decode (partition list,
+attention over the 16-token blocks, merge of split sequences).  Default
+workload: the Llama-3-70B-shaped mixed-length layer (256 sequences, 90% of
+~350 tokens and 10% of ~32000, 64 query / 8 KV heads, head_dim 128, bf16).
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME]
+                    [--variant auto|fma|mma] [--impl pa|reference]
+
+* value      logical KV GB/s of the step (sum over sequences of
+             len x kv_heads x head_dim x 2 (K,V) x 2 bytes / step time),
+             inputs resident in HBM, CUDA events around exactly K steps.
+* e2e        the same metric through the public API from pinned host
+             buffers: host allocator (slots, table), H2D of q/k/v/slots/
+             table/lens, cache write, decode, D2H of the output, per step.
+* roofline   the attention kernel alone: algorithmic bytes / its average
+             CUDA-event duration vs the measured HBM copy bandwidth.
+* cpu_baseline  the fp64 CPU oracle on a bounded sample of the workload.
+--impl reference times only that oracle (the reference arm).
+Under torchrun every rank runs its own replica (weak scaling, no
+collective on the data path; a barrier and a max over ranks for timing).
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV GB/s and seqs·steps/s; % of GB300 HBM peak"
+DESCR = {
+    "llama70b": "Llama-3-70B-shaped mixed-length decode layer: 256 seqs (230 x 300+U{1..100}, "
+                "26 x 30000+U{1..4000} tokens), 64 q / 8 kv heads, head_dim 128, bf16, block 16",
+    "llama8b": "Llama-3-8B-shaped decode layer: 64 seqs U{128..2048} tokens, 32 q / 8 kv heads, "
+               "head_dim 128, bf16, block 16",
+    "long": "long-context decode: 8 seqs x 32768 tokens, 32 q / 8 kv heads, head_dim 128, bf16, "
+            "512-token partitions + merge",
+    "tiny": "tiny decode: 4 seqs {1,17,33,100}, 4 q / 2 kv heads, head_dim 64, fp16",
+}
+VARIANTS = {"auto": 0, "fma": 1, "mma": 2}
+
+
+# --------------------------------------------------------------------------- helpers
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def algorithmic_bytes(lens, hq, hkv, d, elem=2):
+    """Bytes the attention kernel must move: K/V of every token once per KV
+    head, block ids, q, and either the output (one partition) or the fp32
+    partial (max, sum, head_dim values) of every partition."""
+    L = np.asarray(lens, np.int64)
+    kv = int(L.sum()) * hkv * d * elem * 2
+    ids = int(((L + 15) // 16).sum()) * 4
+    q = len(L) * hq * d * elem
+    nparts = (L + 511) // 512
+    single = nparts == 1
+    out = int(single.sum()) * hq * d * elem
+    partial = int(nparts[~single].sum()) * hq * (d + 2) * 4
+    return kv + ids + q + out + partial
+
+
+def logical_kv_bytes(lens, hkv, d, elem=2):
+    return int(np.asarray(lens, np.int64).sum()) * hkv * d * elem * 2
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons), stamped on arrival."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        self.err = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.err = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.err}
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not win:
+            win = [p for (_, p) in self.samples]
+            note = "timed region shorter than the sampling period: samples around it"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        pw = [num(p[3]) for p in win if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(win), "note": note}
+
+
+def gpu_identity(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        items = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(items):
+            return items[local_rank]
+    return str(local_rank)
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_rows(lens, n_long):
+    """Rows of the workload keeping its short/long mix: n_long of the long
+    sequences and 9 x n_long of the short ones (all when the mix is flat)."""
+    lens = np.asarray(lens)
+    med = np.median(lens)
+    long_rows = np.flatnonzero(lens > 10 * med)
+    short_rows = np.flatnonzero(lens <= 10 * med)
+    if len(long_rows) == 0:
+        return short_rows[:max(1, n_long)]
+    return np.concatenate([long_rows[:n_long], short_rows[:9 * n_long]])
+
+
+def time_oracle(workload, rows, threads, seed=0):
+    import oracle
+    from paged_kv_cache_blocks_gb300 import workloads as W
+    lens = W.workload_lengths(workload, seed)[rows]
+    b = W.make_batch(workload, seed=seed, poison=False, lens_override=lens.tolist())
+    w = b.workload
+    kc, vc = W.place_new_tokens(b, 0)
+    q = b.layers[0].q.numpy().view(np.uint16)
+    kc, vc = kc.numpy().view(np.uint16), vc.numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.decode(q, kc, vc, b.block_tables, b.seq_lens, w.scale, w.dtype, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, lens, b
+
+
+def cpu_baseline(workload, budget_s=12.0):
+    import oracle
+    oracle.build()
+    from paged_kv_cache_blocks_gb300 import workloads as W
+    threads = len(os.sched_getaffinity(0))
+    w = W.WORKLOADS[workload]
+    lens_all = W.workload_lengths(workload, 0)
+    rows = oracle_sample_rows(lens_all, 1)
+    t1, lens, _ = time_oracle(workload, rows, threads)
+    n_long = 1
+    has_long = (np.asarray(lens_all) > 10 * np.median(lens_all)).any()
+    if has_long:
+        n_long = int(max(1, min(int((np.asarray(lens_all) > 10 * np.median(lens_all)).sum()),
+                                round(budget_s / max(t1, 1e-3)))))
+        rows = oracle_sample_rows(lens_all, n_long)
+        t1, lens, _ = time_oracle(workload, rows, threads)
+    kvb = logical_kv_bytes(lens, w.num_kv_heads, w.head_dim)
+    return {"value": kvb / t1 / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": t1, "seqs_steps_per_s": len(lens) / t1,
+            "sample": f"{len(lens)} of the {len(lens_all)} sequences of the same workload "
+                      f"({int((np.asarray(lens) > 10 * np.median(lens_all)).sum())} long, same "
+                      f"length draw), {int(np.sum(lens))} tokens, one decode step, fp64, "
+                      f"{threads} OpenMP threads; excludes input generation"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    from paged_kv_cache_blocks_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    threads = len(os.sched_getaffinity(0))
+    lens_all = W.workload_lengths(args.workload, 0)
+    per_step = min(12.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = oracle_sample_rows(lens_all, 1)
+    t1, lens, _ = time_oracle(args.workload, rows, threads)
+    if (np.asarray(lens_all) > 10 * np.median(lens_all)).any():
+        n_long = int(max(1, min(26, round(per_step / max(t1, 1e-3)))))
+        rows = oracle_sample_rows(lens_all, n_long)
+    import oracle as O
+    b = W.make_batch(args.workload, seed=0, poison=False,
+                     lens_override=np.asarray(lens_all)[rows].tolist())
+    kc, vc = W.place_new_tokens(b, 0)
+    q = b.layers[0].q.numpy().view(np.uint16)
+    kc, vc = kc.numpy().view(np.uint16), vc.numpy().view(np.uint16)
+    for _ in range(args.warmup):
+        O.decode(q, kc, vc, b.block_tables, b.seq_lens, w.scale, w.dtype, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.decode(q, kc, vc, b.block_tables, b.seq_lens, w.scale, w.dtype, threads=threads)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    kvb = logical_kv_bytes(b.seq_lens, w.num_kv_heads, w.head_dim)
+    val = kvb / dt / 1e9
+    sample = (f"{len(b.seq_lens)} of the {len(lens_all)} sequences of the workload "
+              f"({int(np.sum(b.seq_lens))} tokens) per step, fp64 oracle, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": DESCR.get(args.workload, args.workload),
+                                            "sample": sample},
+            "seqs_steps_per_s": len(b.seq_lens) / dt,
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_pa(args, rank, world, local_rank):
+    from paged_kv_cache_blocks_gb300 import build as pb
+    pb.build()
+    from paged_kv_cache_blocks_gb300 import binding as pa
+    from paged_kv_cache_blocks_gb300 import workloads as W
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    w = W.WORKLOADS[args.workload]
+    b = W.make_batch(args.workload, seed=rank, poison=False, device="cuda")
+    Lr = b.layers[0]
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
+    q, kc, vc = Lr.q.view(dt), Lr.k_cache.view(dt), Lr.v_cache.view(dt)
+    nk, nv = Lr.new_k.view(dt), Lr.new_v.view(dt)
+    tab = torch.from_numpy(b.block_tables).to(dev)
+    lens = torch.from_numpy(b.seq_lens).to(dev)
+    slots = torch.from_numpy(b.slot_mapping).to(dev)
+    mb = b.block_tables.shape[1]
+    msl = int(b.seq_lens.max())
+    ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    variant = VARIANTS[args.variant]
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        pa.pa_cache_write(nk, nv, slots, kc, vc)
+        pa.pa_decode(q, kc, vc, tab, lens, w.scale, max_seq_len=msl, out=out, workspace=ws,
+                     variant=variant, events=evs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bits = pa.pa_decode_check(ws)
+    if bits:
+        raise RuntimeError(f"device error bits {bits} during warm-up")
+
+    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_identity(local_rank)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(ev_pairs[i])
+    stop.record(stream)
+    barrier()
+    t_host1 = time.time()
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    ms_total = start.elapsed_time(stop)
+    kern_ms = [a.elapsed_time(z) for a, z in ev_pairs]
+    ms_step = ms_total / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    kvb = logical_kv_bytes(b.seq_lens, Hkv, D)
+    kv_gbs = kvb * world / (ms_step * 1e-3) / 1e9
+    alg = algorithmic_bytes(b.seq_lens, Hq, Hkv, D)
+    kern_avg = statistics.fmean(kern_ms)
+    peak, peak_kind = measured_peaks()
+    achieved = alg / (kern_avg * 1e-3) / 1e9
+
+    # ---- end to end through the public API, host buffers -------------------------
+    e2e = run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist)
+
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        try:
+            cpu = cpu_baseline(args.workload)
+        except Exception as ex:  # report, do not hide
+            cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle",
+                   "sample": f"failed: {ex!r}"}
+    traffic = load_traffic(args.workload, args.variant)
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    line = {
+        "metric": METRIC, "value": kv_gbs, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f16", "data": "synthetic",
+        "config": {"workload": DESCR.get(args.workload, args.workload),
+                   "num_seqs": B, "kv_tokens": int(b.seq_lens.sum()),
+                   "logical_kv_bytes_per_step": kvb,
+                   "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV per step vs 129 MB L2; "
+                         "no flush",
+                   "step": "pa_cache_write (one new token per sequence) + pa_decode",
+                   "variant": args.variant, "parallelism": f"replicas x{world}"},
+        "seqs_steps_per_s": B * world / (ms_step * 1e-3),
+        "hbm_frac_step": (kvb / (ms_step * 1e-3) / 1e9) / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "attend_kernel", "kernel_ms": kern_avg,
+                     "algorithmic_bytes": alg, "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def load_traffic(workload, variant):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    matches this kernel build (else null)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        ent = d.get(f"{workload}:{variant}")
+        return ent.get("dram_bytes_per_launch") if ent else None
+    except Exception:
+        return None
+
+
+def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
+    """Same step through the public API from pinned host memory."""
+    B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
+    steps = max(1, min(args.steps, args.e2e_steps))
+    total = steps + args.warmup
+    lens0 = b.seq_lens.astype(np.int64) - 1
+    mb = int(((lens0 + total + 15) // 16).max())
+    need = int(((lens0 + total + 15) // 16).sum())
+    nb = max(b.num_blocks, int(math.ceil(need * 1.05)))
+    order = np.random.default_rng(123).permutation(nb).astype(np.int32)
+    alloc = pa.Allocator(nb, order)
+    ids = np.array([alloc.seq_create() for _ in range(B)], np.int64)
+    table_h = torch.full((B, mb), -1, dtype=torch.int32).pin_memory()
+    lens_h = torch.zeros(B, dtype=torch.int32).pin_memory()
+    ids_c = ids.ctypes.data_as(__import__("ctypes").c_void_p)
+    scratch = np.empty(int(lens0.max()) + 1, np.int64)
+    for i in range(B):  # the tokens already in the cache
+        one = np.array([ids[i]], np.int64)
+        if lens0[i] > 0:
+            pa.lib().pa_seq_append_slots(alloc._h, one.ctypes.data, 1, int(lens0[i]),
+                                         scratch.ctypes.data, None, None, 0, None,
+                                         table_h[i:i + 1].numpy().ctypes.data, mb,
+                                         lens_h[i:i + 1].numpy().ctypes.data)
+    dtype_bytes = 2
+    g = torch.Generator().manual_seed(99)
+    q_h = torch.randn((B, Hq, D), generator=g).to(dt).pin_memory()
+    k_h = torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory()
+    v_h = torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory()
+    slots_h = torch.empty(B, dtype=torch.int64).pin_memory()
+    out_h = torch.empty((B, Hq, D), dtype=dt).pin_memory()
+    kc = torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev)
+    vc = torch.zeros_like(kc)
+    q_d, k_d, v_d = torch.empty_like(q_h, device=dev), torch.empty_like(k_h, device=dev), \
+        torch.empty_like(v_h, device=dev)
+    slots_d = torch.empty(B, dtype=torch.int64, device=dev)
+    table_d = torch.empty((B, mb), dtype=torch.int32, device=dev)
+    lens_d = torch.empty(B, dtype=torch.int32, device=dev)
+    out_d = torch.empty((B, Hq, D), dtype=dt, device=dev)
+    msl = mb * 16
+    ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
+    slots_np, table_np, lens_np = slots_h.numpy(), table_h.numpy(), lens_h.numpy()
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, slots_h, table_h, lens_h))
+    d2h = out_h.numel() * out_h.element_size()
+    kv_bytes = []
+
+    def one_step():
+        rc = pa.lib().pa_seq_append_slots(alloc._h, ids_c, B, 1, slots_np.ctypes.data, None, None,
+                                          0, None, table_np.ctypes.data, mb, lens_np.ctypes.data)
+        if rc != 0:
+            raise RuntimeError(pa.lib().pa_last_error_string().decode())
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        slots_d.copy_(slots_h, non_blocking=True)
+        table_d.copy_(table_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        pa.pa_cache_write(k_d, v_d, slots_d, kc, vc)
+        pa.pa_decode(q_d, kc, vc, table_d, lens_d, w.scale, max_seq_len=msl, out=out_d,
+                     workspace=ws, variant=variant)
+        out_h.copy_(out_d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        kv_bytes.append(int(lens_np.astype(np.int64).sum()) * Hkv * D * dtype_bytes * 2)
+
+    for _ in range(args.warmup):
+        one_step()
+    kv_bytes.clear()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one_step()
+    barrier()
+    sec = (time.perf_counter() - t0) / steps
+    if dist is not None:
+        t = torch.tensor([sec], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        sec = float(t.item())
+    alloc.close()
+    return {"value": statistics.fmean(kv_bytes) * world / sec / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": sec * 1e3,
+            "path": "host allocator append_slots -> H2D (pinned) q,k,v,slots,table,lens -> "
+                    "pa_cache_write -> pa_decode -> D2H out -> sync"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="llama70b", choices=sorted(DESCR))
+    ap.add_argument("--variant", default="auto", choices=sorted(VARIANTS))
+    ap.add_argument("--impl", default="pa", choices=["pa", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_pa(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,220 @@
+/*
+ * libpa -- paged KV-cache decode attention for GB300 (sm_103a), C ABI.
+ *
+ * The KV cache of every running sequence is cut into fixed blocks of 16
+ * tokens that need not be contiguous in memory; a per-sequence block table
+ * maps logical block j to a physical block id, the way a page table maps
+ * virtual pages to frames.  Sources:
+ *   [P3] "vLLM Nedir? PagedAttention ile Production LLM Serving",
+ *        sections "PagedAttention", "Bir istek motorun icinde",
+ *        "Asil sisen sey agirlik degil, KV cache";
+ *   [P4] "vLLM ve Triton ile maliyet optimizasyonu -- pratik karsilastirma",
+ *        section 03 ("Yontem"), steps 1-3, copy-on-write and the paragraph
+ *        on scaled dot-product attention;
+ *   [P1] "Yerel LLM sistemlerinde backpressure ve olcekleme", section
+ *        "KV butcesi" (grouped-query attention: 64 query heads, 8 KV heads).
+ *
+ * Conventions for every call:
+ *   - Every function returns a pa_status (0 = PA_OK).  No exception or abort
+ *     crosses the ABI.  After an error, pa_last_error_string() describes it
+ *     (per calling thread).
+ *   - The caller owns every device buffer, including the decode workspace
+ *     (sized by pa_decode_workspace_bytes).  The library owns only the host
+ *     allocator objects it creates.
+ *   - Device calls take a CUDA stream as `void* stream` (a cudaStream_t;
+ *     NULL = the legacy default stream), enqueue their kernels on it and
+ *     return without synchronising.  Pointers named d_* are device memory;
+ *     all others are host memory.
+ *   - Physical cache layout, per K and per V:
+ *       cache[num_blocks][num_kv_heads][16][head_dim]  (16-bit elements),
+ *     so one (block, KV head) tile of 16 x head_dim elements is contiguous.
+ *   - Element types: PA_F16 (IEEE binary16) or PA_BF16 (bfloat16) for q,
+ *     k, v, the caches and the output.  head_dim 64 or 128.  The number of
+ *     query heads per KV head (G = num_q_heads / num_kv_heads) is 1, 2, 4
+ *     or 8; query head i reads KV head i / G.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,      /* bad argument, shape, id or size */
+    PA_ERR_OOM = 2,          /* the allocator's free queue cannot cover the request */
+    PA_ERR_UNSUPPORTED = 3,  /* dtype / head_dim / group size this build has no kernel for */
+    PA_ERR_SHARED_WRITE = 4, /* reserved: write into a block held by several sequences */
+    PA_ERR_CUDA = 5,         /* a CUDA call failed (launch, tensor map, copy) */
+    PA_ERR_DEVICE = 6        /* a kernel flagged bad data (see pa_decode_check) */
+} pa_status;
+
+enum { PA_F16 = 0, PA_BF16 = 1 };
+enum { PA_BLOCK_SIZE = 16 };
+
+/* Device error bits reported by pa_decode_check. */
+enum {
+    PA_DEVERR_SEQ_LEN = 1,   /* a seq_len < 0 or > max_seq_len: clamped into range */
+    PA_DEVERR_BLOCK_ID = 2,  /* a block id outside [0, num_blocks): read as zeros */
+    PA_DEVERR_TIMEOUT = 4    /* an internal wait gave up; the output is not valid */
+};
+
+const char* pa_last_error_string(void);
+const char* pa_version(void);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator.  [P3] "PagedAttention" and "Bir istek motorun
+ * icinde" steps 2 (allocate_slots) and 5 (finished blocks go back to the
+ * free queue); [P4] section 03 step 3 (a block is taken only when the
+ * current one is full) and the copy-on-write paragraph; [P3] last
+ * paragraph of "PagedAttention" (shared blocks carry a reference count).
+ *
+ * Free queue: first in, first out.  Its initial order is `free_order` (a
+ * permutation of 0..num_blocks-1) or 0,1,2,... when NULL; freed blocks join
+ * the back in table order.  Sequence ids are 0,1,2,... and never reused.
+ * An allocator object is not thread-safe; use one per thread or lock.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_alloc pa_alloc_t;
+
+typedef struct {
+    int64_t num_blocks;
+    int64_t free_blocks;    /* in the free queue */
+    int64_t used_blocks;    /* reference count > 0 */
+    int64_t shared_blocks;  /* reference count > 1 */
+    int64_t refs;           /* sum of reference counts = table entries of live sequences */
+    int64_t seqs;           /* live sequences */
+    int64_t frag_tokens;    /* sum over live sequences of unfilled slots in their tables */
+} pa_stats_t;
+
+/* block_size must be 16.  *out receives the new allocator. */
+int pa_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order,
+                    pa_alloc_t** out);
+void pa_alloc_destroy(pa_alloc_t* a);
+
+/* New empty sequence. */
+int pa_seq_create(pa_alloc_t* a, int64_t* seq_id_out);
+
+/* New sequence sharing the blocks that hold the parent's first
+ * prefix_tokens tokens (0 <= prefix_tokens <= parent length); their
+ * reference counts go up.  If the last shared block is only partly covered,
+ * the first later write into it, by either holder, copies it (see
+ * pa_seq_append_slots). */
+int pa_seq_fork(pa_alloc_t* a, int64_t parent, int32_t prefix_tokens, int64_t* child_out);
+
+/* Drop a sequence: every block's count goes down; a block reaching 0 joins
+ * the free queue.  An unknown or already freed id is PA_ERR_INVALID. */
+int pa_seq_free(pa_alloc_t* a, int64_t seq_id);
+
+/* Reserve tokens_each new token slots for each of n_seqs distinct
+ * sequences, sequence by sequence.  Slot of a token = physical block id * 16
+ * + position % 16; a block is popped from the free queue when the position
+ * starts a new block.  Writing into a block held by several sequences first
+ * moves the writer onto a fresh block: the pair (source, destination) is
+ * reported so the caller copies the block's contents on the device before
+ * writing (cow_* arrays, capacity cow_capacity; *n_cow_out = pairs).
+ *
+ *   slot_mapping_out [n_seqs * tokens_each]  int64, sequence-major
+ *   block_table_io   [n_seqs][max_blocks]    optional (NULL): row i is
+ *                    updated in place with the entries that changed
+ *   seq_lens_io      [n_seqs]                optional (NULL): new lengths
+ *
+ * All or nothing: if the free queue cannot cover the call (new blocks plus
+ * copy targets), or cow_capacity or max_blocks is too small, nothing changes
+ * and PA_ERR_OOM / PA_ERR_INVALID is returned. */
+int pa_seq_append_slots(pa_alloc_t* a, const int64_t* seq_ids, int32_t n_seqs,
+                        int32_t tokens_each, int64_t* slot_mapping_out,
+                        int32_t* cow_src_out, int32_t* cow_dst_out, int32_t cow_capacity,
+                        int32_t* n_cow_out, int32_t* block_table_io, int32_t max_blocks,
+                        int32_t* seq_lens_io);
+
+/* Block table rows [n][max_blocks] (padding -1) and lengths of n sequences. */
+int pa_seq_block_table(pa_alloc_t* a, const int64_t* seq_ids, int32_t n, int32_t max_blocks,
+                       int32_t* table_out, int32_t* seq_lens_out);
+
+int pa_alloc_stats(pa_alloc_t* a, pa_stats_t* out);
+
+/* ------------------------------------------------------------------------
+ * Cache write.  [P3] "Bir istek motorun icinde" step 2; [P4] section 03
+ * steps 1-3: the new token's key and value rows go to the slot the
+ * allocator handed out.
+ *
+ *   d_k, d_v          [num_tokens][num_kv_heads][head_dim]
+ *   d_slot_mapping    [num_tokens] int64; slot s -> block s/16, row s%16.
+ *                     s < 0 is padding and writes nothing; a slot whose
+ *                     block is >= num_blocks writes nothing either.
+ *   d_k_cache, d_v_cache  [num_blocks][num_kv_heads][16][head_dim]
+ *
+ * Bit copy: the cached bytes equal the input bytes.  Two tokens with the
+ * same slot leave one of them (unspecified).  num_tokens == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+int pa_cache_write(const void* d_k, const void* d_v, const int64_t* d_slot_mapping,
+                   int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                   void* d_k_cache, void* d_v_cache, int64_t num_blocks, int32_t dtype,
+                   void* stream);
+
+/* ------------------------------------------------------------------------
+ * Decode attention.  [P4] section 03: the maths of scaled dot-product
+ * attention does not change under paging, only where K and V are read
+ * from; the kernel follows the block table to gather them.  For every
+ * sequence b and query head i (KV head h = i / G):
+ *
+ *   out[b][i] = sum_t softmax_t(scale * q[b][i] . K_b[t]) * V_b[t],
+ *   t = 0 .. seq_lens[b]-1, K_b[t] = k_cache[table[b][t/16]][h][t%16].
+ *
+ *   d_q              [num_seqs][num_q_heads][head_dim]
+ *   d_k_cache, d_v_cache  as for pa_cache_write (num_blocks blocks)
+ *   d_block_tables   [num_seqs][max_blocks_per_seq] int32; entries past a
+ *                    sequence's last block are never read
+ *   d_seq_lens       [num_seqs] int32, the new token included
+ *   max_seq_len      host-side bound on every seq_lens[b]; <= 0 means
+ *                    max_blocks_per_seq * 16.  It sizes the workspace.
+ *   d_out            [num_seqs][num_q_heads][head_dim]; seq_len 0 gives 0
+ *   d_workspace      >= pa_decode_workspace_bytes(...) bytes, 256-byte
+ *                    aligned, owned by the caller; its contents need no
+ *                    initialisation and are overwritten by every call, so
+ *                    calls sharing one workspace must not overlap in time.
+ *
+ * Accumulation is fp32 (online softmax over 16-token blocks; sequences
+ * longer than 512 tokens are split into 512-token partitions whose partial
+ * results a second kernel merges), with one rounding to the element type at
+ * the end.  Bad device data never faults: it is clamped or read as zeros
+ * and flagged in the workspace (pa_decode_check). */
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_seq_len);
+
+int pa_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,
+              const int32_t* d_block_tables, int32_t max_blocks_per_seq,
+              const int32_t* d_seq_lens, int32_t num_seqs, int32_t max_seq_len,
+              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+              int32_t dtype, void* d_out, void* d_workspace, size_t workspace_bytes,
+              void* stream);
+
+/* Options for pa_decode_ex.  Zero-initialised = the pa_decode behaviour. */
+typedef struct {
+    int32_t variant;         /* 0 auto, 1 CUDA-core FMA + warp shuffles, 2 tensor-core mma */
+    int32_t reserved0;
+    void* event_before_main; /* optional cudaEvent_t recorded just before the attention */
+    void* event_after_main;  /* kernel and just after it, on the same stream */
+    int64_t reserved[4];
+} pa_decode_opts;
+
+int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                 int64_t num_blocks, const int32_t* d_block_tables, int32_t max_blocks_per_seq,
+                 const int32_t* d_seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                 int32_t dtype, void* d_out, void* d_workspace, size_t workspace_bytes,
+                 void* stream, const pa_decode_opts* opts);
+
+/* Waits for `stream`, then reads the device error bits the last decode
+ * using this workspace left (PA_DEVERR_*; 0 = clean) into *error_bits.
+ * Returns PA_ERR_DEVICE when any bit is set. */
+int pa_decode_check(const void* d_workspace, void* stream, int32_t* error_bits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

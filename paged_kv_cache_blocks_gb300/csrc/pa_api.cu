@@ -1,0 +1,156 @@
+// C ABI of libpa: argument checks, error strings and dispatch to the kernels.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <string>
+
+#include "../../include/pa.h"
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+thread_local std::string g_last_error;
+}
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+}  // namespace pa
+
+namespace {
+
+int fail(int code, const std::string& msg) {
+  pa::set_error(msg);
+  return code;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_head_dim(int32_t d) { return d == 64 || d == 128; }
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_last_error_string(void) { return pa::g_last_error.c_str(); }
+
+const char* pa_version(void) { return "libpa 0.1 (sm_103a)"; }
+
+int pa_cache_write(const void* d_k, const void* d_v, const int64_t* d_slot_mapping, int32_t num_tokens,
+                   int32_t num_kv_heads, int32_t head_dim, void* d_k_cache, void* d_v_cache,
+                   int64_t num_blocks, int32_t dtype, void* stream) {
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "pa_cache_write: num_tokens < 0");
+  if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_cache_write: dtype");
+  if (!supported_head_dim(head_dim))
+    return fail(PA_ERR_UNSUPPORTED, "pa_cache_write: head_dim must be 64 or 128");
+  if (num_kv_heads <= 0 || num_blocks <= 0)
+    return fail(PA_ERR_INVALID, "pa_cache_write: num_kv_heads and num_blocks must be > 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!d_k || !d_v || !d_slot_mapping || !d_k_cache || !d_v_cache)
+    return fail(PA_ERR_INVALID, "pa_cache_write: NULL pointer");
+  if (!aligned(d_k, 16) || !aligned(d_v, 16) || !aligned(d_k_cache, 16) || !aligned(d_v_cache, 16) ||
+      !aligned(d_slot_mapping, 8))
+    return fail(PA_ERR_INVALID, "pa_cache_write: k, v and caches must be 16-byte aligned");
+  std::string why;
+  int rc = pa::cache_write_launch(d_k, d_v, d_slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                  d_k_cache, d_v_cache, num_blocks, stream, &why);
+  return rc ? fail(rc, why) : PA_OK;
+}
+
+size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_seq_len) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  return pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len);
+}
+
+int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,
+                 const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
+                 int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                 int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
+                 size_t workspace_bytes, void* stream, const pa_decode_opts* opts) {
+  if (num_seqs < 0) return fail(PA_ERR_INVALID, "pa_decode: num_seqs < 0");
+  if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype");
+  if (!supported_head_dim(head_dim))
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: head_dim must be 64 or 128");
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "pa_decode: num_q_heads must be a positive multiple of num_kv_heads");
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: query heads per KV head must be 1, 2, 4 or 8");
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID, "pa_decode: num_blocks and max_blocks_per_seq must be > 0");
+  if (num_blocks * num_kv_heads * PA_BLOCK_SIZE > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: num_blocks * num_kv_heads * 16 must be < 2^31");
+  if (static_cast<int64_t>(max_blocks_per_seq) * PA_BLOCK_SIZE > INT32_MAX)
+    return fail(PA_ERR_INVALID, "pa_decode: max_blocks_per_seq too large");
+  const int32_t cap = max_blocks_per_seq * PA_BLOCK_SIZE;
+  if (max_seq_len <= 0) max_seq_len = cap;
+  if (max_seq_len > cap)
+    return fail(PA_ERR_INVALID, "pa_decode: max_seq_len exceeds max_blocks_per_seq * 16");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_decode: scale is not finite");
+  if (opts && (opts->variant < 0 || opts->variant > 2))
+    return fail(PA_ERR_INVALID, "pa_decode: opts->variant must be 0, 1 or 2");
+  if (num_seqs == 0) return PA_OK;
+  const int64_t per_seq_parts = (max_seq_len + pa::kPartTokens - 1) / pa::kPartTokens;
+  if (static_cast<int64_t>(num_seqs) * per_seq_parts * num_kv_heads > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode: too many partitions for one call");
+  if (!d_q || !d_k_cache || !d_v_cache || !d_block_tables || !d_seq_lens || !d_out || !d_workspace)
+    return fail(PA_ERR_INVALID, "pa_decode: NULL pointer");
+  if (!aligned(d_k_cache, 16) || !aligned(d_v_cache, 16) || !aligned(d_q, 16) || !aligned(d_out, 16) ||
+      !aligned(d_workspace, 256) || !aligned(d_block_tables, 4) || !aligned(d_seq_lens, 4))
+    return fail(PA_ERR_INVALID,
+                "pa_decode: q, out and caches must be 16-byte aligned, the workspace 256-byte aligned");
+  const size_t need = pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len);
+  if (workspace_bytes < need)
+    return fail(PA_ERR_INVALID, "pa_decode: workspace smaller than pa_decode_workspace_bytes()");
+
+  pa::DecodeArgs a;
+  a.q = d_q;
+  a.k_cache = d_k_cache;
+  a.v_cache = d_v_cache;
+  a.num_blocks = num_blocks;
+  a.block_tables = d_block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.seq_lens = d_seq_lens;
+  a.num_seqs = num_seqs;
+  a.max_seq_len = max_seq_len;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.out = d_out;
+  a.workspace = d_workspace;
+  a.stream = stream;
+  a.variant = opts ? opts->variant : 0;
+  a.ev_before = opts ? opts->event_before_main : nullptr;
+  a.ev_after = opts ? opts->event_after_main : nullptr;
+  std::string why;
+  int rc = pa::decode_launch(a, &why);
+  return rc ? fail(rc, why) : PA_OK;
+}
+
+int pa_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,
+              const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
+              int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+              int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
+              size_t workspace_bytes, void* stream) {
+  return pa_decode_ex(d_q, d_k_cache, d_v_cache, num_blocks, d_block_tables, max_blocks_per_seq,
+                      d_seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, scale,
+                      dtype, d_out, d_workspace, workspace_bytes, stream, nullptr);
+}
+
+int pa_decode_check(const void* d_workspace, void* stream, int32_t* error_bits) {
+  if (!d_workspace || !error_bits) return fail(PA_ERR_INVALID, "pa_decode_check: NULL argument");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("pa_decode_check: ") + cudaGetErrorString(e));
+  int32_t bits = 0;
+  e = cudaMemcpy(&bits, d_workspace, sizeof(bits), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("pa_decode_check: ") + cudaGetErrorString(e));
+  *error_bits = bits;
+  if (bits) return fail(PA_ERR_DEVICE, "pa_decode_check: the device flagged bad input (see error bits)");
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Cache write for sm_103a: scatter each new token's K and V rows into the
+// paged cache through the slot mapping ("vLLM Nedir? PagedAttention ile
+// Production LLM Serving", section "Bir istek motorun icinde", step 2;
+// "vLLM ve Triton ile maliyet optimizasyonu", section 03, steps 1-3).
+//
+// One thread per 16-byte chunk of a (token, KV head) row; blockIdx.y picks K
+// or V.  Loads and stores are 16-byte vectors, consecutive threads touch
+// consecutive chunks of a row, so both sides are fully coalesced.  The work
+// is a few hundred KB per step, so the kernel is launch- and latency-bound.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+__global__ void __launch_bounds__(256)
+    cache_write_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                       const int64_t* __restrict__ slot_mapping, int64_t n_chunks, int chunks_per_token,
+                       int chunks_per_row, int hkv, uint4* __restrict__ k_cache,
+                       uint4* __restrict__ v_cache, int64_t num_blocks) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n_chunks) return;
+  const int64_t t = i / chunks_per_token;
+  const int rem = static_cast<int>(i - t * chunks_per_token);
+  const int h = rem / chunks_per_row;
+  const int c = rem - h * chunks_per_row;
+  const int64_t s = slot_mapping[t];
+  if (s < 0) return;                      // padding token
+  const int64_t blk = s / kBlock;
+  if (blk >= num_blocks) return;          // outside the pool: not written
+  const int64_t off = s - blk * kBlock;
+  const int64_t dst = ((blk * hkv + h) * kBlock + off) * chunks_per_row + c;
+  if (blockIdx.y == 0) {
+    k_cache[dst] = k[i];
+  } else {
+    v_cache[dst] = v[i];
+  }
+}
+
+int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
+                       int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
+                       int64_t num_blocks, void* stream, std::string* why) {
+  const int chunks_per_row = head_dim * 2 / 16;
+  const int chunks_per_token = chunks_per_row * num_kv_heads;
+  const int64_t n_chunks = static_cast<int64_t>(num_tokens) * chunks_per_token;
+  if (n_chunks == 0) return 0;
+  const int threads = 256;
+  const int64_t blocks = (n_chunks + threads - 1) / threads;
+  dim3 grid(static_cast<unsigned>(blocks), 2);
+  cache_write_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, n_chunks,
+      chunks_per_token, chunks_per_row, num_kv_heads, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), num_blocks);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("cache_write launch: ") + cudaGetErrorString(e);
+    return 5;
+  }
+  return 0;
+}
+
+}  // namespace pa

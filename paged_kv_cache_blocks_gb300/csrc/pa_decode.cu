@@ -1,0 +1,855 @@
+// Paged decode attention for sm_103a.
+//
+// What it computes ("vLLM ve Triton ile maliyet optimizasyonu", section 03):
+// scaled dot-product attention of each sequence's single new query against
+// its K/V, which the kernel gathers from scattered 16-token blocks by
+// following the block table.  Grouped-query attention ("Yerel LLM
+// sistemlerinde backpressure ve olcekleme", section "KV butcesi"): the G
+// query heads of one KV head are processed together, so every K/V tile is
+// read from HBM once per group, not once per query head.
+//
+// Three kernels per call, all on the caller's stream:
+//   1. prep   (1 CTA)    clamps lengths, cuts every sequence into 512-token
+//                        partitions, lists them (full partitions first) in
+//                        the workspace and resets the work counters;
+//   2. attend (persistent, one or two CTAs per SM)
+//                        one work item = (partition, KV head).  Warp 0 is the
+//                        producer: it takes items from an atomic counter,
+//                        reads the partition's block ids and streams each
+//                        block's K and V tiles into a ring of shared-memory
+//                        stages with TMA (128-byte swizzle), completion on
+//                        mbarriers.  The other warps consume blocks
+//                        round-robin, each keeping an online softmax (running
+//                        max and sum, fp32) for the G heads; at the end of an
+//                        item they merge their states through shared memory
+//                        and write either the final output (one partition)
+//                        or the partition's (max, sum, unnormalised output);
+//   3. merge  (persistent) combines the partitions of split sequences.
+//
+// Two math variants for the per-block QK^T / softmax / PV step, selected at
+// run time for the A/B measurement:
+//   FMA  CUDA-core fp32 FMAs; scores reduced and broadcast with warp shuffles;
+//   MMA  mma.sync m16n8k16 (16 tokens x 8 heads x 16 dims): S^T = K Q^T, then
+//        O^T += V^T P with P moved into operand layout by movmatrix.
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+struct ItemInfo {
+  int32_t b, h, p, len, nparts, nblk, g0, part;
+};
+
+struct DecodeParams {
+  const void* q;
+  void* out;
+  const int32_t* tables;
+  const int32_t* seq_lens;
+  WsHeader* ws;
+  PartInfo* parts;
+  int2* seq_first;
+  int32_t* split;
+  float2* ml;
+  float* acc;
+  int64_t num_blocks;
+  int32_t max_blocks;
+  int32_t num_seqs;
+  int32_t max_seq_len;
+  int32_t hq, hkv, G;
+  float scale_log2;
+};
+
+// ---------------------------------------------------------------------------
+// 1. prep
+
+__device__ __forceinline__ int clamp_len(const DecodeParams& P, int b) {
+  int L = P.seq_lens[b];
+  if (L < 0 || L > P.max_seq_len) {
+    atomicOr(&P.ws->error_bits, kErrSeqLen);
+    L = L < 0 ? 0 : P.max_seq_len;
+  }
+  return L;
+}
+
+// Exclusive scan over the 1024 threads of the block; *total = sum.
+__device__ int block_exclusive_scan(int v, int* sw, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sw[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nw ? sw[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    sw[lane] = t;
+  }
+  __syncthreads();
+  int res = (w ? sw[w - 1] : 0) + x - v;
+  *total = sw[nw - 1];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint4) {
+  __shared__ int sw[32];
+  __shared__ int s_total_full, s_nsplit;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    P.ws->error_bits = 0;
+    s_total_full = 0;
+    s_nsplit = 0;
+  }
+  __syncthreads();
+  // pass A: number of full partitions
+  int mine = 0;
+  for (int b = tid; b < P.num_seqs; b += blockDim.x) mine += clamp_len(P, b) / kPartTokens;
+  atomicAdd(&s_total_full, mine);
+  __syncthreads();
+  const int total_full = s_total_full;
+  // pass B: place partitions; full ones first, then the partial tails
+  int carry_full = 0, carry_tail = 0;
+  for (int base = 0; base < P.num_seqs; base += blockDim.x) {
+    const int b = base + tid;
+    int L = 0;
+    if (b < P.num_seqs) L = clamp_len(P, b);
+    const int nfull = L / kPartTokens;
+    const int tail = (L % kPartTokens) != 0;
+    int tot_f, tot_t;
+    const int fo = block_exclusive_scan(nfull, sw, &tot_f);
+    const int to = block_exclusive_scan(tail, sw, &tot_t);
+    if (b < P.num_seqs) {
+      const int nparts = nfull + tail;
+      const int first = carry_full + fo;
+      const int tail_idx = tail ? total_full + carry_tail + to : -1;
+      P.seq_first[b] = make_int2(first, tail_idx);
+      for (int p = 0; p < nfull; ++p) P.parts[first + p] = PartInfo{b, p, L, nparts};
+      if (tail) P.parts[tail_idx] = PartInfo{b, nfull, L, nparts};
+      if (nparts > 1) P.split[atomicAdd(&s_nsplit, 1)] = b;
+      if (L == 0) {  // empty softmax: the output is defined as 0
+        uint4* o = reinterpret_cast<uint4*>(P.out) + static_cast<int64_t>(b) * row_uint4;
+        for (int i = 0; i < row_uint4; ++i) o[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    carry_full += tot_f;
+    carry_tail += tot_t;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int n_parts = carry_full + carry_tail;
+    P.ws->n_parts = n_parts;
+    P.ws->n_items = n_parts * P.hkv;
+    P.ws->next_item = 0;
+    P.ws->n_split = s_nsplit;
+    P.ws->next_split = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. attend
+
+template <int D>
+struct Tile {
+  static constexpr int kHalfBytes = 16 * 64 * 2;             // one 16 x 64 box
+  static constexpr int kHalves = D / 64;                     // boxes per K (or V) tile
+  static constexpr int kKVBytes = kHalves * kHalfBytes;      // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kKVBytes;           // K then V
+};
+
+// Shared-memory address of 16-byte chunk c (0 .. D/8-1) of token row r.
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t tile, int r, int c) {
+  return tile + (c >> 3) * 2048 + swz128(r, c & 7);
+}
+
+template <int D, int NC>
+struct MergeSlot {
+  float acc[NC][8][D + 4];
+  float m[NC][8];
+  float l[NC][8];
+};
+
+// ---- MMA math ----------------------------------------------------------------
+
+template <typename T, int D>
+struct MmaState {
+  uint32_t qb[D / 16][2];
+  float m[2], l[2];
+  float o[D / 16][4];
+
+  __device__ __forceinline__ void begin(const DecodeParams& P, const ItemInfo& it, int lane, float*) {
+    const int g = lane >> 2, t = lane & 3;
+    const T* q = static_cast<const T*>(P.q) +
+                 (static_cast<int64_t>(it.b) * P.hq + it.h * P.G + g) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      if (g < P.G) {
+        qb[ks][0] = *reinterpret_cast<const uint32_t*>(q + 16 * ks + 2 * t);
+        qb[ks][1] = *reinterpret_cast<const uint32_t*>(q + 16 * ks + 2 * t + 8);
+      } else {
+        qb[ks][0] = qb[ks][1] = 0u;
+      }
+    }
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  }
+
+  __device__ __forceinline__ void block(uint32_t sK, uint32_t sV, int nvalid, float scale_log2,
+                                        int lane, float*) {
+    const int g = lane >> 2, t = lane & 3;
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // S^T[token][head] = sum_d K[token][d] Q[head][d]
+    {
+      const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int cofs = lane >> 4;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(a0, a1, a2, a3, chunk_addr(sK, r, 2 * ks + cofs));
+        Mma<T>::run(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      }
+    }
+    // s[0]: (token g, head 2t)  s[1]: (g, 2t+1)  s[2]: (g+8, 2t)  s[3]: (g+8, 2t+1)
+    const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
+    const float x0 = v0 ? s[0] * scale_log2 : -INFINITY;
+    const float x1 = v0 ? s[1] * scale_log2 : -INFINITY;
+    const float x2 = v1 ? s[2] * scale_log2 : -INFINITY;
+    const float x3 = v1 ? s[3] * scale_log2 : -INFINITY;
+    float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o2));
+      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o2));
+    }
+    const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);  // finite: nvalid >= 1
+    const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
+    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+    l[0] = l[0] * al0 + (p0 + p2);
+    l[1] = l[1] * al1 + (p1 + p3);
+    m[0] = mn0;
+    m[1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+    // P[token][head] (accumulator layout) -> B operand (token = k, head = n)
+    const uint32_t b0 = movmatrix_trans(pack2<T>(p0, p1));
+    const uint32_t b1 = movmatrix_trans(pack2<T>(p2, p3));
+    // Rows past the sequence end may hold anything (NaN included): zero them
+    // in the V operand so 0 * garbage cannot reach the sum.
+    uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+    if (nvalid < 16) {
+      mk0 = (2 * t < nvalid ? 0x0000ffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
+      mk1 = (2 * t + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+    {
+      const int r = (lane & 7) + (lane >> 4) * 8;
+      const int cofs = (lane >> 3) & 1;
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(a0, a1, a2, a3, chunk_addr(sV, r, 2 * mt + cofs));
+        Mma<T>::run(o[mt], a0 & mk0, a1 & mk0, a2 & mk1, a3 & mk1, b0, b1);
+      }
+    }
+  }
+
+  template <int NC>
+  __device__ __forceinline__ void store(MergeSlot<D, NC>& ms, int w, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float L0 = l[0], L1 = l[1];
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+      L0 += __shfl_xor_sync(0xffffffffu, L0, o2);
+      L1 += __shfl_xor_sync(0xffffffffu, L1, o2);
+    }
+    if (g == 0) {
+      ms.m[w][2 * t] = m[0];
+      ms.m[w][2 * t + 1] = m[1];
+      ms.l[w][2 * t] = L0;
+      ms.l[w][2 * t + 1] = L1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      ms.acc[w][2 * t][16 * mt + g] = o[mt][0];
+      ms.acc[w][2 * t + 1][16 * mt + g] = o[mt][1];
+      ms.acc[w][2 * t][16 * mt + g + 8] = o[mt][2];
+      ms.acc[w][2 * t + 1][16 * mt + g + 8] = o[mt][3];
+    }
+  }
+};
+
+// ---- FMA math ----------------------------------------------------------------
+// QK lanes: token = lane & 15, head half = lane >> 4 (HPG heads each).
+// PV lanes: 16-byte chunk c = lane % (D/8), head group = lane / (D/8).
+// Per-warp scratch (fp32): q[8][D] scaled by scale*log2(e), p[8][16], alpha[8].
+
+template <int D>
+struct FmaScratch {
+  static constexpr int kFloats = 8 * D + 8 * 16 + 8;
+};
+
+template <typename T, int D, int HPG>
+struct FmaState {
+  static constexpr int kChunks = D / 8;
+  static constexpr int kGroups = 32 / kChunks;                 // PV head groups
+  static constexpr int HPV = (HPG * 2 + kGroups - 1) / kGroups;  // PV heads per lane
+  float m[HPG], l[HPG];
+  float acc[HPV][8];
+  int G;
+
+  __device__ __forceinline__ void begin(const DecodeParams& P, const ItemInfo& it, int lane,
+                                        float* scr) {
+    G = P.G;
+    const T* q = static_cast<const T*>(P.q) + (static_cast<int64_t>(it.b) * P.hq + it.h * P.G) * D;
+    for (int e = lane; e < P.G * D; e += 32) scr[e] = to_float<T>(q[e]) * P.scale_log2;
+#pragma unroll
+    for (int j = 0; j < HPG; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < HPV; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+    __syncwarp();
+  }
+
+  __device__ __forceinline__ void block(uint32_t sK, uint32_t sV, int nvalid, float,
+                                        int lane, float* scr) {
+    float* qs = scr;
+    float* ps = scr + 8 * D;
+    float* as = ps + 8 * 16;
+    const int tok = lane & 15, hh = lane >> 4;
+    float s[HPG];
+#pragma unroll
+    for (int j = 0; j < HPG; ++j) s[j] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < kChunks; ++c) {
+      uint4 kv;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(kv.x), "=r"(kv.y), "=r"(kv.z), "=r"(kv.w)
+                   : "r"(chunk_addr(sK, tok, c)));
+      const float2 k0 = unpack2<T>(kv.x), k1 = unpack2<T>(kv.y);
+      const float2 k2 = unpack2<T>(kv.z), k3 = unpack2<T>(kv.w);
+#pragma unroll
+      for (int j = 0; j < HPG; ++j) {
+        const int head = hh * HPG + j;
+        if (head < G) {
+          const float4 qa = *reinterpret_cast<const float4*>(qs + head * D + 8 * c);
+          const float4 qc = *reinterpret_cast<const float4*>(qs + head * D + 8 * c + 4);
+          float a = s[j];
+          a = fmaf(qa.x, k0.x, a);
+          a = fmaf(qa.y, k0.y, a);
+          a = fmaf(qa.z, k1.x, a);
+          a = fmaf(qa.w, k1.y, a);
+          a = fmaf(qc.x, k2.x, a);
+          a = fmaf(qc.y, k2.y, a);
+          a = fmaf(qc.z, k3.x, a);
+          a = fmaf(qc.w, k3.y, a);
+          s[j] = a;
+        }
+      }
+    }
+    const bool valid = tok < nvalid;
+#pragma unroll
+    for (int j = 0; j < HPG; ++j) {
+      const int head = hh * HPG + j;
+      float x = valid ? s[j] : -INFINITY;
+      float bm = x;
+#pragma unroll
+      for (int o2 = 1; o2 < 16; o2 <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o2));
+      const float mn = fmaxf(m[j], bm);
+      const float al = exp2f(m[j] - mn);
+      const float p = exp2f(x - mn);
+      l[j] = l[j] * al + p;
+      m[j] = mn;
+      if (head < G) {
+        ps[head * 16 + tok] = p;
+        if (tok == 0) as[head] = al;
+      }
+    }
+    __syncwarp();
+    const int c = lane % kChunks, hg = lane / kChunks;
+#pragma unroll
+    for (int j = 0; j < HPV; ++j) {
+      const int head = hg * HPV + j;
+      if (head < G) {
+        const float al = as[head];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] *= al;
+      }
+    }
+    for (int r = 0; r < nvalid; ++r) {
+      uint4 vv;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(vv.x), "=r"(vv.y), "=r"(vv.z), "=r"(vv.w)
+                   : "r"(chunk_addr(sV, r, c)));
+      const float2 v0 = unpack2<T>(vv.x), v1 = unpack2<T>(vv.y);
+      const float2 v2 = unpack2<T>(vv.z), v3 = unpack2<T>(vv.w);
+#pragma unroll
+      for (int j = 0; j < HPV; ++j) {
+        const int head = hg * HPV + j;
+        if (head < G) {
+          const float p = ps[head * 16 + r];
+          acc[j][0] = fmaf(p, v0.x, acc[j][0]);
+          acc[j][1] = fmaf(p, v0.y, acc[j][1]);
+          acc[j][2] = fmaf(p, v1.x, acc[j][2]);
+          acc[j][3] = fmaf(p, v1.y, acc[j][3]);
+          acc[j][4] = fmaf(p, v2.x, acc[j][4]);
+          acc[j][5] = fmaf(p, v2.y, acc[j][5]);
+          acc[j][6] = fmaf(p, v3.x, acc[j][6]);
+          acc[j][7] = fmaf(p, v3.y, acc[j][7]);
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  template <int NC>
+  __device__ __forceinline__ void store(MergeSlot<D, NC>& ms, int w, int lane) {
+    const int tok = lane & 15, hh = lane >> 4;
+#pragma unroll
+    for (int j = 0; j < HPG; ++j) {
+      float L = l[j];
+#pragma unroll
+      for (int o2 = 1; o2 < 16; o2 <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+      const int head = hh * HPG + j;
+      if (tok == 0 && head < 8) {
+        ms.m[w][head] = head < G ? m[j] : -INFINITY;
+        ms.l[w][head] = head < G ? L : 0.f;
+      }
+    }
+    const int c = lane % kChunks, hg = lane / kChunks;
+#pragma unroll
+    for (int j = 0; j < HPV; ++j) {
+      const int head = hg * HPV + j;
+      if (head < G) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ms.acc[w][head][8 * c + e] = acc[j][e];
+      }
+    }
+  }
+};
+
+constexpr size_t align_up_c(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+template <typename T, int D, int NC, int S, bool kFma>
+struct AttendCfg {
+  static constexpr int kThreads = 32 * (NC + 1);
+  static constexpr int kStageBytes = Tile<D>::kStageBytes;
+  static constexpr size_t kStagesOff = 0;
+  static constexpr size_t kMergeOff = static_cast<size_t>(S) * kStageBytes;
+  static constexpr size_t kScrOff = kMergeOff + 2 * sizeof(MergeSlot<D, NC>);
+  static constexpr size_t kScrBytes = kFma ? NC * FmaScratch<D>::kFloats * sizeof(float) : 0;
+  static constexpr size_t kBarOff = align_up_c(kScrOff + kScrBytes, 16);
+  // full[S], empty[S], item_full[2], item_empty[2], merge_full[2]
+  static constexpr size_t kInfoOff = kBarOff + (2 * S + 6) * sizeof(uint64_t);
+  static constexpr size_t kIdsOff = kInfoOff + 2 * sizeof(ItemInfo);
+  static constexpr size_t kAbortOff = kIdsOff + 2 * 32 * sizeof(int32_t);
+  static constexpr size_t kBytes = kAbortOff + 16 + 1024;  // + slack to 1024-align the base
+};
+
+template <typename T, int D, int NC, int S, bool kFma, int HPG>
+__global__ void __launch_bounds__(32 * (NC + 1))
+    attend_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeParams P) {
+  using Cfg = AttendCfg<T, D, NC, S, kFma>;
+  using State = typename std::conditional<kFma, FmaState<T, D, HPG>, MmaState<T, D>>::type;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem + Cfg::kStagesOff;
+  MergeSlot<D, NC>* merge = reinterpret_cast<MergeSlot<D, NC>*>(smem + Cfg::kMergeOff);
+  float* scratch = reinterpret_cast<float*>(smem + Cfg::kScrOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
+  uint64_t* empty = full + S;
+  uint64_t* item_full = empty + S;
+  uint64_t* item_empty = item_full + 2;
+  uint64_t* merge_full = item_empty + 2;
+  ItemInfo* info = reinterpret_cast<ItemInfo*>(smem + Cfg::kInfoOff);
+  int32_t* ids = reinterpret_cast<int32_t*>(smem + Cfg::kIdsOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kAbortOff);
+  int* err = &P.ws->error_bits;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&item_full[s], 1);
+      mbar_init(&item_empty[s], NC);
+      mbar_init(&merge_full[s], NC);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    const int32_t n_items = *reinterpret_cast<volatile int32_t*>(&P.ws->n_items);
+    const int64_t y_oob = P.num_blocks * P.hkv * kBlock;  // one past the pool: reads as zeros
+    uint32_t g = 0;  // blocks issued by this CTA
+    bool ok = true;
+    for (uint32_t it = 0; ok; ++it) {
+      const int slot = it & 1;
+      int item = 0;
+      if (lane == 0) {
+        item = atomicAdd(&P.ws->next_item, 1);
+        ok = mbar_wait(&item_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, err);
+      }
+      item = __shfl_sync(0xffffffffu, item, 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (item >= n_items) {
+        if (lane == 0) {
+          info[slot].b = -1;
+          mbar_arrive(&item_full[slot]);
+        }
+        break;
+      }
+      const int part = item / P.hkv, h = item - part * P.hkv;
+      const PartInfo pi = P.parts[part];
+      const int first_tok = pi.p * kPartTokens;
+      const int nblk = min(kPartBlocks, (pi.len - first_tok + kBlock - 1) / kBlock);
+      if (lane < nblk) {
+        int32_t id = P.tables[static_cast<int64_t>(pi.b) * P.max_blocks + pi.p * kPartBlocks + lane];
+        if (id < 0 || id >= P.num_blocks) {
+          atomicOr(err, kErrBlockId);
+          id = -1;
+        }
+        ids[slot * 32 + lane] = id;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        info[slot] = ItemInfo{pi.b, h, pi.p, pi.len, pi.nparts, nblk, static_cast<int32_t>(g), part};
+        mbar_arrive(&item_full[slot]);
+        for (int j = 0; j < nblk && ok; ++j, ++g) {
+          const int st = g % S;
+          ok = mbar_wait(&empty[st], ((g / S) & 1) ^ 1, abort_flag, err);
+          if (!ok) break;
+          const int32_t id = ids[slot * 32 + j];
+          const int32_t y = static_cast<int32_t>(id < 0 ? y_oob : (static_cast<int64_t>(id) * P.hkv + h) * kBlock);
+          uint8_t* dst = stages + static_cast<size_t>(st) * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&full[st], Cfg::kStageBytes);
+#pragma unroll
+          for (int hf = 0; hf < Tile<D>::kHalves; ++hf) {
+            tma_load_2d(dst + hf * Tile<D>::kHalfBytes, &tm_k, hf * 64, y, &full[st]);
+            tma_load_2d(dst + Tile<D>::kKVBytes + hf * Tile<D>::kHalfBytes, &tm_v, hf * 64, y, &full[st]);
+          }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      g = __shfl_sync(0xffffffffu, g, 0);
+    }
+    if (!ok && lane == 0) {
+      // Abort: let the copies this CTA issued land before it exits.
+      const uint32_t lo = g > static_cast<uint32_t>(S) ? g - S : 0;
+      for (uint32_t k = lo; k < g; ++k) {
+        unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(&full[k % S], (k / S) & 1) &&
+               global_timer_ns() - t0 < kWaitLimitNs / 4) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  const int w = warp - 1;
+  float* scr = scratch + (kFma ? w * FmaScratch<D>::kFloats : 0);
+  State st;
+  for (uint32_t it = 0;; ++it) {
+    const int slot = it & 1;
+    bool ok = mbar_wait(&item_full[slot], (it >> 1) & 1, abort_flag, err);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const ItemInfo inf = info[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&item_empty[slot]);
+    if (inf.b < 0) break;
+
+    st.begin(P, inf, lane, scr);
+    bool alive = true;
+    for (int j = w; j < inf.nblk; j += NC) {
+      const uint32_t gg = inf.g0 + j;
+      const int s = gg % S;
+      ok = mbar_wait(&full[s], (gg / S) & 1, abort_flag, err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        alive = false;
+        break;
+      }
+      const uint32_t sK = smem_u32(stages + static_cast<size_t>(s) * Cfg::kStageBytes);
+      const int nvalid = min(kBlock, inf.len - (inf.p * kPartTokens + j * kBlock));
+      st.block(sK, sK + Tile<D>::kKVBytes, nvalid, P.scale_log2, lane, scr);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!alive) break;
+
+    MergeSlot<D, NC>& ms = merge[slot];
+    st.template store<NC>(ms, w, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&merge_full[slot]);
+    ok = mbar_wait(&merge_full[slot], (it >> 1) & 1, abort_flag, err);
+    if (!__all_sync(0xffffffffu, ok)) break;
+
+    // Combine the NC warp states; this thread's share of the G*D outputs.
+    const int G = P.G;
+    const int head0 = inf.h * G;
+    const bool single = inf.nparts == 1;
+    for (int e = w * 32 + lane; e < G * D; e += NC * 32) {
+      const int hd = e / D, d = e - hd * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < NC; ++k) M = fmaxf(M, ms.m[k][hd]);
+      float Lsum = 0.f, O = 0.f;
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        const float wk = exp2f(ms.m[k][hd] - M);
+        Lsum = fmaf(ms.l[k][hd], wk, Lsum);
+        O = fmaf(ms.acc[k][hd][d], wk, O);
+      }
+      const int64_t row = static_cast<int64_t>(inf.b) * P.hq + head0 + hd;
+      if (single) {
+        static_cast<T*>(P.out)[row * D + d] = from_float<T>(O / Lsum);
+      } else {
+        const int64_t prow = static_cast<int64_t>(inf.part) * P.hq + head0 + hd;
+        P.acc[prow * D + d] = O;
+        if (d == 0) P.ml[prow] = make_float2(M, Lsum);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. merge of split sequences
+
+template <typename T, int D>
+__global__ void __launch_bounds__(D) merge_kernel(const DecodeParams P) {
+  const int n_work = *reinterpret_cast<volatile int32_t*>(&P.ws->n_split) * P.hq;
+  const int d = threadIdx.x;
+  for (int wi = blockIdx.x; wi < n_work; wi += gridDim.x) {
+    const int b = P.split[wi / P.hq];
+    const int i = wi - (wi / P.hq) * P.hq;
+    const int2 sf = P.seq_first[b];
+    const int L = clamp_len(P, b);
+    const int nfull = L / kPartTokens;
+    const int nparts = nfull + ((L % kPartTokens) != 0);
+    float M = -INFINITY;
+    for (int p = 0; p < nparts; ++p) {
+      const int idx = p < nfull ? sf.x + p : sf.y;
+      M = fmaxf(M, P.ml[static_cast<int64_t>(idx) * P.hq + i].x);
+    }
+    float Lsum = 0.f, O = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+      const int idx = p < nfull ? sf.x + p : sf.y;
+      const int64_t prow = static_cast<int64_t>(idx) * P.hq + i;
+      const float2 ml = P.ml[prow];
+      const float wgt = exp2f(ml.x - M);
+      Lsum = fmaf(ml.y, wgt, Lsum);
+      O = fmaf(P.acc[prow * D + d], wgt, O);
+    }
+    static_cast<T*>(P.out)[(static_cast<int64_t>(b) * P.hq + i) * D + d] = from_float<T>(O / Lsum);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn(std::string* why) {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  if (!fn && why) *why = "cuTensorMapEncodeTiled is not available from the driver";
+  return fn;
+}
+
+bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D,
+                      std::string* why) {
+  EncodeTiledFn fn = get_encode_fn(why);
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(D),
+                        static_cast<cuuint64_t>(num_blocks) * hkv * kBlock};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlock)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (why) *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+struct LaunchShape {
+  int grid;
+  size_t smem;
+};
+
+template <typename T, int D, int NC, int S, bool kFma, int HPG>
+bool launch_attend(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& P,
+                   int64_t max_items, cudaStream_t stream, std::string* why) {
+  using Cfg = AttendCfg<T, D, NC, S, kFma>;
+  auto kern = attend_kernel<T, D, NC, S, kFma, HPG>;
+  static int occ_cache[64] = {0};  // per device ordinal
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int slot = dev & 63;
+  if (occ_cache[slot] == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kBytes));
+    if (e != cudaSuccess) {
+      *why = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e);
+      return false;
+    }
+    int per_sm = 0, sms = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg::kThreads, Cfg::kBytes);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (per_sm < 1) per_sm = 1;
+    occ_cache[slot] = per_sm * sms;
+  }
+  int64_t grid = occ_cache[slot];
+  if (grid > max_items) grid = max_items;
+  if (grid < 1) grid = 1;
+  kern<<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kBytes, stream>>>(tk, tv, P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("attend launch: ") + cudaGetErrorString(e);
+    return false;
+  }
+  return true;
+}
+
+template <typename T, int D>
+bool dispatch_attend(int variant, int G, const CUtensorMap& tk, const CUtensorMap& tv,
+                     const DecodeParams& P, int64_t max_items, cudaStream_t s, std::string* why) {
+  constexpr int NC = 4;
+  if (variant == 1) {
+    constexpr int S = 6;
+    if (G <= 2) return launch_attend<T, D, NC, S, true, 1>(tk, tv, P, max_items, s, why);
+    if (G <= 4) return launch_attend<T, D, NC, S, true, 2>(tk, tv, P, max_items, s, why);
+    return launch_attend<T, D, NC, S, true, 4>(tk, tv, P, max_items, s, why);
+  }
+  constexpr int S = 8;
+  return launch_attend<T, D, NC, S, false, 1>(tk, tv, P, max_items, s, why);
+}
+
+}  // namespace
+
+int decode_launch(const DecodeArgs& a, std::string* why) {
+  const WsLayout L = ws_layout(a.num_seqs, a.num_q_heads, a.head_dim, a.max_seq_len);
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  DecodeParams P;
+  P.q = a.q;
+  P.out = a.out;
+  P.tables = a.block_tables;
+  P.seq_lens = a.seq_lens;
+  P.ws = reinterpret_cast<WsHeader*>(ws);
+  P.parts = reinterpret_cast<PartInfo*>(ws + L.off_parts);
+  P.seq_first = reinterpret_cast<int2*>(ws + L.off_seq_first);
+  P.split = reinterpret_cast<int32_t*>(ws + L.off_split);
+  P.ml = reinterpret_cast<float2*>(ws + L.off_ml);
+  P.acc = reinterpret_cast<float*>(ws + L.off_acc);
+  P.num_blocks = a.num_blocks;
+  P.max_blocks = a.max_blocks_per_seq;
+  P.num_seqs = a.num_seqs;
+  P.max_seq_len = a.max_seq_len;
+  P.hq = a.num_q_heads;
+  P.hkv = a.num_kv_heads;
+  P.G = a.num_q_heads / a.num_kv_heads;
+  P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+
+  CUtensorMap tk, tv;
+  if (!encode_cache_map(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why) ||
+      !encode_cache_map(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why))
+    return 5;
+
+  cudaStream_t s = static_cast<cudaStream_t>(a.stream);
+  const int row_uint4 = a.num_q_heads * a.head_dim * 2 / 16;
+  prep_kernel<<<1, 1024, 0, s>>>(P, row_uint4);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("prep launch: ") + cudaGetErrorString(e);
+    return 5;
+  }
+  if (a.ev_before) cudaEventRecord(static_cast<cudaEvent_t>(a.ev_before), s);
+  const int64_t max_items = L.max_parts * a.num_kv_heads;
+  const int variant = a.variant == 0 ? 2 : a.variant;
+  bool ok;
+  if (a.dtype == 1) {
+    ok = a.head_dim == 128
+             ? dispatch_attend<__nv_bfloat16, 128>(variant, P.G, tk, tv, P, max_items, s, why)
+             : dispatch_attend<__nv_bfloat16, 64>(variant, P.G, tk, tv, P, max_items, s, why);
+  } else {
+    ok = a.head_dim == 128 ? dispatch_attend<__half, 128>(variant, P.G, tk, tv, P, max_items, s, why)
+                           : dispatch_attend<__half, 64>(variant, P.G, tk, tv, P, max_items, s, why);
+  }
+  if (!ok) return 5;
+  if (a.ev_after) cudaEventRecord(static_cast<cudaEvent_t>(a.ev_after), s);
+
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  if (mgrid > 4 * sms) mgrid = 4 * sms;
+  if (mgrid < 1) mgrid = 1;
+  if (a.dtype == 1) {
+    if (a.head_dim == 128) merge_kernel<__nv_bfloat16, 128><<<static_cast<unsigned>(mgrid), 128, 0, s>>>(P);
+    else merge_kernel<__nv_bfloat16, 64><<<static_cast<unsigned>(mgrid), 64, 0, s>>>(P);
+  } else {
+    if (a.head_dim == 128) merge_kernel<__half, 128><<<static_cast<unsigned>(mgrid), 128, 0, s>>>(P);
+    else merge_kernel<__half, 64><<<static_cast<unsigned>(mgrid), 64, 0, s>>>(P);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("merge launch: ") + cudaGetErrorString(e);
+    return 5;
+  }
+  return 0;
+}
+
+size_t decode_workspace_bytes(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
+                              int64_t max_seq_len) {
+  return ws_layout(num_seqs, num_q_heads, head_dim, max_seq_len).total;
+}
+
+}  // namespace pa

@@ -1,0 +1,46 @@
+// Internal host-side interfaces between the C ABI layer and the kernels.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace pa {
+
+// Sets the calling thread's message for pa_last_error_string().
+void set_error(const std::string& msg);
+
+struct DecodeArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  int64_t num_blocks;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* seq_lens;
+  int32_t num_seqs;
+  int32_t max_seq_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  float scale;
+  int32_t dtype;
+  void* out;
+  void* workspace;
+  void* stream;
+  int32_t variant;
+  void* ev_before;
+  void* ev_after;
+};
+
+// Both return 0 on success or a pa_status code, with *why set on failure.
+int decode_launch(const DecodeArgs& a, std::string* why);
+size_t decode_workspace_bytes(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
+                              int64_t max_seq_len);
+
+int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
+                       int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
+                       int64_t num_blocks, void* stream, std::string* why);
+
+}  // namespace pa

@@ -105,6 +105,13 @@ def _draw_lengths(w, g):
     raise KeyError(w.name)
 
 
+def workload_lengths(name, seed=0):
+    """The sequence lengths make_batch(name, seed) draws (int64 numpy)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) * 1000 + _SEED_SALT[name])
+    return _draw_lengths(WORKLOADS[name], g).numpy()
+
+
 def _bits(x, dtype):
     """fp32 tensor -> int16 tensor holding the RNE-rounded 16-bit patterns."""
     return x.to(_TORCH_DTYPE[dtype]).view(torch.int16)

@@ -1,0 +1,119 @@
+"""pa_decode on the GPU against the fp64 oracle, through the C ABI.
+
+Every workload of the workload table is covered: the small ones on every
+output, the 70B-shaped batch and the 32-layer step on sampled sequences the
+oracle computes one by one, both math variants.  Pools are NaN-poisoned
+wherever no token lives, so a stray read shows up as a non-finite output."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as U
+from paged_kv_cache_blocks_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+VARIANTS = [1, 2]   # 1 = CUDA-core FMA, 2 = tensor-core mma
+
+
+@pytest.fixture(scope="module")
+def pa():
+    return U.require_gpu()
+
+
+def run(pa, b, layer=0, variant=0, **kw):
+    q, kc, vc, tab, lens = U.device_inputs(b, layer)
+    out = pa.pa_decode(q, kc, vc, tab, lens, b.workload.scale, variant=variant, **kw)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "long"])
+def test_full_parity(pa, name, variant):
+    b = U.batch(name)
+    got = run(pa, b, variant=variant)
+    U.assert_close(got, U.oracle_out(b), f"{name} v{variant}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_llama70b_mixed_sampled(pa, variant):
+    b = U.batch("llama70b")
+    got = run(pa, b, variant=variant)
+    assert np.isfinite(got).all()
+    lens = b.seq_lens
+    long_rows = np.flatnonzero(lens > 20000)[:5]
+    short_rows = np.flatnonzero(lens < 1000)[::23]
+    rows = np.concatenate([long_rows, short_rows])
+    U.assert_close(got[rows], U.oracle_out(b, rows=rows), f"llama70b v{variant}")
+
+
+def test_fullstep_two_layers_write_then_decode(pa):
+    """Shared-prefix batch (4 groups x 32 sequences on one 1024-token prefix):
+    cache write of the new token, then decode, per layer."""
+    b = U.batch("fullstep", num_layers=2)
+    w = b.workload
+    rows = np.array([0, 1, 31, 32, 63, 64, 96, 127])
+    slots = torch.from_numpy(b.slot_mapping).cuda()
+    tab = torch.from_numpy(b.block_tables).cuda()
+    lens = torch.from_numpy(b.seq_lens).cuda()
+    for layer in range(2):
+        Lr = b.layers[layer]
+        kc, vc = U.to_dev(Lr.k_cache, w.dtype).clone(), U.to_dev(Lr.v_cache, w.dtype).clone()
+        pa.pa_cache_write(U.to_dev(Lr.new_k, w.dtype), U.to_dev(Lr.new_v, w.dtype), slots, kc, vc)
+        out = pa.pa_decode(U.to_dev(Lr.q, w.dtype), kc, vc, tab, lens, w.scale)
+        got = out.double().cpu().numpy()
+        assert np.isfinite(got).all()
+        U.assert_close(got[rows], U.oracle_out(b, layer, rows=rows), f"fullstep layer {layer}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama8b"])
+def test_relabelled_blocks_give_identical_output(pa, name):
+    b = U.batch(name)
+    a = run(pa, b)
+    r = W.relabel_blocks(b, 7)
+    assert np.array_equal(a, run(pa, r))
+
+
+EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1023, 1024, 1025, 1537, 2048, 3]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["tiny", "llama70b", "llama8b"])
+def test_edge_lengths(pa, name, variant):
+    b = U.batch(name, seed=5, lens=tuple(EDGE_LENS))
+    U.assert_close(run(pa, b, variant=variant), U.oracle_out(b), f"edges {name} v{variant}")
+
+
+def test_empty_sequences_give_zeros(pa):
+    b = U.batch("llama8b", seed=6, lens=(0, 5, 0, 600))
+    got = run(pa, b)
+    assert np.array_equal(got[[0, 2]], np.zeros_like(got[[0, 2]]))
+    U.assert_close(got[[1, 3]], U.oracle_out(b, rows=[1, 3]), "empty")
+
+
+def test_device_error_flags_without_fault(pa):
+    """A length past max_seq_len is clamped and flagged; a block id outside
+    the pool reads zeros and is flagged; the other sequences stay right."""
+    b = U.batch("llama8b", seed=7, lens=(40, 100, 60))
+    q, kc, vc, tab, lens = U.device_inputs(b)
+    ws = torch.empty(pa.pa_decode_workspace_bytes(3, q.shape[1], q.shape[2], 64),
+                     dtype=torch.uint8, device="cuda")
+    out = pa.pa_decode(q, kc, vc, tab, lens, b.workload.scale, max_seq_len=64, workspace=ws)
+    bits = pa.pa_decode_check(ws)
+    assert bits & pa.PA_DEVERR_SEQ_LEN
+    got = out.double().cpu().numpy()
+    U.assert_close(got[[0, 2]], U.oracle_out(b, rows=[0, 2]), "clamped neighbour")
+    tab2 = tab.clone()
+    tab2[1, 2] = b.num_blocks + 5
+    out = pa.pa_decode(q, kc, vc, tab2, lens, b.workload.scale, workspace=ws)
+    assert pa.pa_decode_check(ws) & pa.PA_DEVERR_BLOCK_ID
+    got = out.double().cpu().numpy()
+    U.assert_close(got[[0, 2]], U.oracle_out(b, rows=[0, 2]), "bad-id neighbour")
+    out = pa.pa_decode(q, kc, vc, tab, lens, b.workload.scale, workspace=ws)
+    assert pa.pa_decode_check(ws) == 0
+
+
+def test_variants_agree_closely(pa):
+    b = U.batch("llama8b")
+    a, c = run(pa, b, variant=1), run(pa, b, variant=2)
+    assert np.max(np.abs(a - c)) <= 1e-2

@@ -1,0 +1,81 @@
+"""libpa loads, exports every symbol include/pa.h declares, and rejects bad
+arguments with status codes (host-side checks only: no kernel runs here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from paged_kv_cache_blocks_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version(L):
+    assert b"sm_103a" in L.pa_version()
+
+
+def _decode_args(**kw):
+    from paged_kv_cache_blocks_gb300 import binding as b
+    a = dict(q=1 << 20, k=1 << 20, v=1 << 20, nb=100, tab=1 << 20, mb=8, lens=1 << 20, B=4,
+             msl=0, hq=8, hkv=2, d=128, scale=0.1, dtype=b.PA_BF16, out=1 << 20, ws=1 << 20,
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return (P(a["q"]), P(a["k"]), P(a["v"]), a["nb"], P(a["tab"]), a["mb"], P(a["lens"]), a["B"],
+            a["msl"], a["hq"], a["hkv"], a["d"], a["scale"], a["dtype"], P(a["out"]), P(a["ws"]),
+            a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(d=96), 3), (dict(dtype=7), 3), (dict(hq=6, hkv=4), 1), (dict(hq=32, hkv=2), 3),
+    (dict(nb=0), 1), (dict(mb=0), 1), (dict(msl=8 * 16 + 1), 1), (dict(scale=float("inf")), 1),
+    (dict(q=0), 1), (dict(ws=1 << 20 | 8), 1), (dict(k=(1 << 20) + 2), 1), (dict(wsb=16), 1),
+    (dict(B=-1), 1), (dict(nb=1 << 27, hkv=2, hq=2), 3),
+])
+def test_decode_rejects_bad_arguments(L, bad, code):
+    rc = L.pa_decode(*_decode_args(**bad))
+    assert rc == code, L.pa_last_error_string()
+    assert L.pa_last_error_string()
+
+
+def test_decode_zero_sequences_is_a_noop(L):
+    assert L.pa_decode(*_decode_args(B=0)) == 0
+
+
+def test_cache_write_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    p = P(1 << 20)
+    assert L.pa_cache_write(p, p, p, -1, 8, 128, p, p, 10, 1, None) == 1
+    assert L.pa_cache_write(p, p, p, 4, 8, 80, p, p, 10, 1, None) == 3
+    assert L.pa_cache_write(p, p, p, 4, 8, 128, p, p, 10, 5, None) == 3
+    assert L.pa_cache_write(p, p, P(0), 4, 8, 128, p, p, 10, 1, None) == 1
+    assert L.pa_cache_write(P((1 << 20) + 8), p, p, 4, 8, 128, p, p, 10, 1, None) == 1
+    assert L.pa_cache_write(p, p, p, 0, 8, 128, p, p, 10, 1, None) == 0   # nothing to do
+
+
+def test_workspace_size_grows_with_partitions(L):
+    a = L.pa_decode_workspace_bytes(8, 32, 128, 512)
+    b = L.pa_decode_workspace_bytes(8, 32, 128, 513)
+    assert b > a > 0
+    # partial results: (max, sum) + head_dim floats per (partition, query head)
+    assert b - a >= 8 * 32 * (128 + 2) * 4
+    assert L.pa_decode_workspace_bytes(-1, 32, 128, 512) == 0
