@@ -306,6 +306,9 @@ def run_pa(args, rank, world, local_rank):
 
     ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(args.steps)]
+    for a, z in ev_pairs:   # torch creates the CUDA event on its first record
+        a.record(stream)
+        z.record(stream)
     sampler = ClockSampler(gpu_identity(local_rank)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

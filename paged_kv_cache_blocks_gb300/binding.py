@@ -152,6 +152,9 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0,
         o = PaDecodeOpts()
         o.variant = variant
         if events:
+            for e in events:       # torch creates the CUDA event lazily, on first record
+                if not e.cuda_event:
+                    e.record(torch.cuda.current_stream() if stream is None else stream)
             o.event_before_main = events[0].cuda_event
             o.event_after_main = events[1].cuda_event
         opts = ctypes.byref(o)

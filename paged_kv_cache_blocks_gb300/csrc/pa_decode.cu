@@ -24,7 +24,9 @@
 //                        item they merge their states through shared memory
 //                        and write either the final output (one partition)
 //                        or the partition's (max, sum, unnormalised output);
-//   3. merge  (persistent) combines the partitions of split sequences.
+//   3. merge  (grid-stride) combines the partitions of split sequences:
+//                        one CTA per (sequence, KV head), slices of
+//                        partitions merged with a running maximum.
 //
 // Two math variants for the per-block QK^T / softmax / PV step, selected at
 // run time for the A/B measurement:
@@ -646,33 +648,121 @@ __global__ void __launch_bounds__(32 * (NC + 1))
 
 // ---------------------------------------------------------------------------
 // 3. merge of split sequences
+//
+// One CTA per (split sequence, KV head), grid-stride.  The CTA's threads are
+// kMergeSlices slices of 128; slice s merges partitions s, s + kMergeSlices,
+// ... with a running maximum (the same online rule as inside a partition),
+// each thread owning up to kE float4 columns of the G x D block, so a
+// partition is one fully coalesced read of G*D*4 bytes per slice.  The
+// slices' (max, sum, output) are then combined in shared memory.
+
+constexpr int kMergeSlices = 4;
+constexpr int kMergeThreads = 128 * kMergeSlices;
 
 template <typename T, int D>
-__global__ void __launch_bounds__(D) merge_kernel(const DecodeParams P) {
-  const int n_work = *reinterpret_cast<volatile int32_t*>(&P.ws->n_split) * P.hq;
-  const int d = threadIdx.x;
+__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodeParams P) {
+  constexpr int kE = (8 * D / 4 + 127) / 128;  // float4 columns per thread (G <= 8)
+  __shared__ float4 so[kMergeSlices][8 * D / 4];
+  __shared__ float sm[kMergeSlices][8], sl[kMergeSlices][8];
+  const int n_work = *reinterpret_cast<volatile int32_t*>(&P.ws->n_split) * P.hkv;
+  const int G = P.G;
+  const int n4 = G * D / 4;
+  const int tid = threadIdx.x, slice = tid >> 7, t = tid & 127;
+  const float4* acc4 = reinterpret_cast<const float4*>(P.acc);
   for (int wi = blockIdx.x; wi < n_work; wi += gridDim.x) {
-    const int b = P.split[wi / P.hq];
-    const int i = wi - (wi / P.hq) * P.hq;
+    const int b = P.split[wi / P.hkv];
+    const int h = wi - (wi / P.hkv) * P.hkv;
+    const int64_t head0 = static_cast<int64_t>(h) * G;
     const int2 sf = P.seq_first[b];
-    const int L = clamp_len(P, b);
+    int L = P.seq_lens[b];
+    L = L < 0 ? 0 : (L > P.max_seq_len ? P.max_seq_len : L);
     const int nfull = L / kPartTokens;
     const int nparts = nfull + ((L % kPartTokens) != 0);
-    float M = -INFINITY;
-    for (int p = 0; p < nparts; ++p) {
-      const int idx = p < nfull ? sf.x + p : sf.y;
-      M = fmaxf(M, P.ml[static_cast<int64_t>(idx) * P.hq + i].x);
+    int e4[kE], gk[kE];
+    float m[kE], l[kE];
+    float4 o[kE];
+#pragma unroll
+    for (int k = 0; k < kE; ++k) {
+      e4[k] = t + 128 * k;
+      gk[k] = min(4 * e4[k] / D, 7);
+      m[k] = -INFINITY;
+      l[k] = 0.f;
+      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float Lsum = 0.f, O = 0.f;
-    for (int p = 0; p < nparts; ++p) {
-      const int idx = p < nfull ? sf.x + p : sf.y;
-      const int64_t prow = static_cast<int64_t>(idx) * P.hq + i;
-      const float2 ml = P.ml[prow];
-      const float wgt = exp2f(ml.x - M);
-      Lsum = fmaf(ml.y, wgt, Lsum);
-      O = fmaf(P.acc[prow * D + d], wgt, O);
+    constexpr int U = 4;
+    for (int p0 = slice; p0 < nparts; p0 += U * kMergeSlices) {
+      float4 a[U][kE];
+      float2 ml[U][kE];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int p = p0 + u * kMergeSlices;
+        if (p < nparts) {
+          const int64_t idx = p < nfull ? sf.x + p : sf.y;
+#pragma unroll
+          for (int k = 0; k < kE; ++k)
+            if (e4[k] < n4) {
+              a[u][k] = __ldcg(&acc4[(idx * P.hq + head0) * (D / 4) + e4[k]]);
+              ml[u][k] = __ldcg(&P.ml[idx * P.hq + head0 + gk[k]]);
+            }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (p0 + u * kMergeSlices < nparts) {
+#pragma unroll
+          for (int k = 0; k < kE; ++k)
+            if (e4[k] < n4) {
+              const float mn = fmaxf(m[k], ml[u][k].x);
+              const float al = exp2f(m[k] - mn), wg = exp2f(ml[u][k].x - mn);
+              l[k] = fmaf(l[k], al, ml[u][k].y * wg);
+              o[k].x = fmaf(o[k].x, al, a[u][k].x * wg);
+              o[k].y = fmaf(o[k].y, al, a[u][k].y * wg);
+              o[k].z = fmaf(o[k].z, al, a[u][k].z * wg);
+              o[k].w = fmaf(o[k].w, al, a[u][k].w * wg);
+              m[k] = mn;
+            }
+        }
+      }
     }
-    static_cast<T*>(P.out)[(static_cast<int64_t>(b) * P.hq + i) * D + d] = from_float<T>(O / Lsum);
+#pragma unroll
+    for (int k = 0; k < kE; ++k)
+      if (e4[k] < n4) {
+        so[slice][e4[k]] = o[k];
+        if ((4 * e4[k]) % D == 0) {  // one thread per head publishes (max, sum)
+          sm[slice][gk[k]] = m[k];
+          sl[slice][gk[k]] = l[k];
+        }
+      }
+    __syncthreads();
+    if (slice == 0) {
+#pragma unroll
+      for (int k = 0; k < kE; ++k)
+        if (e4[k] < n4) {
+          const int g = gk[k];
+          float M = -INFINITY;
+#pragma unroll
+          for (int s2 = 0; s2 < kMergeSlices; ++s2) M = fmaxf(M, sm[s2][g]);
+          float Ls = 0.f;
+          float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int s2 = 0; s2 < kMergeSlices; ++s2) {
+            const float wg = exp2f(sm[s2][g] - M);  // 0 for a slice without partitions
+            const float4 x = so[s2][e4[k]];
+            Ls = fmaf(sl[s2][g], wg, Ls);
+            O.x = fmaf(x.x, wg, O.x);
+            O.y = fmaf(x.y, wg, O.y);
+            O.z = fmaf(x.z, wg, O.z);
+            O.w = fmaf(x.w, wg, O.w);
+          }
+          const float inv = 1.f / Ls;
+          T* dst = static_cast<T*>(P.out) + (static_cast<int64_t>(b) * P.hq + head0) * D + 4 * e4[k];
+          uint2 pk;
+          pk.x = pack2<T>(O.x * inv, O.y * inv);
+          pk.y = pack2<T>(O.z * inv, O.w * inv);
+          *reinterpret_cast<uint2*>(dst) = pk;
+        }
+    }
+    __syncthreads();
   }
 }
 
@@ -829,15 +919,16 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
   if (mgrid > 4 * sms) mgrid = 4 * sms;
   if (mgrid < 1) mgrid = 1;
+  const unsigned mg = static_cast<unsigned>(mgrid);
   if (a.dtype == 1) {
-    if (a.head_dim == 128) merge_kernel<__nv_bfloat16, 128><<<static_cast<unsigned>(mgrid), 128, 0, s>>>(P);
-    else merge_kernel<__nv_bfloat16, 64><<<static_cast<unsigned>(mgrid), 64, 0, s>>>(P);
+    if (a.head_dim == 128) merge_kernel<__nv_bfloat16, 128><<<mg, kMergeThreads, 0, s>>>(P);
+    else merge_kernel<__nv_bfloat16, 64><<<mg, kMergeThreads, 0, s>>>(P);
   } else {
-    if (a.head_dim == 128) merge_kernel<__half, 128><<<static_cast<unsigned>(mgrid), 128, 0, s>>>(P);
-    else merge_kernel<__half, 64><<<static_cast<unsigned>(mgrid), 64, 0, s>>>(P);
+    if (a.head_dim == 128) merge_kernel<__half, 128><<<mg, kMergeThreads, 0, s>>>(P);
+    else merge_kernel<__half, 64><<<mg, kMergeThreads, 0, s>>>(P);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) {
