@@ -214,6 +214,32 @@ int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache,
  * Returns PA_ERR_DEVICE when any bit is set. */
 int pa_decode_check(const void* d_workspace, void* stream, int32_t* error_bits);
 
+/* ------------------------------------------------------------------------
+ * Decode without any allocation.  The pages have no counterpart: this is a
+ * convenience for callers that cannot allocate device memory or pass a
+ * workspace (a fixed, pre-planned memory budget, a plugin or callback that
+ * owns no device memory, code that must not allocate next to a caching
+ * allocator).  Same arguments and result as pa_decode, minus the workspace:
+ * the scratch is one static 64 MiB device array per device, held from the
+ * library's module load until process exit.
+ *   - Batches whose pa_decode_workspace_bytes(num_seqs, num_q_heads,
+ *     head_dim, max_seq_len) exceeds 64 MiB are rejected with
+ *     PA_ERR_INVALID (nothing is launched).
+ *   - Calls no cudaMalloc/cudaFree or other allocating routine.
+ *   - The first call on a device looks up the array's device address (and
+ *     may load the module); make that first call before any stream capture.
+ *   - Every call on a device shares the array and leaves its contents
+ *     behind; each call rewrites what it reads, but calls whose kernels may
+ *     overlap on the GPU (unordered streams) race on it and must not be
+ *     issued.  Device error bits of the last call are not readable through
+ *     this entry point.
+ * ---------------------------------------------------------------------- */
+int pa_decode_noalloc(const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                      int64_t num_blocks, const int32_t* d_block_tables, int32_t max_blocks_per_seq,
+                      const int32_t* d_seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                      int32_t dtype, void* d_out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -61,6 +61,8 @@ _SIGS = {
     "pa_decode_ex": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, SZ, P, P],
                      ctypes.c_int),
     "pa_decode_check": ([P, P, P], ctypes.c_int),
+    "pa_decode_noalloc": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P],
+                          ctypes.c_int),
 }
 
 
@@ -162,6 +164,23 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0,
                             _ptr(seq_lens), B, msl, Hq, Hkv, D, float(scale), _dtype_code(q, dtype),
                             _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream), opts)
     _check(rc, "pa_decode")
+    return out
+
+
+def pa_decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0, out=None,
+                      dtype=None, stream=None):
+    """pa_decode for callers that cannot allocate: the scratch is a fixed
+    64 MiB static device array inside libpa (batches needing more are
+    rejected).  Allocates nothing itself when ``out`` is given."""
+    _need_cuda(q, k_cache, v_cache, block_tables, seq_lens)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib().pa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.shape[0],
+                                 _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+                                 max_seq_len, Hq, k_cache.shape[1], D, float(scale),
+                                 _dtype_code(q, dtype), _ptr(out), _stream(stream))
+    _check(rc, "pa_decode_noalloc")
     return out
 
 
