@@ -65,7 +65,7 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def algorithmic_bytes(lens, hq, hkv, d, elem=2):
+def algorithmic_bytes(lens, hq, hkv, d, elem=2, part_tokens=512):
     """Bytes the attention kernel must move: K/V of every token once per KV
     head, block ids, q, and either the output (one partition) or the fp32
     partial (max, sum, head_dim values) of every partition."""
@@ -73,7 +73,7 @@ def algorithmic_bytes(lens, hq, hkv, d, elem=2):
     kv = int(L.sum()) * hkv * d * elem * 2
     ids = int(((L + 15) // 16).sum()) * 4
     q = len(L) * hq * d * elem
-    nparts = (L + 511) // 512
+    nparts = (L + part_tokens - 1) // part_tokens
     single = nparts == 1
     out = int(single.sum()) * hq * d * elem
     partial = int(nparts[~single].sum()) * hq * (d + 2) * 4
@@ -145,6 +145,21 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(pw) if pw else None,
                 "reasons": reasons, "samples": len(win), "note": note}
+
+
+def reduce_max(value, dist=None, device="cpu"):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, seconds_max):
+    """Whole-job rate: every rank processes the same number of units (weak
+    scaling), the job takes as long as its slowest rank."""
+    return units_per_rank * world / seconds_max
 
 
 def gpu_identity(local_rank):
@@ -325,15 +340,12 @@ def run_pa(args, rank, world, local_rank):
         sampler.stop()
     ms_total = start.elapsed_time(stop)
     kern_ms = [a.elapsed_time(z) for a, z in ev_pairs]
-    ms_step = ms_total / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = reduce_max(ms_total / args.steps, dist, dev)
 
     kvb = logical_kv_bytes(b.seq_lens, Hkv, D)
-    kv_gbs = kvb * world / (ms_step * 1e-3) / 1e9
-    alg = algorithmic_bytes(b.seq_lens, Hq, Hkv, D)
+    kv_gbs = job_throughput(kvb, world, ms_step * 1e-3) / 1e9
+    part_tokens = int(ws[24:28].view(torch.int32).item())   # chosen by the prep kernel
+    alg = algorithmic_bytes(b.seq_lens, Hq, Hkv, D, part_tokens=part_tokens)
     kern_avg = statistics.fmean(kern_ms)
     peak, peak_kind = measured_peaks()
     achieved = alg / (kern_avg * 1e-3) / 1e9
@@ -363,8 +375,9 @@ def run_pa(args, rank, world, local_rank):
                    "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV per step vs 129 MB L2; "
                          "no flush",
                    "step": "pa_cache_write (one new token per sequence) + pa_decode",
-                   "variant": args.variant, "parallelism": f"replicas x{world}"},
-        "seqs_steps_per_s": B * world / (ms_step * 1e-3),
+                   "variant": args.variant, "partition_tokens": part_tokens,
+                   "parallelism": f"replicas x{world}"},
+        "seqs_steps_per_s": job_throughput(B, world, ms_step * 1e-3),
         "hbm_frac_step": (kvb / (ms_step * 1e-3) / 1e9) / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -380,18 +393,35 @@ def run_pa(args, rank, world, local_rank):
     return 0
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one attention launch, from
+# the ncu captures summarised in profiles/ (file named below), keyed by the
+# hash of the kernel sources they were taken on: a changed kernel reports null.
+TRAFFIC = {
+    ("llama70b", "auto"): {"bytes": 3.77e9 + 19.24e6, "kernel_src": "89dc4da88bac4115",
+                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
+    ("llama70b", "mma"): {"bytes": 3.77e9 + 19.24e6, "kernel_src": "89dc4da88bac4115",
+                          "profile": "profiles/attend_kernel_llama70b_dram.md"},
+    ("llama8b", "auto"): {"bytes": 321.78e6 + 4.74e6, "kernel_src": "89dc4da88bac4115",
+                          "profile": "profiles/attend_kernel_llama70b_dram.md"},
+}
+
+
+def kernel_src_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_blocks_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def load_traffic(workload, variant):
-    """DRAM bytes per attention launch from the committed ncu summary, if it
-    matches this kernel build (else null)."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    """DRAM bytes per attention launch from the ncu capture of this kernel
+    build, or None when there is none (or the kernel changed since)."""
+    ent = TRAFFIC.get((workload, variant))
+    if not ent or ent["kernel_src"] != kernel_src_hash():
         return None
-    try:
-        d = json.load(open(p))
-        ent = d.get(f"{workload}:{variant}")
-        return ent.get("dram_bytes_per_launch") if ent else None
-    except Exception:
-        return None
+    return ent["bytes"]
 
 
 def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
@@ -465,13 +495,9 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
     for _ in range(steps):
         one_step()
     barrier()
-    sec = (time.perf_counter() - t0) / steps
-    if dist is not None:
-        t = torch.tensor([sec], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        sec = float(t.item())
+    sec = reduce_max((time.perf_counter() - t0) / steps, dist, dev)
     alloc.close()
-    return {"value": statistics.fmean(kv_bytes) * world / sec / 1e9, "unit": "GB/s",
+    return {"value": job_throughput(statistics.fmean(kv_bytes), world, sec) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": sec * 1e3,
             "path": "host allocator append_slots -> H2D (pinned) q,k,v,slots,table,lens -> "

@@ -104,40 +104,78 @@ __device__ int block_exclusive_scan(int v, int* sw, int* total) {
   return res;
 }
 
-__global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint4) {
+// Partition size: the largest of 512, 1024, 2048 tokens that still leaves at
+// least `target_full_items` full-partition work items, so long sequences make
+// fewer partials to merge while the persistent grid stays balanced.  Partial
+// (tail) partitions are ordered longest first by a counting sort on their
+// size, so the dynamic work queue ends on the shortest items.
+__global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint4,
+                                                    int target_full_items) {
   __shared__ int sw[32];
-  __shared__ int s_total_full, s_nsplit;
+  __shared__ int s_full[3];
+  __shared__ int s_hist[kMaxPartBlocks + 1];
+  __shared__ int s_nsplit, s_total_tail;
   const int tid = threadIdx.x;
   if (tid == 0) {
     P.ws->error_bits = 0;
-    s_total_full = 0;
+    s_full[0] = s_full[1] = s_full[2] = 0;
     s_nsplit = 0;
   }
+  for (int i = tid; i <= kMaxPartBlocks; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
-  // pass A: number of full partitions
-  int mine = 0;
-  for (int b = tid; b < P.num_seqs; b += blockDim.x) mine += clamp_len(P, b) / kPartTokens;
-  atomicAdd(&s_total_full, mine);
+  // pass A: full partitions for each candidate size
+  int f1 = 0, f2 = 0, f4 = 0;
+  for (int b = tid; b < P.num_seqs; b += blockDim.x) {
+    const int L = clamp_len(P, b);
+    f1 += L / kPartTokens;
+    f2 += L / (2 * kPartTokens);
+    f4 += L / (4 * kPartTokens);
+  }
+  atomicAdd(&s_full[0], f1);
+  atomicAdd(&s_full[1], f2);
+  atomicAdd(&s_full[2], f4);
   __syncthreads();
-  const int total_full = s_total_full;
-  // pass B: place partitions; full ones first, then the partial tails
-  int carry_full = 0, carry_tail = 0;
+  int pt = kPartTokens, total_full = s_full[0];
+  if (static_cast<int64_t>(s_full[2]) * P.hkv >= target_full_items) {
+    pt = 4 * kPartTokens;
+    total_full = s_full[2];
+  } else if (static_cast<int64_t>(s_full[1]) * P.hkv >= target_full_items) {
+    pt = 2 * kPartTokens;
+    total_full = s_full[1];
+  }
+  // tails by size (blocks), then start offsets in descending size order
+  for (int b = tid; b < P.num_seqs; b += blockDim.x) {
+    const int r = P.seq_lens[b] < 0 ? 0 : clamp_len(P, b) % pt;
+    if (r) atomicAdd(&s_hist[(r + kBlock - 1) / kBlock], 1);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int run = 0;
+    for (int sz = pt / kBlock; sz >= 1; --sz) {
+      const int c = s_hist[sz];
+      s_hist[sz] = run;
+      run += c;
+    }
+    s_total_tail = run;
+  }
+  __syncthreads();
+  // pass B: full partitions in sequence order, tails at their sorted slots
+  int carry_full = 0;
   for (int base = 0; base < P.num_seqs; base += blockDim.x) {
     const int b = base + tid;
     int L = 0;
     if (b < P.num_seqs) L = clamp_len(P, b);
-    const int nfull = L / kPartTokens;
-    const int tail = (L % kPartTokens) != 0;
-    int tot_f, tot_t;
+    const int nfull = L / pt;
+    const int r = L % pt;
+    int tot_f;
     const int fo = block_exclusive_scan(nfull, sw, &tot_f);
-    const int to = block_exclusive_scan(tail, sw, &tot_t);
     if (b < P.num_seqs) {
-      const int nparts = nfull + tail;
+      const int nparts = nfull + (r != 0);
       const int first = carry_full + fo;
-      const int tail_idx = tail ? total_full + carry_tail + to : -1;
+      const int tail_idx = r ? total_full + atomicAdd(&s_hist[(r + kBlock - 1) / kBlock], 1) : -1;
       P.seq_first[b] = make_int2(first, tail_idx);
       for (int p = 0; p < nfull; ++p) P.parts[first + p] = PartInfo{b, p, L, nparts};
-      if (tail) P.parts[tail_idx] = PartInfo{b, nfull, L, nparts};
+      if (r) P.parts[tail_idx] = PartInfo{b, nfull, L, nparts};
       if (nparts > 1) P.split[atomicAdd(&s_nsplit, 1)] = b;
       if (L == 0) {  // empty softmax: the output is defined as 0
         uint4* o = reinterpret_cast<uint4*>(P.out) + static_cast<int64_t>(b) * row_uint4;
@@ -145,16 +183,16 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
       }
     }
     carry_full += tot_f;
-    carry_tail += tot_t;
   }
   __syncthreads();
   if (tid == 0) {
-    const int n_parts = carry_full + carry_tail;
+    const int n_parts = total_full + s_total_tail;
     P.ws->n_parts = n_parts;
     P.ws->n_items = n_parts * P.hkv;
     P.ws->next_item = 0;
     P.ws->n_split = s_nsplit;
     P.ws->next_split = 0;
+    P.ws->part_tokens = pt;
   }
 }
 
@@ -464,7 +502,7 @@ struct AttendCfg {
   // full[S], empty[S], item_full[2], item_empty[2], merge_full[2]
   static constexpr size_t kInfoOff = kBarOff + (2 * S + 6) * sizeof(uint64_t);
   static constexpr size_t kIdsOff = kInfoOff + 2 * sizeof(ItemInfo);
-  static constexpr size_t kAbortOff = kIdsOff + 2 * 32 * sizeof(int32_t);
+  static constexpr size_t kAbortOff = kIdsOff + 2 * kMaxPartBlocks * sizeof(int32_t);
   static constexpr size_t kBytes = kAbortOff + 16 + 1024;  // + slack to 1024-align the base
 };
 
@@ -513,6 +551,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       tma_prefetch_desc(&tm_v);
     }
     const int32_t n_items = *reinterpret_cast<volatile int32_t*>(&P.ws->n_items);
+    const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
     const int64_t y_oob = P.num_blocks * P.hkv * kBlock;  // one past the pool: reads as zeros
     uint32_t g = 0;  // blocks issued by this CTA
     bool ok = true;
@@ -535,15 +574,16 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       }
       const int part = item / P.hkv, h = item - part * P.hkv;
       const PartInfo pi = P.parts[part];
-      const int first_tok = pi.p * kPartTokens;
-      const int nblk = min(kPartBlocks, (pi.len - first_tok + kBlock - 1) / kBlock);
-      if (lane < nblk) {
-        int32_t id = P.tables[static_cast<int64_t>(pi.b) * P.max_blocks + pi.p * kPartBlocks + lane];
+      const int first_tok = pi.p * pt;
+      const int nblk = min(pt / kBlock, (pi.len - first_tok + kBlock - 1) / kBlock);
+      const int32_t* trow = P.tables + static_cast<int64_t>(pi.b) * P.max_blocks + first_tok / kBlock;
+      for (int j = lane; j < nblk; j += 32) {
+        int32_t id = trow[j];
         if (id < 0 || id >= P.num_blocks) {
           atomicOr(err, kErrBlockId);
           id = -1;
         }
-        ids[slot * 32 + lane] = id;
+        ids[slot * kMaxPartBlocks + j] = id;
       }
       __syncwarp();
       if (lane == 0) {
@@ -553,7 +593,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
           const int st = g % S;
           ok = mbar_wait(&empty[st], ((g / S) & 1) ^ 1, abort_flag, err);
           if (!ok) break;
-          const int32_t id = ids[slot * 32 + j];
+          const int32_t id = ids[slot * kMaxPartBlocks + j];
           const int32_t y = static_cast<int32_t>(id < 0 ? y_oob : (static_cast<int64_t>(id) * P.hkv + h) * kBlock);
           uint8_t* dst = stages + static_cast<size_t>(st) * Cfg::kStageBytes;
           mbar_arrive_expect_tx(&full[st], Cfg::kStageBytes);
@@ -582,6 +622,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
 
   // ---------------------------------------------------------------- consumers
   const int w = warp - 1;
+  const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
   float* scr = scratch + (kFma ? w * FmaScratch<D>::kFloats : 0);
   State st;
   for (uint32_t it = 0;; ++it) {
@@ -604,7 +645,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
         break;
       }
       const uint32_t sK = smem_u32(stages + static_cast<size_t>(s) * Cfg::kStageBytes);
-      const int nvalid = min(kBlock, inf.len - (inf.p * kPartTokens + j * kBlock));
+      const int nvalid = min(kBlock, inf.len - (inf.p * pt + j * kBlock));
       st.block(sK, sK + Tile<D>::kKVBytes, nvalid, P.scale_log2, lane, scr);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -665,6 +706,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodePar
   __shared__ float4 so[kMergeSlices][8 * D / 4];
   __shared__ float sm[kMergeSlices][8], sl[kMergeSlices][8];
   const int n_work = *reinterpret_cast<volatile int32_t*>(&P.ws->n_split) * P.hkv;
+  const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
   const int G = P.G;
   const int n4 = G * D / 4;
   const int tid = threadIdx.x, slice = tid >> 7, t = tid & 127;
@@ -676,8 +718,8 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodePar
     const int2 sf = P.seq_first[b];
     int L = P.seq_lens[b];
     L = L < 0 ? 0 : (L > P.max_seq_len ? P.max_seq_len : L);
-    const int nfull = L / kPartTokens;
-    const int nparts = nfull + ((L % kPartTokens) != 0);
+    const int nfull = L / pt;
+    const int nparts = nfull + ((L % pt) != 0);
     int e4[kE], gk[kE];
     float m[kE], l[kE];
     float4 o[kE];
@@ -895,7 +937,11 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
 
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const int row_uint4 = a.num_q_heads * a.head_dim * 2 / 16;
-  prep_kernel<<<1, 1024, 0, s>>>(P, row_uint4);
+  int dev0 = 0, n_sm = 0;
+  cudaGetDevice(&dev0);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev0);
+  // 8 full-partition items per attention CTA (two CTAs per SM)
+  prep_kernel<<<1, 1024, 0, s>>>(P, row_uint4, 16 * n_sm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("prep launch: ") + cudaGetErrorString(e);

@@ -11,8 +11,9 @@
 namespace pa {
 
 constexpr int kBlock = 16;          // tokens per KV block
-constexpr int kPartTokens = 512;    // tokens per decode partition
-constexpr int kPartBlocks = kPartTokens / kBlock;
+constexpr int kPartTokens = 512;    // smallest decode partition (tokens)
+constexpr int kMaxPartMult = 4;     // partitions are 512, 1024 or 2048 tokens
+constexpr int kMaxPartBlocks = kPartTokens * kMaxPartMult / kBlock;
 
 // Device error bits (mirrored by PA_DEVERR_* in pa.h).
 constexpr int kErrSeqLen = 1;
@@ -31,7 +32,8 @@ struct WsHeader {
   int32_t next_item;    // dynamic work counter of the attention kernel
   int32_t n_split;      // sequences with more than one partition
   int32_t next_split;   // dynamic work counter of the merge kernel
-  int32_t pad[58];
+  int32_t part_tokens;  // tokens per partition chosen for this call
+  int32_t pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 

@@ -84,6 +84,24 @@ def test_edge_lengths(pa, name, variant):
     U.assert_close(run(pa, b, variant=variant), U.oracle_out(b), f"edges {name} v{variant}")
 
 
+def test_2048_token_partitions_edges(pa):
+    """Enough long sequences that the prep kernel picks 2048-token
+    partitions; lengths around its multiples and tiny ones beside them."""
+    lens = (32768,) * 20 + (2047, 2048, 2049, 4095, 4096, 4097, 1, 17, 1000, 6001)
+    b = U.batch("llama70b", seed=8, lens=lens)
+    q, kc, vc, tab, lens_d = U.device_inputs(b)
+    ws = torch.empty(pa.pa_decode_workspace_bytes(len(lens), q.shape[1], q.shape[2],
+                                                  b.block_tables.shape[1] * 16),
+                     dtype=torch.uint8, device="cuda")
+    for variant in (1, 2):
+        out = pa.pa_decode(q, kc, vc, tab, lens_d, b.workload.scale, workspace=ws, variant=variant)
+        torch.cuda.synchronize()
+        assert int(ws[24:28].view(torch.int32).item()) == 2048
+        got = out.double().cpu().numpy()
+        rows = [0, 19] + list(range(20, len(lens)))
+        U.assert_close(got[rows], U.oracle_out(b, rows=rows), f"2048-token partitions v{variant}")
+
+
 def test_empty_sequences_give_zeros(pa):
     b = U.batch("llama8b", seed=6, lens=(0, 5, 0, 600))
     got = run(pa, b)
