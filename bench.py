@@ -47,6 +47,8 @@ DESCR = {
     "long": "long-context decode: 8 seqs x 32768 tokens, 32 q / 8 kv heads, head_dim 128, bf16, "
             "512-token partitions + merge",
     "tiny": "tiny decode: 4 seqs {1,17,33,100}, 4 q / 2 kv heads, head_dim 64, fp16",
+    "fullstep": "full decode step: 32 layers of the Llama-3-8B shape, 128 seqs in 4 groups of 32 "
+                "sharing a 1024-token prefix (ref-counted blocks), lens 1024+U{256..7168}, bf16",
 }
 VARIANTS = {"auto": 0, "fma": 1, "mma": 2}
 
@@ -292,25 +294,25 @@ def run_pa(args, rank, world, local_rank):
 
     w = W.WORKLOADS[args.workload]
     b = W.make_batch(args.workload, seed=rank, poison=False, device="cuda")
-    Lr = b.layers[0]
     dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
-    q, kc, vc = Lr.q.view(dt), Lr.k_cache.view(dt), Lr.v_cache.view(dt)
-    nk, nv = Lr.new_k.view(dt), Lr.new_v.view(dt)
+    layers = [(Lr.q.view(dt), Lr.k_cache.view(dt), Lr.v_cache.view(dt), Lr.new_k.view(dt),
+               Lr.new_v.view(dt)) for Lr in b.layers]
+    nl = len(layers)
     tab = torch.from_numpy(b.block_tables).to(dev)
     lens = torch.from_numpy(b.seq_lens).to(dev)
     slots = torch.from_numpy(b.slot_mapping).to(dev)
-    mb = b.block_tables.shape[1]
     msl = int(b.seq_lens.max())
     ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
-    out = torch.empty_like(q)
+    out = torch.empty_like(layers[0][0])
     variant = VARIANTS[args.variant]
     stream = torch.cuda.current_stream()
 
     def step(evs=None):
-        pa.pa_cache_write(nk, nv, slots, kc, vc)
-        pa.pa_decode(q, kc, vc, tab, lens, w.scale, max_seq_len=msl, out=out, workspace=ws,
-                     variant=variant, events=evs)
+        for li, (q, kc, vc, nk, nv) in enumerate(layers):
+            pa.pa_cache_write(nk, nv, slots, kc, vc)
+            pa.pa_decode(q, kc, vc, tab, lens, w.scale, max_seq_len=msl, out=out, workspace=ws,
+                         variant=variant, events=evs[li] if evs else None)
 
     for _ in range(args.warmup):
         step()
@@ -319,11 +321,12 @@ def run_pa(args, rank, world, local_rank):
     if bits:
         raise RuntimeError(f"device error bits {bits} during warm-up")
 
-    ev_pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
-    for a, z in ev_pairs:   # torch creates the CUDA event on its first record
-        a.record(stream)
-        z.record(stream)
+    ev_pairs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(nl)] for _ in range(args.steps)]
+    for row in ev_pairs:   # torch creates the CUDA event on its first record
+        for a, z in row:
+            a.record(stream)
+            z.record(stream)
     sampler = ClockSampler(gpu_identity(local_rank)) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -339,10 +342,10 @@ def run_pa(args, rank, world, local_rank):
         time.sleep(0.15)
         sampler.stop()
     ms_total = start.elapsed_time(stop)
-    kern_ms = [a.elapsed_time(z) for a, z in ev_pairs]
+    kern_ms = [a.elapsed_time(z) for row in ev_pairs for a, z in row]
     ms_step = reduce_max(ms_total / args.steps, dist, dev)
 
-    kvb = logical_kv_bytes(b.seq_lens, Hkv, D)
+    kvb = logical_kv_bytes(b.seq_lens, Hkv, D) * nl
     kv_gbs = job_throughput(kvb, world, ms_step * 1e-3) / 1e9
     part_tokens = int(ws[24:28].view(torch.int32).item())   # chosen by the prep kernel
     alg = algorithmic_bytes(b.seq_lens, Hq, Hkv, D, part_tokens=part_tokens)
@@ -351,7 +354,8 @@ def run_pa(args, rank, world, local_rank):
     achieved = alg / (kern_avg * 1e-3) / 1e9
 
     # ---- end to end through the public API, host buffers -------------------------
-    e2e = run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist)
+    e2e = run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist) \
+        if not args.no_e2e else None
 
     if rank != 0:
         return 0
@@ -370,11 +374,12 @@ def run_pa(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f16", "data": "synthetic",
         "config": {"workload": DESCR.get(args.workload, args.workload),
-                   "num_seqs": B, "kv_tokens": int(b.seq_lens.sum()),
+                   "num_seqs": B, "layers": nl, "kv_tokens": int(b.seq_lens.sum()),
                    "logical_kv_bytes_per_step": kvb,
+                   "unique_kv_bytes_per_step": b.unique_kv_bytes() * nl,
                    "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV per step vs 129 MB L2; "
                          "no flush",
-                   "step": "pa_cache_write (one new token per sequence) + pa_decode",
+                   "step": f"{nl} x (pa_cache_write of one new token per sequence + pa_decode)",
                    "variant": args.variant, "partition_tokens": part_tokens,
                    "parallelism": f"replicas x{world}"},
         "seqs_steps_per_s": job_throughput(B, world, ms_step * 1e-3),
@@ -384,7 +389,7 @@ def run_pa(args, rank, world, local_rank):
                      "kernel": "attend_kernel", "kernel_ms": kern_avg,
                      "algorithmic_bytes": alg, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 4 * nl * args.steps,
         "clocks": clocks,
     }
     if cpu is not None:
@@ -426,7 +431,9 @@ def load_traffic(workload, variant):
 
 def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
     """Same step through the public API from pinned host memory."""
+    import ctypes
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
+    nl = len(b.layers)
     steps = max(1, min(args.steps, args.e2e_steps))
     total = steps + args.warmup
     lens0 = b.seq_lens.astype(np.int64) - 1
@@ -435,38 +442,59 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
     nb = max(b.num_blocks, int(math.ceil(need * 1.05)))
     order = np.random.default_rng(123).permutation(nb).astype(np.int32)
     alloc = pa.Allocator(nb, order)
-    ids = np.array([alloc.seq_create() for _ in range(B)], np.int64)
     table_h = torch.full((B, mb), -1, dtype=torch.int32).pin_memory()
     lens_h = torch.zeros(B, dtype=torch.int32).pin_memory()
-    ids_c = ids.ctypes.data_as(__import__("ctypes").c_void_p)
     scratch = np.empty(int(lens0.max()) + 1, np.int64)
-    for i in range(B):  # the tokens already in the cache
-        one = np.array([ids[i]], np.int64)
-        if lens0[i] > 0:
-            pa.lib().pa_seq_append_slots(alloc._h, one.ctypes.data, 1, int(lens0[i]),
-                                         scratch.ctypes.data, None, None, 0, None,
-                                         table_h[i:i + 1].numpy().ctypes.data, mb,
-                                         lens_h[i:i + 1].numpy().ctypes.data)
-    dtype_bytes = 2
+
+    def append(i, sid, n):
+        one = np.array([sid], np.int64)
+        rc = pa.lib().pa_seq_append_slots(alloc._h, one.ctypes.data, 1, int(n), scratch.ctypes.data,
+                                          None, None, 0, None, table_h[i:i + 1].numpy().ctypes.data,
+                                          mb, lens_h[i:i + 1].numpy().ctypes.data)
+        if rc != 0:
+            raise RuntimeError(pa.lib().pa_last_error_string().decode())
+
+    ids = np.zeros(B, np.int64)
+    if w.name == "fullstep":   # groups share a prefix through fork (ref-counted blocks)
+        per = B // W.PREFIX_GROUPS
+        for gi in range(W.PREFIX_GROUPS):
+            parent = alloc.seq_create()
+            append(gi * per, parent, W.PREFIX_TOKENS)
+            for i in range(gi * per, (gi + 1) * per):
+                ids[i] = alloc.seq_fork(parent, W.PREFIX_TOKENS)
+            alloc.seq_free(parent)
+        rows, _ = alloc.block_table(ids.tolist(), mb)
+        table_h.copy_(torch.tensor(rows, dtype=torch.int32))
+        lens_h.fill_(W.PREFIX_TOKENS)
+        for i in range(B):
+            append(i, ids[i], lens0[i] - W.PREFIX_TOKENS)
+    else:
+        for i in range(B):  # the tokens already in the cache
+            ids[i] = alloc.seq_create()
+            if lens0[i] > 0:
+                append(i, ids[i], lens0[i])
+    ids_c = ids.ctypes.data_as(ctypes.c_void_p)
     g = torch.Generator().manual_seed(99)
-    q_h = torch.randn((B, Hq, D), generator=g).to(dt).pin_memory()
-    k_h = torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory()
-    v_h = torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory()
+    q_h = [torch.randn((B, Hq, D), generator=g).to(dt).pin_memory() for _ in range(nl)]
+    k_h = [torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory() for _ in range(nl)]
+    v_h = [torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory() for _ in range(nl)]
+    out_h = [torch.empty((B, Hq, D), dtype=dt).pin_memory() for _ in range(nl)]
     slots_h = torch.empty(B, dtype=torch.int64).pin_memory()
-    out_h = torch.empty((B, Hq, D), dtype=dt).pin_memory()
-    kc = torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev)
-    vc = torch.zeros_like(kc)
-    q_d, k_d, v_d = torch.empty_like(q_h, device=dev), torch.empty_like(k_h, device=dev), \
-        torch.empty_like(v_h, device=dev)
+    caches = [(torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev),
+               torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev)) for _ in range(nl)]
+    q_d = [torch.empty((B, Hq, D), dtype=dt, device=dev) for _ in range(nl)]
+    k_d = [torch.empty((B, Hkv, D), dtype=dt, device=dev) for _ in range(nl)]
+    v_d = [torch.empty((B, Hkv, D), dtype=dt, device=dev) for _ in range(nl)]
+    out_d = [torch.empty((B, Hq, D), dtype=dt, device=dev) for _ in range(nl)]
     slots_d = torch.empty(B, dtype=torch.int64, device=dev)
     table_d = torch.empty((B, mb), dtype=torch.int32, device=dev)
     lens_d = torch.empty(B, dtype=torch.int32, device=dev)
-    out_d = torch.empty((B, Hq, D), dtype=dt, device=dev)
     msl = mb * 16
     ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
     slots_np, table_np, lens_np = slots_h.numpy(), table_h.numpy(), lens_h.numpy()
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, slots_h, table_h, lens_h))
-    d2h = out_h.numel() * out_h.element_size()
+    nbytes = lambda t: t.numel() * t.element_size()
+    h2d = sum(nbytes(t) for t in q_h + k_h + v_h) + sum(nbytes(t) for t in (slots_h, table_h, lens_h))
+    d2h = sum(nbytes(t) for t in out_h)
     kv_bytes = []
 
     def one_step():
@@ -474,18 +502,20 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
                                           0, None, table_np.ctypes.data, mb, lens_np.ctypes.data)
         if rc != 0:
             raise RuntimeError(pa.lib().pa_last_error_string().decode())
-        q_d.copy_(q_h, non_blocking=True)
-        k_d.copy_(k_h, non_blocking=True)
-        v_d.copy_(v_h, non_blocking=True)
         slots_d.copy_(slots_h, non_blocking=True)
         table_d.copy_(table_h, non_blocking=True)
         lens_d.copy_(lens_h, non_blocking=True)
-        pa.pa_cache_write(k_d, v_d, slots_d, kc, vc)
-        pa.pa_decode(q_d, kc, vc, table_d, lens_d, w.scale, max_seq_len=msl, out=out_d,
-                     workspace=ws, variant=variant)
-        out_h.copy_(out_d, non_blocking=True)
+        for li in range(nl):
+            q_d[li].copy_(q_h[li], non_blocking=True)
+            k_d[li].copy_(k_h[li], non_blocking=True)
+            v_d[li].copy_(v_h[li], non_blocking=True)
+            kc, vc = caches[li]
+            pa.pa_cache_write(k_d[li], v_d[li], slots_d, kc, vc)
+            pa.pa_decode(q_d[li], kc, vc, table_d, lens_d, w.scale, max_seq_len=msl, out=out_d[li],
+                         workspace=ws, variant=variant)
+            out_h[li].copy_(out_d[li], non_blocking=True)
         torch.cuda.current_stream().synchronize()
-        kv_bytes.append(int(lens_np.astype(np.int64).sum()) * Hkv * D * dtype_bytes * 2)
+        kv_bytes.append(int(lens_np.astype(np.int64).sum()) * Hkv * D * 2 * 2 * nl)
 
     for _ in range(args.warmup):
         one_step()
@@ -500,8 +530,8 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
     return {"value": job_throughput(statistics.fmean(kv_bytes), world, sec) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": sec * 1e3,
-            "path": "host allocator append_slots -> H2D (pinned) q,k,v,slots,table,lens -> "
-                    "pa_cache_write -> pa_decode -> D2H out -> sync"}
+            "path": "host allocator append_slots -> H2D (pinned) slots,table,lens and per layer "
+                    "q,k,v -> pa_cache_write -> pa_decode -> D2H out, then sync"}
 
 
 def main():
@@ -514,6 +544,7 @@ def main():
     ap.add_argument("--impl", default="pa", choices=["pa", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -492,6 +492,7 @@ constexpr size_t align_up_c(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 template <typename T, int D, int NC, int S, bool kFma>
 struct AttendCfg {
+  static_assert(S % NC == 0, "each ring stage must always be consumed by the same warp");
   static constexpr int kThreads = 32 * (NC + 1);
   static constexpr int kStageBytes = Tile<D>::kStageBytes;
   static constexpr size_t kStagesOff = 0;
@@ -636,7 +637,12 @@ __global__ void __launch_bounds__(32 * (NC + 1))
 
     st.begin(P, inf, lane, scr);
     bool alive = true;
-    for (int j = w; j < inf.nblk; j += NC) {
+    // Block g of the CTA's stream goes to consumer g % NC.  With S a multiple
+    // of NC, every use of ring stage g % S is then consumed by the same warp,
+    // in order, so a parity wait can never be satisfied by an older phase of
+    // the stage (which would let a warp read a stage before its copy lands).
+    const int j0 = (w - static_cast<int>(static_cast<uint32_t>(inf.g0) % NC) + NC) % NC;
+    for (int j = j0; j < inf.nblk; j += NC) {
       const uint32_t gg = inf.g0 + j;
       const int s = gg % S;
       ok = mbar_wait(&full[s], (gg / S) & 1, abort_flag, err);
@@ -896,7 +902,7 @@ bool dispatch_attend(int variant, int G, const CUtensorMap& tk, const CUtensorMa
                      const DecodeParams& P, int64_t max_items, cudaStream_t s, std::string* why) {
   constexpr int NC = 4;
   if (variant == 1) {
-    constexpr int S = 6;
+    constexpr int S = 4;  // the FMA variant also keeps q, p in shared memory
     if (G <= 2) return launch_attend<T, D, NC, S, true, 1>(tk, tv, P, max_items, s, why);
     if (G <= 4) return launch_attend<T, D, NC, S, true, 2>(tk, tv, P, max_items, s, why);
     return launch_attend<T, D, NC, S, true, 4>(tk, tv, P, max_items, s, why);
@@ -966,7 +972,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  if (mgrid > 4 * sms) mgrid = 4 * sms;
+  if (mgrid > 2 * sms) mgrid = 2 * sms;  // one wave at two CTAs per SM
   if (mgrid < 1) mgrid = 1;
   const unsigned mg = static_cast<unsigned>(mgrid);
   if (a.dtype == 1) {

@@ -1,0 +1,137 @@
+"""Model check of the attention kernel's shared-memory ring protocol (CPU).
+
+The kernel's producer warp streams blocks into S stages; consumer warps wait
+on a per-stage "full" mbarrier with a parity bit and release the stage on an
+"empty" mbarrier.  A parity wait only asks "has the phase of this parity
+completed", so if two consecutive uses of one stage could be consumed by
+different warps, a warp waiting for round r+1 could pass on round r-1's
+completed phase and read the stage before its copy lands.  The kernel rules
+that out by giving block g of a CTA's stream to consumer g % NC with
+S % NC == 0.  This test runs a randomised discrete-event model of the
+protocol with exact mbarrier parity semantics (try_wait.parity(P) is true
+iff the barrier's current phase parity differs from P) and checks that no
+consumer ever reads a stage holding a block other than the one it waits for.
+The item-relative assignment the kernel used before is shown to fail with
+S = 6, NC = 4 (it reads stale stages or deadlocks)."""
+import random
+
+import pytest
+
+
+class Barrier:
+    def __init__(self, count):
+        self.count = count
+        self.pending = count
+        self.phase = 0            # completed phases
+        self.tx = 0
+
+    def try_wait(self, parity):
+        return (self.phase & 1) != parity
+
+    def arrive(self):
+        self.pending -= 1
+        self._maybe_complete()
+
+    def expect_tx(self, n):
+        self.tx += n
+        self.arrive()
+
+    def complete_tx(self, n):
+        self.tx -= n
+        self._maybe_complete()
+
+    def _maybe_complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+
+def simulate(S, NC, rule, items, seed):
+    """Returns the number of stale reads (0 = protocol safe), or -1 if the
+    protocol deadlocks (nobody can move for a long time)."""
+    rng = random.Random(seed)
+    full = [Barrier(1) for _ in range(S)]
+    empty = [Barrier(1) for _ in range(S)]
+    stage_tag = [None] * S
+    in_flight = []                     # (land_time, stage, block)
+    g0s, g = [], 0
+    for n in items:
+        g0s.append(g)
+        g += n
+    total = g
+    # consumer state: (item index, next position in its block list)
+    def blocks_of(w, it):
+        g0, n = g0s[it], items[it]
+        if rule == "global":
+            j0 = (w - g0 % NC) % NC
+        else:                           # item-relative (the old rule)
+            j0 = w
+        return [g0 + j for j in range(j0, n, NC)]
+
+    cons = [{"it": 0, "list": blocks_of(w, 0), "pos": 0, "at_merge": False} for w in range(NC)]
+    merge_arrived = [0] * len(items)
+    next_issue = 0
+    stale = 0
+    t = 0
+    done = [False] * NC
+    while not all(done):
+        t += 1
+        if t > 200 * total + 20000:
+            return -1
+        # copies land after a random delay
+        for rec in [r for r in in_flight if r[0] <= t]:
+            in_flight.remove(rec)
+            _, s, blk = rec
+            stage_tag[s] = blk
+            full[s].complete_tx(1)
+        actor = rng.randrange(NC + 1)
+        if actor == NC:                 # producer issues the next block
+            if next_issue < total:
+                s, r = next_issue % S, next_issue // S
+                if empty[s].try_wait((r & 1) ^ 1):
+                    full[s].expect_tx(1)
+                    stage_tag[s] = ("landing", next_issue)
+                    in_flight.append((t + rng.randint(1, 40), s, next_issue))
+                    next_issue += 1
+            continue
+        c = cons[actor]
+        if done[actor]:
+            continue
+        if c["at_merge"]:               # merge barrier: all consumers of the item
+            if merge_arrived[c["it"]] == NC:
+                c["it"] += 1
+                c["at_merge"] = False
+                if c["it"] == len(items):
+                    done[actor] = True
+                else:
+                    c["list"], c["pos"] = blocks_of(actor, c["it"]), 0
+            continue
+        if c["pos"] == len(c["list"]):
+            merge_arrived[c["it"]] += 1
+            c["at_merge"] = True
+            continue
+        blk = c["list"][c["pos"]]
+        s, r = blk % S, blk // S
+        if full[s].try_wait(r & 1):
+            if stage_tag[s] != blk:
+                stale += 1
+            empty[s].arrive()
+            c["pos"] += 1
+    return stale
+
+
+def random_items(rng, n):
+    return [rng.randint(1, 40) for _ in range(n)]
+
+
+@pytest.mark.parametrize("S,NC", [(4, 4), (8, 4), (12, 4), (8, 2), (8, 8)])
+def test_global_assignment_never_reads_a_stale_stage(S, NC):
+    rng = random.Random(S * 100 + NC)
+    for seed in range(40):
+        assert simulate(S, NC, "global", random_items(rng, 12), seed) == 0
+
+
+def test_item_relative_assignment_with_six_stages_is_unsafe():
+    rng = random.Random(7)
+    results = [simulate(6, 4, "item", random_items(rng, 12), seed) for seed in range(10)]
+    assert any(r != 0 for r in results)     # stale reads or deadlock
