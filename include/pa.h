@@ -157,6 +157,23 @@ int pa_cache_write(const void* d_k, const void* d_v, const int64_t* d_slot_mappi
                    void* stream);
 
 /* ------------------------------------------------------------------------
+ * Copy-on-write block copy.  [P4] section 03: a block shared by several
+ * sequences is kept once and copied when one holder writes into it; the
+ * allocator reports the (source, destination) pairs in pa_seq_append_slots.
+ *
+ * For each pair i, block d_dst[i] becomes a copy of block d_src[i]: every KV
+ * head's 16 rows, in K and in V (bit copy).  d_src, d_dst: [n_pairs] int32,
+ * device.  A pair naming a block outside [0, num_blocks) is skipped.
+ * Destinations must be distinct and must not be the source of another pair
+ * in the same call (true of the allocator's pairs: destinations come fresh
+ * from the free queue); otherwise the result is unspecified.  Enqueue it
+ * before the cache write that caused the copy.
+ * ---------------------------------------------------------------------- */
+int pa_copy_blocks(void* d_k_cache, void* d_v_cache, int64_t num_blocks, int32_t num_kv_heads,
+                   int32_t head_dim, const int32_t* d_src, const int32_t* d_dst, int32_t n_pairs,
+                   void* stream);
+
+/* ------------------------------------------------------------------------
  * Decode attention.  [P4] section 03: the maths of scaled dot-product
  * attention does not change under paging, only where K and V are read
  * from; the kernel follows the block table to gather them.  For every

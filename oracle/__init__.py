@@ -7,8 +7,9 @@ oracle imports nothing from the product.
 
 Parts:
 
-* ``pa_oracle.c`` -- cache write, block-table gather and textbook softmax
-  attention in fp64 (built to ``liboracle.so`` by :func:`build`).
+* ``pa_oracle.c`` -- cache write, copy-on-write block copy, block-table
+  gather and textbook softmax attention in fp64 (built to ``liboracle.so``
+  by :func:`build`).
 * :mod:`oracle.allocator` -- the block allocator model (free queue, ref
   counts, copy-on-write).
 * :func:`kv_bytes_per_token` -- the pages' KV size formula.
@@ -63,6 +64,8 @@ class OracleLib:
         lib.oracle_bits_to_double.restype = None
         lib.oracle_cache_write.argtypes = [P, P, P, i64, i32, i32, i32, P, P, i64]
         lib.oracle_cache_write.restype = i64
+        lib.oracle_copy_blocks.argtypes = [P, P, i64, i32, i32, i32, P, P, i64]
+        lib.oracle_copy_blocks.restype = i64
         lib.oracle_gather.argtypes = [P, ctypes.c_int, P, i32, i32, i32, i32, i32, P]
         lib.oracle_gather.restype = None
         lib.oracle_decode.argtypes = [P, P, P, ctypes.c_int, P, i32, P, i32, i32, i32, i32, i32,
@@ -131,6 +134,21 @@ def cache_write(k, v, slot_mapping, k_cache, v_cache, block_size=16, handle=None
     assert kc.shape == (nb, Hkv, block_size, D) and vc.shape == kc.shape
     bad = _load(handle).oracle_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, block_size,
                                      _ptr(kc), _ptr(vc), nb)
+    return kc, vc, int(bad)
+
+
+def copy_blocks(k_cache, v_cache, src, dst, block_size=16, handle=None):
+    """Copies of the caches with block src[i] copied to block dst[i], K and V.
+
+    Returns (k_cache', v_cache', n_skipped) -- pairs naming a block outside
+    the pool are skipped.
+    """
+    kc, vc = np.array(k_cache, np.uint16, copy=True), np.array(v_cache, np.uint16, copy=True)
+    src, dst = _c(np.asarray(src, np.int32), np.int32), _c(np.asarray(dst, np.int32), np.int32)
+    nb, Hkv, bs, D = kc.shape
+    assert bs == block_size and vc.shape == kc.shape and src.shape == dst.shape
+    bad = _load(handle).oracle_copy_blocks(_ptr(kc), _ptr(vc), nb, Hkv, D, block_size, _ptr(src),
+                                           _ptr(dst), src.size)
     return kc, vc, int(bad)
 
 

@@ -22,6 +22,9 @@
  *       "vLLM Nedir?", section "Bir istek motorun icinde", step 2
  *       (allocate_slots); "vLLM ve Triton", section 03, step 3.
  *
+ *   - Copy-on-write: a shared block is copied to a fresh block before one of
+ *     its holders writes into it.  "vLLM ve Triton", section 03.
+ *
  *   - Attention: the maths of scaled dot-product attention is unchanged by
  *     paging, only where K and V are read from changes:
  *       out = softmax(q K^T / sqrt(d_k)) V  over the sequence's tokens.
@@ -123,6 +126,33 @@ int64_t oracle_cache_write(const uint16_t* k, const uint16_t* v, const int64_t* 
         }
     }
     return out_of_range;
+}
+
+/* ---- copy-on-write block copy ---- */
+
+/*
+ * For every pair i: every KV head's 16 rows of block src[i] are copied to
+ * block dst[i], in K and in V.  A block shared by several sequences is
+ * copied when one holder writes into it ("vLLM ve Triton ile maliyet
+ * optimizasyonu", section 03, the copy-on-write paragraph).  Pairs with an
+ * id outside the pool are skipped (counted in the return value).
+ */
+int64_t oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, int64_t num_blocks,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                           const int32_t* src, const int32_t* dst, int64_t n_pairs) {
+    int64_t skipped = 0;
+    int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;
+    for (int64_t i = 0; i < n_pairs; ++i) {
+        if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks) {
+            ++skipped;
+            continue;
+        }
+        for (int64_t e = 0; e < per_block; ++e) {
+            k_cache[dst[i] * per_block + e] = k_cache[src[i] * per_block + e];
+            v_cache[dst[i] * per_block + e] = v_cache[src[i] * per_block + e];
+        }
+    }
+    return skipped;
 }
 
 /* ---- gather ---- */

@@ -55,6 +55,7 @@ _SIGS = {
     "pa_seq_block_table": ([P, P, I32, I32, P, P], ctypes.c_int),
     "pa_alloc_stats": ([P, P], ctypes.c_int),
     "pa_cache_write": ([P, P, P, I32, I32, I32, P, P, I64, I32, P], ctypes.c_int),
+    "pa_copy_blocks": ([P, P, I64, I32, I32, P, P, I32, P], ctypes.c_int),
     "pa_decode_workspace_bytes": ([I32, I32, I32, I32], SZ),
     "pa_decode": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, SZ, P],
                   ctypes.c_int),
@@ -122,6 +123,16 @@ def pa_cache_write(k, v, slot_mapping, k_cache, v_cache, dtype=None, stream=None
     rc = lib().pa_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, H, D, _ptr(k_cache),
                               _ptr(v_cache), k_cache.shape[0], _dtype_code(k, dtype), _stream(stream))
     _check(rc, "pa_cache_write")
+
+
+def pa_copy_blocks(k_cache, v_cache, src, dst, stream=None):
+    """Copy-on-write: block dst[i] of both caches becomes a copy of block src[i]."""
+    _need_cuda(k_cache, v_cache, src, dst)
+    assert src.dtype == torch.int32 and dst.dtype == torch.int32 and src.shape == dst.shape
+    NB, Hkv, _, D = k_cache.shape
+    rc = lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), NB, Hkv, D, _ptr(src), _ptr(dst),
+                              src.numel(), _stream(stream))
+    _check(rc, "pa_copy_blocks")
 
 
 def pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len):

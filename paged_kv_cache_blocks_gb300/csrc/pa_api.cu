@@ -58,6 +58,25 @@ int pa_cache_write(const void* d_k, const void* d_v, const int64_t* d_slot_mappi
   return rc ? fail(rc, why) : PA_OK;
 }
 
+int pa_copy_blocks(void* d_k_cache, void* d_v_cache, int64_t num_blocks, int32_t num_kv_heads,
+                   int32_t head_dim, const int32_t* d_src, const int32_t* d_dst, int32_t n_pairs,
+                   void* stream) {
+  if (n_pairs < 0) return fail(PA_ERR_INVALID, "pa_copy_blocks: n_pairs < 0");
+  if (!supported_head_dim(head_dim))
+    return fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: head_dim must be 64 or 128");
+  if (num_kv_heads <= 0 || num_blocks <= 0)
+    return fail(PA_ERR_INVALID, "pa_copy_blocks: num_kv_heads and num_blocks must be > 0");
+  if (n_pairs == 0) return PA_OK;
+  if (!d_k_cache || !d_v_cache || !d_src || !d_dst)
+    return fail(PA_ERR_INVALID, "pa_copy_blocks: NULL pointer");
+  if (!aligned(d_k_cache, 16) || !aligned(d_v_cache, 16) || !aligned(d_src, 4) || !aligned(d_dst, 4))
+    return fail(PA_ERR_INVALID, "pa_copy_blocks: caches must be 16-byte aligned");
+  std::string why;
+  int rc = pa::copy_blocks_launch(d_k_cache, d_v_cache, num_blocks, num_kv_heads, head_dim, d_src,
+                                  d_dst, n_pairs, stream, &why);
+  return rc ? fail(rc, why) : PA_OK;
+}
+
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                  int32_t max_seq_len) {
   if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;

@@ -1,4 +1,6 @@
-// Cache write for sm_103a: scatter each new token's K and V rows into the
+// Cache write and copy-on-write block copy for sm_103a.
+//
+// Cache write: scatter each new token's K and V rows into the
 // paged cache through the slot mapping ("vLLM Nedir? PagedAttention ile
 // Production LLM Serving", section "Bir istek motorun icinde", step 2;
 // "vLLM ve Triton ile maliyet optimizasyonu", section 03, steps 1-3).
@@ -53,6 +55,41 @@ int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("cache_write launch: ") + cudaGetErrorString(e);
+    return 5;
+  }
+  return 0;
+}
+
+// Copy-on-write block copy ("vLLM ve Triton ile maliyet optimizasyonu",
+// section 03: a shared block is copied when one holder writes into it).
+// One CTA per (pair, K or V): the whole block -- every KV head's 16 rows -- is
+// contiguous in the [num_blocks][num_kv_heads][16][head_dim] layout, so each
+// CTA streams it with 16-byte loads and stores.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
+                       int64_t num_blocks, int chunks_per_block) {
+  const int i = blockIdx.x;
+  const int32_t s = src[i], d = dst[i];
+  if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks || s == d) return;
+  uint4* cache = blockIdx.y == 0 ? k_cache : v_cache;
+  const uint4* from = cache + static_cast<int64_t>(s) * chunks_per_block;
+  uint4* to = cache + static_cast<int64_t>(d) * chunks_per_block;
+  for (int c = threadIdx.x; c < chunks_per_block; c += blockDim.x) to[c] = from[c];
+}
+
+int copy_blocks_launch(void* k_cache, void* v_cache, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t head_dim, const int32_t* src, const int32_t* dst, int32_t n_pairs,
+                       void* stream, std::string* why) {
+  if (n_pairs == 0) return 0;
+  const int chunks_per_block = num_kv_heads * kBlock * head_dim * 2 / 16;
+  dim3 grid(static_cast<unsigned>(n_pairs), 2);
+  copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src, dst, num_blocks,
+      chunks_per_block);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("copy_blocks launch: ") + cudaGetErrorString(e);
     return 5;
   }
   return 0;

@@ -43,4 +43,8 @@ int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping
                        int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
                        int64_t num_blocks, void* stream, std::string* why);
 
+int copy_blocks_launch(void* k_cache, void* v_cache, int64_t num_blocks, int32_t num_kv_heads,
+                       int32_t head_dim, const int32_t* src, const int32_t* dst, int32_t n_pairs,
+                       void* stream, std::string* why);
+
 }  // namespace pa

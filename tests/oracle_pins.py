@@ -118,6 +118,20 @@ def pin_cache_write_golden(oracle, handle=None):
     assert np.array_equal(vc, ev), g["cite"]
 
 
+def pin_copy_blocks_golden(oracle, handle=None):
+    g = json.load(open(os.path.join(GOLD, "copy_blocks_example.json")))
+    nb, H, D = g["num_blocks"], g["num_kv_heads"], g["head_dim"]
+    b, h, r, d = np.meshgrid(np.arange(nb), np.arange(H), np.arange(16), np.arange(D), indexing="ij")
+    vals = (1000 * b + 100 * h + 10 * (r % 10) + d).astype(np.float16).view(np.uint16)
+    kc, vc = vals.copy(), (vals + 1).astype(np.uint16)
+    k2, v2, skipped = oracle.copy_blocks(kc, vc, g["src"], g["dst"],
+                                         handle=handle)
+    assert skipped == g["expect_skipped"], g["cite"]
+    for blk, srcb in enumerate(g["expect_block_source"]):
+        assert np.array_equal(k2[blk], kc[srcb]), (blk, g["cite"])
+        assert np.array_equal(v2[blk], vc[srcb]), (blk, g["cite"])
+
+
 def pin_gather_is_contiguous_source(oracle, handle=None):
     for batch in small_batches():
         w = batch.workload
@@ -214,5 +228,6 @@ def pin_closed_forms(oracle, handle=None):
     assert np.array_equal(o, np.zeros_like(o))
 
 
-ALL_PINS = [pin_kv_bytes, pin_bits, pin_cache_write_golden, pin_gather_is_contiguous_source,
+ALL_PINS = [pin_kv_bytes, pin_bits, pin_cache_write_golden, pin_copy_blocks_golden,
+            pin_gather_is_contiguous_source,
             pin_matches_sdpa, pin_relabel_invariance, pin_closed_forms]

@@ -27,6 +27,10 @@ MUTANTS = {
     "write_row_reversed": ("* block_size + off) * (int64_t)head_dim",
                            "* block_size + (block_size - 1 - off)) * (int64_t)head_dim"),
     "negative_slot_written": ("if (s < 0) continue;", "if (s < 0) s = 0;"),
+    "copy_v_from_k": ("v_cache[dst[i] * per_block + e] = v_cache[src[i] * per_block + e];",
+                      "v_cache[dst[i] * per_block + e] = k_cache[src[i] * per_block + e];"),
+    "copy_direction": ("k_cache[dst[i] * per_block + e] = k_cache[src[i] * per_block + e];",
+                       "k_cache[src[i] * per_block + e] = k_cache[dst[i] * per_block + e];"),
 }
 
 
