@@ -303,7 +303,13 @@ def run_pa(args, rank, world, local_rank):
     lens = torch.from_numpy(b.seq_lens).to(dev)
     slots = torch.from_numpy(b.slot_mapping).to(dev)
     msl = int(b.seq_lens.max())
-    ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
+    grouped = args.grouped and any(m > 1 and p > 0 for m, p in b.groups)
+    if grouped:
+        goff, gpre = (torch.from_numpy(x).to(dev) for x in b.group_arrays())
+        ws = torch.empty(pa.pa_decode_grouped_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8,
+                         device=dev)
+    else:
+        ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
     out = torch.empty_like(layers[0][0])
     variant = VARIANTS[args.variant]
     stream = torch.cuda.current_stream()
@@ -311,8 +317,12 @@ def run_pa(args, rank, world, local_rank):
     def step(evs=None):
         for li, (q, kc, vc, nk, nv) in enumerate(layers):
             pa.pa_cache_write(nk, nv, slots, kc, vc)
-            pa.pa_decode(q, kc, vc, tab, lens, w.scale, max_seq_len=msl, out=out, workspace=ws,
-                         variant=variant, events=evs[li] if evs else None)
+            if grouped:
+                pa.pa_decode_grouped(q, kc, vc, tab, lens, w.scale, goff, gpre, max_seq_len=msl,
+                                     out=out, workspace=ws)
+            else:
+                pa.pa_decode(q, kc, vc, tab, lens, w.scale, max_seq_len=msl, out=out, workspace=ws,
+                             variant=variant, events=evs[li] if evs else None)
 
     for _ in range(args.warmup):
         step()
@@ -342,7 +352,7 @@ def run_pa(args, rank, world, local_rank):
         time.sleep(0.15)
         sampler.stop()
     ms_total = start.elapsed_time(stop)
-    kern_ms = [a.elapsed_time(z) for row in ev_pairs for a, z in row]
+    kern_ms = [a.elapsed_time(z) for row in ev_pairs for a, z in row] if not grouped else [float("nan")]
     ms_step = reduce_max(ms_total / args.steps, dist, dev)
 
     kvb = logical_kv_bytes(b.seq_lens, Hkv, D) * nl
@@ -381,6 +391,8 @@ def run_pa(args, rank, world, local_rank):
                          "no flush",
                    "step": f"{nl} x (pa_cache_write of one new token per sequence + pa_decode)",
                    "variant": args.variant, "partition_tokens": part_tokens,
+                   "shared_prefix": "pa_decode_grouped (prefix read once per group and KV head)"
+                                    if grouped else "none (pa_decode)",
                    "parallelism": f"replicas x{world}"},
         "seqs_steps_per_s": job_throughput(B, world, ms_step * 1e-3),
         "hbm_frac_step": (kvb / (ms_step * 1e-3) / 1e9) / peak,
@@ -545,6 +557,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--grouped", action="store_true",
+                    help="decode shared-prefix groups with pa_decode_grouped (fullstep)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -60,7 +60,9 @@ enum { PA_BLOCK_SIZE = 16 };
 enum {
     PA_DEVERR_SEQ_LEN = 1,   /* a seq_len < 0 or > max_seq_len: clamped into range */
     PA_DEVERR_BLOCK_ID = 2,  /* a block id outside [0, num_blocks): read as zeros */
-    PA_DEVERR_TIMEOUT = 4    /* an internal wait gave up; the output is not valid */
+    PA_DEVERR_TIMEOUT = 4,   /* an internal wait gave up; the output is not valid */
+    PA_DEVERR_GROUP = 8      /* pa_decode_grouped: a group's offsets or shared prefix were
+                                invalid; those sequences were decoded without sharing */
 };
 
 const char* pa_last_error_string(void);
@@ -225,6 +227,38 @@ int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache,
                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
                  int32_t dtype, void* d_out, void* d_workspace, size_t workspace_bytes,
                  void* stream, const pa_decode_opts* opts);
+
+/* ------------------------------------------------------------------------
+ * Decode with shared prefixes ("cascade").  [P3] "PagedAttention" last
+ * paragraph and [P4] section 03: requests with a common prefix (a shared
+ * system prompt, beam search, parallel sampling) point at the same physical
+ * blocks.  Same result as pa_decode; the shared blocks are read from HBM
+ * once per (group, KV head) instead of once per sequence, and their
+ * attention is computed for all members at once on the tensor cores.
+ *
+ *   d_group_offsets       [num_groups + 1] int32, device: group g is the
+ *                         contiguous sequences [off[g], off[g+1]);
+ *                         off[0] = 0, off[num_groups] = num_seqs, non-decreasing
+ *   d_group_prefix_tokens [num_groups] int32, device: tokens every member of g
+ *                         holds in the same physical blocks as the group's
+ *                         first member (a multiple of 16, at most any member's
+ *                         length; 0 = no sharing).  The caller vouches that
+ *                         the members' tables agree on those blocks (the
+ *                         allocator's forks guarantee it).
+ *   workspace             >= pa_decode_grouped_workspace_bytes(...)
+ *
+ * Invalid offsets or prefixes are flagged (PA_DEVERR_GROUP) and the affected
+ * sequences are decoded without sharing -- still the correct result. */
+size_t pa_decode_grouped_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                         int32_t max_seq_len);
+
+int pa_decode_grouped(const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                      int64_t num_blocks, const int32_t* d_block_tables, int32_t max_blocks_per_seq,
+                      const int32_t* d_seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                      int32_t dtype, const int32_t* d_group_offsets,
+                      const int32_t* d_group_prefix_tokens, int32_t num_groups, void* d_out,
+                      void* d_workspace, size_t workspace_bytes, void* stream);
 
 /* Waits for `stream`, then reads the device error bits the last decode
  * using this workspace left (PA_DEVERR_*; 0 = clean) into *error_bits.

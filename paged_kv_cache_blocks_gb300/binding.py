@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_UNSUPPORTED, PA_ERR_SHARED_WRITE, PA_ERR_CUDA, \
     PA_ERR_DEVICE = range(7)
 PA_F16, PA_BF16 = 0, 1
-PA_DEVERR_SEQ_LEN, PA_DEVERR_BLOCK_ID, PA_DEVERR_TIMEOUT = 1, 2, 4
+PA_DEVERR_SEQ_LEN, PA_DEVERR_BLOCK_ID, PA_DEVERR_TIMEOUT, PA_DEVERR_GROUP = 1, 2, 4, 8
 BLOCK_SIZE = 16
 
 _STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID", 2: "PA_ERR_OOM", 3: "PA_ERR_UNSUPPORTED",
@@ -62,6 +62,9 @@ _SIGS = {
     "pa_decode_ex": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, SZ, P, P],
                      ctypes.c_int),
     "pa_decode_check": ([P, P, P], ctypes.c_int),
+    "pa_decode_grouped_workspace_bytes": ([I32, I32, I32, I32], SZ),
+    "pa_decode_grouped": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, I32, P,
+                           P, SZ, P], ctypes.c_int),
     "pa_decode_noalloc": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P],
                           ctypes.c_int),
 }
@@ -192,6 +195,35 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, max_se
                                  max_seq_len, Hq, k_cache.shape[1], D, float(scale),
                                  _dtype_code(q, dtype), _ptr(out), _stream(stream))
     _check(rc, "pa_decode_noalloc")
+    return out
+
+
+def pa_decode_grouped_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len):
+    return int(lib().pa_decode_grouped_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len))
+
+
+def pa_decode_grouped(q, k_cache, v_cache, block_tables, seq_lens, scale, group_offsets,
+                      group_prefix_tokens, max_seq_len=0, out=None, workspace=None, dtype=None,
+                      stream=None):
+    """pa_decode where contiguous groups of sequences share a prefix:
+    group_offsets [G+1] and group_prefix_tokens [G] are int32 CUDA tensors."""
+    _need_cuda(q, k_cache, v_cache, block_tables, seq_lens, group_offsets, group_prefix_tokens)
+    assert group_offsets.dtype == torch.int32 and group_prefix_tokens.dtype == torch.int32
+    B, Hq, D = q.shape
+    NB, Hkv = k_cache.shape[0], k_cache.shape[1]
+    mb = block_tables.shape[1]
+    msl = max_seq_len if max_seq_len > 0 else mb * BLOCK_SIZE
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(max(pa_decode_grouped_workspace_bytes(B, Hq, D, msl), 256),
+                                dtype=torch.uint8, device=q.device)
+    rc = lib().pa_decode_grouped(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), mb,
+                                 _ptr(seq_lens), B, msl, Hq, Hkv, D, float(scale),
+                                 _dtype_code(q, dtype), _ptr(group_offsets),
+                                 _ptr(group_prefix_tokens), group_prefix_tokens.numel(), _ptr(out),
+                                 _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "pa_decode_grouped")
     return out
 
 

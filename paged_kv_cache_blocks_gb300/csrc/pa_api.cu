@@ -83,11 +83,17 @@ size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t 
   return pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len);
 }
 
-int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,
-                 const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
-                 int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
-                 int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
-                 size_t workspace_bytes, void* stream, const pa_decode_opts* opts) {
+}  // extern "C"
+
+namespace {
+
+int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,
+                  const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
+                  int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                  int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
+                  size_t workspace_bytes, void* stream, const pa_decode_opts* opts,
+                  const int32_t* d_group_offsets, const int32_t* d_group_prefix_tokens,
+                  int32_t num_groups) {
   if (num_seqs < 0) return fail(PA_ERR_INVALID, "pa_decode: num_seqs < 0");
   if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype");
   if (!supported_head_dim(head_dim))
@@ -120,9 +126,16 @@ int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache, 
       !aligned(d_workspace, 256) || !aligned(d_block_tables, 4) || !aligned(d_seq_lens, 4))
     return fail(PA_ERR_INVALID,
                 "pa_decode: q, out and caches must be 16-byte aligned, the workspace 256-byte aligned");
-  const size_t need = pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len);
+  if (num_groups < 0 || num_groups > num_seqs)
+    return fail(PA_ERR_INVALID, "pa_decode_grouped: num_groups must be in [1, num_seqs]");
+  if (num_groups > 0 && (!d_group_offsets || !d_group_prefix_tokens))
+    return fail(PA_ERR_INVALID, "pa_decode_grouped: NULL group array");
+  const size_t need = pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len,
+                                                 num_groups > 0);
   if (workspace_bytes < need)
-    return fail(PA_ERR_INVALID, "pa_decode: workspace smaller than pa_decode_workspace_bytes()");
+    return fail(PA_ERR_INVALID, num_groups > 0
+                                    ? "pa_decode_grouped: workspace smaller than pa_decode_grouped_workspace_bytes()"
+                                    : "pa_decode: workspace smaller than pa_decode_workspace_bytes()");
 
   pa::DecodeArgs a;
   a.q = d_q;
@@ -145,9 +158,47 @@ int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache, 
   a.variant = opts ? opts->variant : 0;
   a.ev_before = opts ? opts->event_before_main : nullptr;
   a.ev_after = opts ? opts->event_after_main : nullptr;
+  a.group_off = d_group_offsets;
+  a.group_prefix = d_group_prefix_tokens;
+  a.num_groups = num_groups;
   std::string why;
   int rc = pa::decode_launch(a, &why);
   return rc ? fail(rc, why) : PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,
+                 const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
+                 int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                 int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
+                 size_t workspace_bytes, void* stream, const pa_decode_opts* opts) {
+  return decode_common(d_q, d_k_cache, d_v_cache, num_blocks, d_block_tables, max_blocks_per_seq,
+                       d_seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, scale,
+                       dtype, d_out, d_workspace, workspace_bytes, stream, opts, nullptr, nullptr, 0);
+}
+
+size_t pa_decode_grouped_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                         int32_t max_seq_len) {
+  if (num_seqs < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  return pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, true);
+}
+
+int pa_decode_grouped(const void* d_q, const void* d_k_cache, const void* d_v_cache,
+                      int64_t num_blocks, const int32_t* d_block_tables, int32_t max_blocks_per_seq,
+                      const int32_t* d_seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
+                      int32_t dtype, const int32_t* d_group_offsets,
+                      const int32_t* d_group_prefix_tokens, int32_t num_groups, void* d_out,
+                      void* d_workspace, size_t workspace_bytes, void* stream) {
+  if (num_groups <= 0 && num_seqs > 0)
+    return fail(PA_ERR_INVALID, "pa_decode_grouped: num_groups must be >= 1");
+  return decode_common(d_q, d_k_cache, d_v_cache, num_blocks, d_block_tables, max_blocks_per_seq,
+                       d_seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, scale,
+                       dtype, d_out, d_workspace, workspace_bytes, stream, nullptr, d_group_offsets,
+                       d_group_prefix_tokens, num_groups);
 }
 
 int pa_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,

@@ -35,6 +35,7 @@
 //        O^T += V^T P with P moved into operand layout by movmatrix.
 #include <cuda.h>
 
+#include <mutex>
 #include <type_traits>
 
 #include "pa_device.cuh"
@@ -43,7 +44,7 @@
 namespace pa {
 
 struct ItemInfo {
-  int32_t b, h, p, len, nparts, nblk, g0, part;
+  int32_t b, h, p, len, nparts, nblk, g0, part, start, pad0;
 };
 
 struct DecodeParams {
@@ -55,6 +56,13 @@ struct DecodeParams {
   PartInfo* parts;
   int2* seq_first;
   int32_t* split;
+  int4* seq_prefix;   // per sequence: first prefix partial, group size, chunks, prefix tokens
+  int4* group_info;   // per group: prefix partial base, item base, chunks, row tiles
+  int32_t* group_bad; // per group: shared prefix rejected
+  int4* pitems;       // shared-prefix work items (group, chunk, row tile)
+  const int32_t* group_off;     // [num_groups + 1] or null
+  const int32_t* group_prefix;  // [num_groups] or null
+  int32_t num_groups;
   float2* ml;
   float* acc;
   int64_t num_blocks;
@@ -104,32 +112,84 @@ __device__ int block_exclusive_scan(int v, int* sw, int* total) {
   return res;
 }
 
+// Group of sequence b: the last g with group_off[g] <= b.
+__device__ __forceinline__ int group_of(const DecodeParams& P, int b) {
+  int lo = 0, hi = P.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.group_off[mid] <= b) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
 // Partition size: the largest of 512, 1024, 2048 tokens that still leaves at
 // least `target_full_items` full-partition work items, so long sequences make
 // fewer partials to merge while the persistent grid stays balanced.  Partial
 // (tail) partitions are ordered longest first by a counting sort on their
 // size, so the dynamic work queue ends on the shortest items.
+//
+// Grouped decode: sequences come in contiguous groups whose members share
+// their first `prefix` tokens (whole blocks).  The attention kernel then only
+// covers each member's own tokens [prefix, len); the prefix is cut into
+// 256-token chunks handled once per (group, KV head) by the prefix kernel for
+// all members together.  A group whose prefix is not a multiple of 16 or
+// longer than one of its members is flagged and decoded without sharing.
 __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint4,
                                                     int target_full_items) {
   __shared__ int sw[32];
   __shared__ int s_full[3];
   __shared__ int s_hist[kMaxPartBlocks + 1];
-  __shared__ int s_nsplit, s_total_tail;
+  __shared__ int s_nsplit, s_total_tail, s_groups_ok;
   const int tid = threadIdx.x;
   if (tid == 0) {
     P.ws->error_bits = 0;
     s_full[0] = s_full[1] = s_full[2] = 0;
     s_nsplit = 0;
+    s_groups_ok = 1;
   }
   for (int i = tid; i <= kMaxPartBlocks; i += blockDim.x) s_hist[i] = 0;
   __syncthreads();
+  const int ng = P.num_groups;
+  if (ng > 0) {
+    for (int g = tid; g < ng; g += blockDim.x) {
+      const int a = P.group_off[g], e = P.group_off[g + 1];
+      if (a < 0 || e < a || e > P.num_seqs || (g == 0 && a != 0) || (g == ng - 1 && e != P.num_seqs))
+        s_groups_ok = 0;
+      P.group_bad[g] = 0;
+    }
+  }
+  __syncthreads();
+  const bool use_groups = ng > 0 && s_groups_ok;
+  if (ng > 0 && !use_groups && tid == 0) atomicOr(&P.ws->error_bits, kErrGroup);
+  if (use_groups) {
+    for (int b = tid; b < P.num_seqs; b += blockDim.x) {
+      const int g = group_of(P, b);
+      const int pre = P.group_prefix[g];
+      if (pre < 0 || pre % kBlock != 0 || pre > clamp_len(P, b)) {
+        atomicOr(&P.group_bad[g], 1);
+        atomicOr(&P.ws->error_bits, kErrGroup);
+      }
+    }
+  }
+  __syncthreads();
+  // first token of the attention kernel's partitions for each sequence,
+  // kept in seq_prefix[b].w (rewritten in full in pass B)
+  if (use_groups) {
+    for (int b = tid; b < P.num_seqs; b += blockDim.x) {
+      const int g = group_of(P, b);
+      P.seq_prefix[b] = make_int4(g, 0, 0, P.group_bad[g] ? 0 : P.group_prefix[g]);
+    }
+  }
+  __syncthreads();
+  auto suffix_start = [&](int b) -> int { return use_groups ? P.seq_prefix[b].w : 0; };
   // pass A: full partitions for each candidate size
   int f1 = 0, f2 = 0, f4 = 0;
   for (int b = tid; b < P.num_seqs; b += blockDim.x) {
-    const int L = clamp_len(P, b);
-    f1 += L / kPartTokens;
-    f2 += L / (2 * kPartTokens);
-    f4 += L / (4 * kPartTokens);
+    const int n = clamp_len(P, b) - suffix_start(b);
+    f1 += n / kPartTokens;
+    f2 += n / (2 * kPartTokens);
+    f4 += n / (4 * kPartTokens);
   }
   atomicAdd(&s_full[0], f1);
   atomicAdd(&s_full[1], f2);
@@ -145,7 +205,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
   }
   // tails by size (blocks), then start offsets in descending size order
   for (int b = tid; b < P.num_seqs; b += blockDim.x) {
-    const int r = P.seq_lens[b] < 0 ? 0 : clamp_len(P, b) % pt;
+    const int r = (clamp_len(P, b) - suffix_start(b)) % pt;
     if (r) atomicAdd(&s_hist[(r + kBlock - 1) / kBlock], 1);
   }
   __syncthreads();
@@ -159,24 +219,65 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
     s_total_tail = run;
   }
   __syncthreads();
+  const int n_suffix = total_full + s_total_tail;
+  // groups: prefix chunks, row tiles, partial and work-item bases
+  int n_pitems = 0;
+  if (use_groups) {
+    int carry_r = 0, carry_i = 0;
+    for (int base = 0; base < ng; base += blockDim.x) {
+      const int g = base + tid;
+      int nch = 0, M = 0, nt = 0;
+      if (g < ng) {
+        M = P.group_off[g + 1] - P.group_off[g];
+        const int pre = P.group_bad[g] ? 0 : P.group_prefix[g];
+        nch = (pre > 0 && M > 0) ? (pre + kPrefixChunkTokens - 1) / kPrefixChunkTokens : 0;
+        nt = (M * P.G + kPrefixRows - 1) / kPrefixRows;
+      }
+      int tot_r, tot_i;
+      const int ro = block_exclusive_scan(nch * M, sw, &tot_r);
+      const int io = block_exclusive_scan(nch * nt, sw, &tot_i);
+      if (g < ng) {
+        P.group_info[g] = make_int4(n_suffix + carry_r + ro, carry_i + io, nch, nt);
+        for (int c = 0; c < nch; ++c)
+          for (int t = 0; t < nt; ++t) P.pitems[carry_i + io + c * nt + t] = make_int4(g, c, t, 0);
+      }
+      carry_r += tot_r;
+      carry_i += tot_i;
+    }
+    n_pitems = carry_i;
+  }
+  __syncthreads();
   // pass B: full partitions in sequence order, tails at their sorted slots
   int carry_full = 0;
   for (int base = 0; base < P.num_seqs; base += blockDim.x) {
     const int b = base + tid;
-    int L = 0;
-    if (b < P.num_seqs) L = clamp_len(P, b);
-    const int nfull = L / pt;
-    const int r = L % pt;
+    int L = 0, st = 0;
+    if (b < P.num_seqs) {
+      L = clamp_len(P, b);
+      st = suffix_start(b);
+    }
+    const int nfull = (L - st) / pt;
+    const int r = (L - st) % pt;
     int tot_f;
     const int fo = block_exclusive_scan(nfull, sw, &tot_f);
     if (b < P.num_seqs) {
-      const int nparts = nfull + (r != 0);
+      int4 sp = make_int4(0, 0, 0, st);
+      if (use_groups) {
+        const int g = P.seq_prefix[b].x;
+        const int4 gi = P.group_info[g];
+        if (gi.z > 0) {
+          const int M = P.group_off[g + 1] - P.group_off[g];
+          sp = make_int4(gi.x + (b - P.group_off[g]), M, gi.z, st);
+        }
+      }
+      P.seq_prefix[b] = sp;
+      const int nparts = nfull + (r != 0) + sp.z;
       const int first = carry_full + fo;
       const int tail_idx = r ? total_full + atomicAdd(&s_hist[(r + kBlock - 1) / kBlock], 1) : -1;
       P.seq_first[b] = make_int2(first, tail_idx);
-      for (int p = 0; p < nfull; ++p) P.parts[first + p] = PartInfo{b, p, L, nparts};
-      if (r) P.parts[tail_idx] = PartInfo{b, nfull, L, nparts};
-      if (nparts > 1) P.split[atomicAdd(&s_nsplit, 1)] = b;
+      for (int p = 0; p < nfull; ++p) P.parts[first + p] = PartInfo{b, p, L, nparts, st, 0, 0, 0};
+      if (r) P.parts[tail_idx] = PartInfo{b, nfull, L, nparts, st, 0, 0, 0};
+      if (nparts > 1 || sp.z > 0) P.split[atomicAdd(&s_nsplit, 1)] = b;
       if (L == 0) {  // empty softmax: the output is defined as 0
         uint4* o = reinterpret_cast<uint4*>(P.out) + static_cast<int64_t>(b) * row_uint4;
         for (int i = 0; i < row_uint4; ++i) o[i] = make_uint4(0, 0, 0, 0);
@@ -186,13 +287,14 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
   }
   __syncthreads();
   if (tid == 0) {
-    const int n_parts = total_full + s_total_tail;
-    P.ws->n_parts = n_parts;
-    P.ws->n_items = n_parts * P.hkv;
+    P.ws->n_parts = n_suffix;
+    P.ws->n_suffix_parts = n_suffix;
+    P.ws->n_items = n_suffix * P.hkv;
     P.ws->next_item = 0;
     P.ws->n_split = s_nsplit;
     P.ws->next_split = 0;
     P.ws->part_tokens = pt;
+    P.ws->n_pitems = n_pitems;
   }
 }
 
@@ -492,7 +594,7 @@ constexpr size_t align_up_c(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 template <typename T, int D, int NC, int S, bool kFma>
 struct AttendCfg {
-  static_assert(S % NC == 0, "each ring stage must always be consumed by the same warp");
+  static_assert(S % NC == 0, "within an item, each ring stage must be consumed by one warp");
   static constexpr int kThreads = 32 * (NC + 1);
   static constexpr int kStageBytes = Tile<D>::kStageBytes;
   static constexpr size_t kStagesOff = 0;
@@ -575,7 +677,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       }
       const int part = item / P.hkv, h = item - part * P.hkv;
       const PartInfo pi = P.parts[part];
-      const int first_tok = pi.p * pt;
+      const int first_tok = pi.start + pi.p * pt;
       const int nblk = min(pt / kBlock, (pi.len - first_tok + kBlock - 1) / kBlock);
       const int32_t* trow = P.tables + static_cast<int64_t>(pi.b) * P.max_blocks + first_tok / kBlock;
       for (int j = lane; j < nblk; j += 32) {
@@ -588,7 +690,8 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       }
       __syncwarp();
       if (lane == 0) {
-        info[slot] = ItemInfo{pi.b, h, pi.p, pi.len, pi.nparts, nblk, static_cast<int32_t>(g), part};
+        info[slot] = ItemInfo{pi.b, h, pi.p, pi.len, pi.nparts, nblk, static_cast<int32_t>(g), part,
+                              pi.start, 0};
         mbar_arrive(&item_full[slot]);
         for (int j = 0; j < nblk && ok; ++j, ++g) {
           const int st = g % S;
@@ -637,12 +740,13 @@ __global__ void __launch_bounds__(32 * (NC + 1))
 
     st.begin(P, inf, lane, scr);
     bool alive = true;
-    // Block g of the CTA's stream goes to consumer g % NC.  With S a multiple
-    // of NC, every use of ring stage g % S is then consumed by the same warp,
-    // in order, so a parity wait can never be satisfied by an older phase of
-    // the stage (which would let a warp read a stage before its copy lands).
-    const int j0 = (w - static_cast<int>(static_cast<uint32_t>(inf.g0) % NC) + NC) % NC;
-    for (int j = j0; j < inf.nblk; j += NC) {
+    // Block j of the item goes to consumer j % NC, so which warp sums which
+    // blocks does not depend on scheduling (outputs are bit-reproducible).
+    // With S a multiple of NC, the uses of a ring stage inside one item all
+    // belong to one warp, in order, and items are separated by the merge
+    // barrier below, so a parity wait can never be satisfied by an older
+    // phase of its stage (which would read the stage before its copy lands).
+    for (int j = w; j < inf.nblk; j += NC) {
       const uint32_t gg = inf.g0 + j;
       const int s = gg % S;
       ok = mbar_wait(&full[s], (gg / S) & 1, abort_flag, err);
@@ -651,7 +755,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
         break;
       }
       const uint32_t sK = smem_u32(stages + static_cast<size_t>(s) * Cfg::kStageBytes);
-      const int nvalid = min(kBlock, inf.len - (inf.p * pt + j * kBlock));
+      const int nvalid = min(kBlock, inf.len - (inf.start + inf.p * pt + j * kBlock));
       st.block(sK, sK + Tile<D>::kKVBytes, nvalid, P.scale_log2, lane, scr);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -722,10 +826,12 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodePar
     const int h = wi - (wi / P.hkv) * P.hkv;
     const int64_t head0 = static_cast<int64_t>(h) * G;
     const int2 sf = P.seq_first[b];
+    const int4 sp = P.seq_prefix[b];  // shared-prefix partials: first, stride (group size), count
     int L = P.seq_lens[b];
     L = L < 0 ? 0 : (L > P.max_seq_len ? P.max_seq_len : L);
-    const int nfull = L / pt;
-    const int nparts = nfull + ((L % pt) != 0);
+    const int nfull = (L - sp.w) / pt;
+    const int nsuf = nfull + (((L - sp.w) % pt) != 0);
+    const int nparts = nsuf + sp.z;
     int e4[kE], gk[kE];
     float m[kE], l[kE];
     float4 o[kE];
@@ -745,7 +851,8 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodePar
       for (int u = 0; u < U; ++u) {
         const int p = p0 + u * kMergeSlices;
         if (p < nparts) {
-          const int64_t idx = p < nfull ? sf.x + p : sf.y;
+          const int64_t idx = p < nsuf ? (p < nfull ? sf.x + p : sf.y)
+                                       : static_cast<int64_t>(sp.x) + static_cast<int64_t>(p - nsuf) * sp.y;
 #pragma unroll
           for (int k = 0; k < kE; ++k)
             if (e4[k] < n4) {
@@ -811,6 +918,186 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodePar
         }
     }
     __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 4. shared-prefix attention (grouped decode)
+//
+// One work item = (group, 256-token chunk of the shared prefix, tile of 128
+// query rows, KV head).  The members of a group share the prefix's physical
+// blocks, so the chunk's K and V tiles are loaded once (TMA, 128-byte
+// swizzle) and every member's G query heads attend to them together: a real
+// [128 rows x head_dim] x [head_dim x 16 tokens] product per block, on the
+// tensor cores (mma.sync m16n8k16; eight warps, 16 query rows each, Q kept in
+// registers, P reused from the score accumulators as the PV operand).  Each
+// row's (max, sum, unnormalised output) over the chunk is a partial result
+// that the merge kernel folds into the member's output.
+
+constexpr int kPrefixWarps = kPrefixRows / 16;
+
+template <int D>
+struct PrefixCfg {
+  static constexpr int kStageBytes = Tile<D>::kStageBytes;
+  static constexpr size_t kBytes = static_cast<size_t>(kPrefixChunkBlocks) * kStageBytes + 64 + 1024;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kPrefixWarps * 32)
+    prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeParams P) {
+  using Cfg = PrefixCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPrefixChunkBlocks * Cfg::kStageBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
+  int* err = &P.ws->error_bits;
+  const int n_work = *reinterpret_cast<volatile int32_t*>(&P.ws->n_pitems) * P.hkv;
+  if (blockIdx.x >= n_work) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = P.G;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int64_t y_oob = P.num_blocks * P.hkv * kBlock;
+  uint32_t n_local = 0;
+  for (int wi = blockIdx.x; wi < n_work; wi += gridDim.x, ++n_local) {
+    const int4 item = P.pitems[wi / P.hkv];
+    const int h = wi - (wi / P.hkv) * P.hkv;
+    const int grp = item.x, chunk = item.y, tile = item.z;
+    const int off = P.group_off[grp];
+    const int M = P.group_off[grp + 1] - off;
+    const int4 gi = P.group_info[grp];
+    const int pre = P.group_prefix[grp];
+    const int nblk = min(kPrefixChunkBlocks, pre / kBlock - chunk * kPrefixChunkBlocks);
+    if (tid == 0) {
+      // the prefix blocks are those of the group's first member
+      const int32_t* trow = P.tables + static_cast<int64_t>(off) * P.max_blocks + chunk * kPrefixChunkBlocks;
+      mbar_arrive_expect_tx(bar, nblk * Cfg::kStageBytes);
+      for (int j = 0; j < nblk; ++j) {
+        int32_t id = trow[j];
+        if (id < 0 || id >= P.num_blocks) {
+          atomicOr(err, kErrBlockId);
+          id = -1;
+        }
+        const int32_t y = static_cast<int32_t>(id < 0 ? y_oob : (static_cast<int64_t>(id) * P.hkv + h) * kBlock);
+        uint8_t* dst = smem + static_cast<size_t>(j) * Cfg::kStageBytes;
+#pragma unroll
+        for (int hf = 0; hf < Tile<D>::kHalves; ++hf) {
+          tma_load_2d(dst + hf * Tile<D>::kHalfBytes, &tm_k, hf * 64, y, bar);
+          tma_load_2d(dst + Tile<D>::kKVBytes + hf * Tile<D>::kHalfBytes, &tm_v, hf * 64, y, bar);
+        }
+      }
+    }
+    // this warp's 16 query rows: row r -> member r / G, head r % G
+    const int r0 = tile * kPrefixRows + warp * 16 + g, r1 = r0 + 8;
+    const int m0 = r0 / G, m1 = r1 / G;
+    const bool ok0 = m0 < M, ok1 = m1 < M;
+    const T* q0 = static_cast<const T*>(P.q) + ((static_cast<int64_t>(off) + m0) * P.hq + h * G + r0 % G) * D;
+    const T* q1 = static_cast<const T*>(P.q) + ((static_cast<int64_t>(off) + m1) * P.hq + h * G + r1 % G) * D;
+    uint32_t qa[D / 16][4];
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      qa[ks][0] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + 16 * ks + 2 * t) : 0u;
+      qa[ks][1] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + 16 * ks + 2 * t) : 0u;
+      qa[ks][2] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + 16 * ks + 2 * t + 8) : 0u;
+      qa[ks][3] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + 16 * ks + 2 * t + 8) : 0u;
+    }
+    bool ok = mbar_wait(bar, n_local & 1, abort_flag, err);
+    if (!__syncthreads_and(ok)) {
+      if (tid == 0) {  // let this CTA's copies land before it leaves
+        unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(bar, n_local & 1) && global_timer_ns() - t0 < kWaitLimitNs / 4) {
+        }
+      }
+      return;
+    }
+    float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.f, 0.f};
+    float o[D / 8][4];
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    for (int j = 0; j < nblk; ++j) {
+      const uint32_t sK = smem_u32(smem + static_cast<size_t>(j) * Cfg::kStageBytes);
+      const uint32_t sV = sK + Tile<D>::kKVBytes;
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
+        const int cofs = (lane >> 3) & 1;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t b00, b01, b10, b11;
+          ldmatrix_x4(b00, b01, b10, b11, chunk_addr(sK, tok, 2 * ks + cofs));
+          Mma<T>::run(s0, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
+          Mma<T>::run(s1, qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
+        }
+      }
+      // rows g (s*[0], s*[1]) and g + 8 (s*[2], s*[3]); tokens 2t, 2t+1 (+8 for s1)
+      float x[2][4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        x[e][0] = s0[2 * e] * P.scale_log2;
+        x[e][1] = s0[2 * e + 1] * P.scale_log2;
+        x[e][2] = s1[2 * e] * P.scale_log2;
+        x[e][3] = s1[2 * e + 1] * P.scale_log2;
+      }
+      float pr[2][4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float bm = fmaxf(fmaxf(x[e][0], x[e][1]), fmaxf(x[e][2], x[e][3]));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        const float mn = fmaxf(mr[e], bm);
+        const float al = exp2f(mr[e] - mn);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) pr[e][c] = exp2f(x[e][c] - mn);
+        lr[e] = lr[e] * al + (pr[e][0] + pr[e][1] + pr[e][2] + pr[e][3]);
+        mr[e] = mn;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) {
+          o[nd][2 * e] *= al;
+          o[nd][2 * e + 1] *= al;
+        }
+      }
+      const uint32_t pa0 = pack2<T>(pr[0][0], pr[0][1]), pa1 = pack2<T>(pr[1][0], pr[1][1]);
+      const uint32_t pa2 = pack2<T>(pr[0][2], pr[0][3]), pa3 = pack2<T>(pr[1][2], pr[1][3]);
+      {
+        const int tok = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int cofs = lane >> 4;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; nd += 2) {
+          uint32_t b00, b01, b10, b11;
+          ldmatrix_x4_trans(b00, b01, b10, b11, chunk_addr(sV, tok, nd + cofs));
+          Mma<T>::run(o[nd], pa0, pa1, pa2, pa3, b00, b01);
+          Mma<T>::run(o[nd + 1], pa0, pa1, pa2, pa3, b10, b11);
+        }
+      }
+    }
+    // partial results of this chunk for the warp's rows
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float L = lr[e];
+      L += __shfl_xor_sync(0xffffffffu, L, 1);
+      L += __shfl_xor_sync(0xffffffffu, L, 2);
+      const int r = e ? r1 : r0;
+      const int m = r / G;
+      if (m < M) {
+        const int64_t prow = (static_cast<int64_t>(gi.x) + static_cast<int64_t>(chunk) * M + m) * P.hq +
+                             h * G + r % G;
+        float* dst = P.acc + prow * D;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd)
+          *reinterpret_cast<float2*>(dst + 8 * nd + 2 * t) = make_float2(o[nd][2 * e], o[nd][2 * e + 1]);
+        if (t == 0) P.ml[prow] = make_float2(mr[e], L);
+      }
+    }
+    // every warp is done with the stages before the next item's copies
+    __syncthreads();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
 }
 
@@ -913,8 +1200,67 @@ bool dispatch_attend(int variant, int G, const CUtensorMap& tk, const CUtensorMa
 
 }  // namespace
 
+// One side stream and a fork/join event pair per device, created on first
+// use and kept for the process.  Reusing the events is safe: a stream wait
+// uses the record that precedes it.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream(std::string* why) {
+  static SideStream sides[64];
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) {
+    *why = "device ordinal out of range";
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream& ss = sides[dev];
+  if (!ss.stream) {
+    cudaError_t e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      *why = std::string("side stream: ") + cudaGetErrorString(e);
+      ss = SideStream{};
+      return nullptr;
+    }
+  }
+  return &ss;
+}
+
+template <typename T, int D>
+bool launch_prefix(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& P, int n_sm,
+                   cudaStream_t stream, std::string* why) {
+  using Cfg = PrefixCfg<D>;
+  auto kern = prefix_kernel<T, D>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(Cfg::kBytes));
+    if (e != cudaSuccess) {
+      *why = std::string("cudaFuncSetAttribute (prefix): ") + cudaGetErrorString(e);
+      return false;
+    }
+    attr_set[dev & 63] = true;
+  }
+  kern<<<static_cast<unsigned>(2 * n_sm), kPrefixWarps * 32, Cfg::kBytes, stream>>>(tk, tv, P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("prefix launch: ") + cudaGetErrorString(e);
+    return false;
+  }
+  return true;
+}
+
 int decode_launch(const DecodeArgs& a, std::string* why) {
-  const WsLayout L = ws_layout(a.num_seqs, a.num_q_heads, a.head_dim, a.max_seq_len);
+  const bool grouped = a.num_groups > 0;
+  const WsLayout L = ws_layout(a.num_seqs, a.num_q_heads, a.head_dim, a.max_seq_len, grouped);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   DecodeParams P;
   P.q = a.q;
@@ -925,6 +1271,13 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   P.parts = reinterpret_cast<PartInfo*>(ws + L.off_parts);
   P.seq_first = reinterpret_cast<int2*>(ws + L.off_seq_first);
   P.split = reinterpret_cast<int32_t*>(ws + L.off_split);
+  P.seq_prefix = reinterpret_cast<int4*>(ws + L.off_seq_prefix);
+  P.group_info = reinterpret_cast<int4*>(ws + L.off_group);
+  P.group_bad = reinterpret_cast<int32_t*>(ws + L.off_group_bad);
+  P.pitems = reinterpret_cast<int4*>(ws + L.off_pitems);
+  P.group_off = a.group_off;
+  P.group_prefix = a.group_prefix;
+  P.num_groups = grouped ? a.num_groups : 0;
   P.ml = reinterpret_cast<float2*>(ws + L.off_ml);
   P.acc = reinterpret_cast<float*>(ws + L.off_acc);
   P.num_blocks = a.num_blocks;
@@ -943,6 +1296,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
 
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const int row_uint4 = a.num_q_heads * a.head_dim * 2 / 16;
+  cudaEvent_t join_after_attend = nullptr;
   int dev0 = 0, n_sm = 0;
   cudaGetDevice(&dev0);
   cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev0);
@@ -952,6 +1306,23 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   if (e != cudaSuccess) {
     *why = std::string("prep launch: ") + cudaGetErrorString(e);
     return 5;
+  }
+  if (grouped) {
+    // The prefix kernel moves little data and is mostly latency: it runs on a
+    // library-owned side stream forked from and joined back into the
+    // caller's stream with events, so it overlaps the attention kernel.
+    SideStream* side = side_stream(why);
+    if (!side) return 5;
+    cudaEventRecord(side->fork, s);
+    cudaStreamWaitEvent(side->stream, side->fork, 0);
+    bool okp = a.dtype == 1
+                   ? (a.head_dim == 128 ? launch_prefix<__nv_bfloat16, 128>(tk, tv, P, n_sm, side->stream, why)
+                                        : launch_prefix<__nv_bfloat16, 64>(tk, tv, P, n_sm, side->stream, why))
+                   : (a.head_dim == 128 ? launch_prefix<__half, 128>(tk, tv, P, n_sm, side->stream, why)
+                                        : launch_prefix<__half, 64>(tk, tv, P, n_sm, side->stream, why));
+    if (!okp) return 5;
+    cudaEventRecord(side->join, side->stream);
+    join_after_attend = side->join;
   }
   if (a.ev_before) cudaEventRecord(static_cast<cudaEvent_t>(a.ev_before), s);
   const int64_t max_items = L.max_parts * a.num_kv_heads;
@@ -967,6 +1338,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   }
   if (!ok) return 5;
   if (a.ev_after) cudaEventRecord(static_cast<cudaEvent_t>(a.ev_after), s);
+  if (join_after_attend) cudaStreamWaitEvent(s, join_after_attend, 0);
 
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -991,8 +1363,8 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
 }
 
 size_t decode_workspace_bytes(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
-                              int64_t max_seq_len) {
-  return ws_layout(num_seqs, num_q_heads, head_dim, max_seq_len).total;
+                              int64_t max_seq_len, bool grouped) {
+  return ws_layout(num_seqs, num_q_heads, head_dim, max_seq_len, grouped).total;
 }
 
 }  // namespace pa

@@ -19,6 +19,7 @@ constexpr int kMaxPartBlocks = kPartTokens * kMaxPartMult / kBlock;
 constexpr int kErrSeqLen = 1;
 constexpr int kErrBlockId = 2;
 constexpr int kErrTimeout = 4;
+constexpr int kErrGroup = 8;
 
 // A wait that has not completed after this long gives up (ns of globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -33,39 +34,59 @@ struct WsHeader {
   int32_t n_split;      // sequences with more than one partition
   int32_t next_split;   // dynamic work counter of the merge kernel
   int32_t part_tokens;  // tokens per partition chosen for this call
-  int32_t pad[57];
+  int32_t n_pitems;     // shared-prefix work items (grouped decode)
+  int32_t n_suffix_parts;  // partitions of the attention kernel (= n_parts)
+  int32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
-// Per partition: sequence, partition index, clamped length, partitions of the sequence.
+// Per partition: sequence, partition index, clamped length, partial results of
+// the sequence, first token the partitions cover (after a shared prefix).
 struct PartInfo {
-  int32_t b, p, len, nparts;
+  int32_t b, p, len, nparts, start, pad0, pad1, pad2;
 };
 
+// Shared-prefix chunks of grouped decode: 16 blocks (256 tokens) each.
+constexpr int kPrefixChunkBlocks = 16;
+constexpr int kPrefixChunkTokens = kPrefixChunkBlocks * kBlock;
+constexpr int kPrefixRows = 128;  // query rows (members x heads) per prefix work item
+
 struct WsLayout {
-  size_t off_parts;      // PartInfo[max_parts]
-  size_t off_seq_first;  // int2[num_seqs]: first full partition, tail partition (-1: none)
-  size_t off_split;      // int32[num_seqs]: sequences with nparts > 1
-  size_t off_ml;         // float2[max_parts * num_q_heads]: (max, sum) per partition, head
-  size_t off_acc;        // float[max_parts * num_q_heads * head_dim]: unnormalised output
+  size_t off_parts;       // PartInfo[max_parts]
+  size_t off_seq_first;   // int2[num_seqs]: first full partition, tail partition (-1: none)
+  size_t off_split;       // int32[num_seqs]: sequences whose partial results need a merge
+  size_t off_seq_prefix;  // int4[num_seqs]: first prefix partial, group size, chunks, prefix tokens
+  size_t off_group;       // int4[num_seqs]: per group: partial base, item base, chunks, row tiles
+  size_t off_group_bad;   // int32[num_seqs]: per group: shared prefix rejected
+  size_t off_pitems;      // int4[max_pitems]: (group, chunk, row tile)
+  size_t off_ml;          // float2[(max_parts + max_prefix) * num_q_heads]: (max, sum)
+  size_t off_acc;         // float[(max_parts + max_prefix) * num_q_heads * head_dim]
   size_t total;
-  int64_t max_parts;
+  int64_t max_parts;      // attention-kernel partitions
+  int64_t max_prefix;     // shared-prefix partial rows (grouped decode only)
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline WsLayout ws_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
-                          int64_t max_seq_len) {
+                          int64_t max_seq_len, bool grouped = false) {
   WsLayout L;
   int64_t per_seq = (max_seq_len + kPartTokens - 1) / kPartTokens;
   if (per_seq < 1) per_seq = 1;
   L.max_parts = num_seqs * per_seq;
+  L.max_prefix = grouped ? num_seqs * ((max_seq_len + kPrefixChunkTokens - 1) / kPrefixChunkTokens)
+                         : 0;
+  const int64_t rows = L.max_parts + L.max_prefix;
   size_t o = sizeof(WsHeader);
-  L.off_parts = o;      o = align_up(o + sizeof(PartInfo) * L.max_parts, 256);
-  L.off_seq_first = o;  o = align_up(o + sizeof(int2) * num_seqs, 256);
-  L.off_split = o;      o = align_up(o + sizeof(int32_t) * num_seqs, 256);
-  L.off_ml = o;         o = align_up(o + sizeof(float2) * L.max_parts * num_q_heads, 256);
-  L.off_acc = o;        o = align_up(o + sizeof(float) * L.max_parts * num_q_heads * head_dim, 256);
+  L.off_parts = o;       o = align_up(o + sizeof(PartInfo) * L.max_parts, 256);
+  L.off_seq_first = o;   o = align_up(o + sizeof(int2) * num_seqs, 256);
+  L.off_split = o;       o = align_up(o + sizeof(int32_t) * num_seqs, 256);
+  L.off_seq_prefix = o;  o = align_up(o + sizeof(int4) * num_seqs, 256);
+  L.off_group = o;       o = align_up(o + (grouped ? sizeof(int4) * num_seqs : 0), 256);
+  L.off_group_bad = o;   o = align_up(o + (grouped ? sizeof(int32_t) * num_seqs : 0), 256);
+  L.off_pitems = o;      o = align_up(o + sizeof(int4) * L.max_prefix, 256);
+  L.off_ml = o;          o = align_up(o + sizeof(float2) * rows * num_q_heads, 256);
+  L.off_acc = o;         o = align_up(o + sizeof(float) * rows * num_q_heads * head_dim, 256);
   L.total = o;
   return L;
 }

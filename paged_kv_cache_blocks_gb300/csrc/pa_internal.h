@@ -32,12 +32,15 @@ struct DecodeArgs {
   int32_t variant;
   void* ev_before;
   void* ev_after;
+  const int32_t* group_off = nullptr;     // grouped decode: [num_groups + 1] (device)
+  const int32_t* group_prefix = nullptr;  // [num_groups] shared prefix tokens (device)
+  int32_t num_groups = 0;
 };
 
 // Both return 0 on success or a pa_status code, with *why set on failure.
 int decode_launch(const DecodeArgs& a, std::string* why);
 size_t decode_workspace_bytes(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
-                              int64_t max_seq_len);
+                              int64_t max_seq_len, bool grouped = false);
 
 int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
                        int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,

@@ -142,6 +142,8 @@ class Batch:
     # of (row_start, row_count) ranges of the past draw that form it, in order
     past_ranges: list = None
     seed: int = 0
+    groups: list = None          # (members, shared prefix tokens), contiguous
+    has_new: np.ndarray = None   # sequence has a token of its own to write
 
     # numpy views (host tensors only)
     def np_layer(self, i):
@@ -152,8 +154,9 @@ class Batch:
     def contiguous_kv(self, layer, b):
         """Contiguous [L_b, Hkv, D] uint16 K and V of sequence b (keep_contig)."""
         Lr = self.layers[layer]
-        ks = [Lr.k_past[s:s + n] for s, n in self.past_ranges[b]] + [Lr.new_k[b:b + 1]]
-        vs = [Lr.v_past[s:s + n] for s, n in self.past_ranges[b]] + [Lr.new_v[b:b + 1]]
+        tail = bool(self.has_new[b])
+        ks = [Lr.k_past[s:s + n] for s, n in self.past_ranges[b]] + ([Lr.new_k[b:b + 1]] if tail else [])
+        vs = [Lr.v_past[s:s + n] for s, n in self.past_ranges[b]] + ([Lr.new_v[b:b + 1]] if tail else [])
         f = lambda t: torch.cat(t).numpy().view(np.uint16)
         return f(ks), f(vs)
 
@@ -163,21 +166,28 @@ class Batch:
         return int(self.seq_lens.astype(np.int64).sum()) * w.num_kv_heads * w.head_dim * 2 * 2
 
     def unique_kv_bytes(self):
-        """KV bytes counting a shared physical block once (tails as stored)."""
+        """KV bytes counting the tokens of a shared prefix once per group."""
         w = self.workload
-        per_block_row = w.num_kv_heads * w.head_dim * 2 * 2
-        nb = (self.seq_lens.astype(np.int64) + BLOCK_SIZE - 1) // BLOCK_SIZE
-        if w.name != "fullstep":
-            return int(self.seq_lens.astype(np.int64).sum()) * per_block_row
-        shared_tokens = (PREFIX_GROUPS * (self.workload.num_seqs // PREFIX_GROUPS - 1)) * PREFIX_TOKENS
-        del nb
-        return (int(self.seq_lens.astype(np.int64).sum()) - shared_tokens) * per_block_row
+        per_token = w.num_kv_heads * w.head_dim * 2 * 2
+        repeated = sum((m - 1) * p for m, p in self.groups if m > 1)
+        return (int(self.seq_lens.astype(np.int64).sum()) - repeated) * per_token
+
+    def group_arrays(self):
+        """(offsets [G+1], prefix tokens [G]) int32 for grouped decode."""
+        sizes = [m for m, _ in self.groups]
+        off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+        return off, np.array([p for _, p in self.groups], np.int32)
 
 
 def make_batch(name, seed=0, poison=True, num_layers=None, keep_contig=False, device="cpu",
-               lens_override=None):
+               lens_override=None, groups=None):
     """Build one decode batch.  ``device='cuda'`` draws values on the GPU
-    (timing runs; not comparable bit-for-bit with a CPU draw)."""
+    (timing runs; not comparable bit-for-bit with a CPU draw).
+
+    ``groups``: list of (members, prefix_tokens) covering the sequences in
+    order; members of a group share the physical blocks of their first
+    prefix_tokens tokens (a multiple of 16, at most every member's length).
+    The fullstep workload uses 4 groups sharing 1024 tokens."""
     w = WORKLOADS[name]
     layers_n = w.num_layers if num_layers is None else num_layers
     gseed = int(seed) * 1000 + _SEED_SALT[name]
@@ -188,20 +198,32 @@ def make_batch(name, seed=0, poison=True, num_layers=None, keep_contig=False, de
     if B != w.num_seqs and lens_override is None:
         raise AssertionError
     nblk = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
+    lens_np = lens.numpy().astype(np.int32)
 
-    # --- logical block -> unique block index ---------------------------------
-    grouped = name == "fullstep" and lens_override is None
-    n_groups = PREFIX_GROUPS if grouped else 0
-    pre_blocks = PREFIX_TOKENS // BLOCK_SIZE if grouped else 0
-    group_of = (np.arange(B) * n_groups // B) if grouped else None
+    # --- groups sharing a prefix (contiguous) ---------------------------------------
+    if groups is None and name == "fullstep" and lens_override is None:
+        groups = [(B // PREFIX_GROUPS, PREFIX_TOKENS)] * PREFIX_GROUPS
+    if groups is None:
+        groups = [(1, 0)] * B
+    if sum(m for m, _ in groups) != B:
+        raise ValueError("groups must cover every sequence")
+    group_of = np.repeat(np.arange(len(groups)), [m for m, _ in groups])
+    prefix_of = np.array([groups[gi][1] for gi in group_of], np.int64)
+    for b in range(B):
+        if prefix_of[b] % BLOCK_SIZE or prefix_of[b] > lens_np[b]:
+            raise ValueError("a shared prefix must be whole blocks within every member")
+    shared = [m > 1 and p > 0 for m, p in groups]
+
+    # --- logical block -> unique block index ---------------------------------------
     uniq = []  # per sequence: list of unique block indices
     n_unique = 0
     group_prefix_idx = {}
     for b in range(B):
         row = []
+        gi = int(group_of[b])
         for j in range(int(nblk[b])):
-            if grouped and j < pre_blocks:
-                key = (int(group_of[b]), j)
+            if shared[gi] and j < prefix_of[b] // BLOCK_SIZE:
+                key = (gi, j)
                 if key not in group_prefix_idx:
                     group_prefix_idx[key] = n_unique
                     n_unique += 1
@@ -221,14 +243,17 @@ def make_batch(name, seed=0, poison=True, num_layers=None, keep_contig=False, de
     for b in range(B):
         if uniq[b]:
             tables[b, :len(uniq[b])] = perm[np.asarray(uniq[b], np.int64)]
-    lens_np = lens.numpy().astype(np.int32)
+    # A member whose whole length lies in the shared prefix has no token of
+    # its own to write: its last token is part of the shared draw.
     pos = lens_np.astype(np.int64) - 1
-    slot = np.where(pos >= 0, tables[np.arange(B), np.maximum(pos, 0) // BLOCK_SIZE].astype(np.int64)
+    has_new = (pos >= 0) & ~np.array([shared[int(group_of[b])] and lens_np[b] <= prefix_of[b]
+                                      for b in range(B)], bool)
+    slot = np.where(has_new, tables[np.arange(B), np.maximum(pos, 0) // BLOCK_SIZE].astype(np.int64)
                     * BLOCK_SIZE + np.maximum(pos, 0) % BLOCK_SIZE, -1).astype(np.int64)
 
-    # --- placement of the past tokens (layout only) ------------------------------
-    # Draw rows: ungrouped -> each sequence's L-1 past tokens in sequence order;
-    # grouped -> per group: the shared prefix once, then each member's private part.
+    # --- placement of the tokens already cached (layout only) ------------------------
+    # Draw rows, per group in order: the shared prefix once, then each member's
+    # own tokens before its new one; a lone sequence is a group of one.
     ranges = [None] * B
     dst_blk, dst_off = [], []
     row = 0
@@ -242,17 +267,18 @@ def make_batch(name, seed=0, poison=True, num_layers=None, keep_contig=False, de
         row += t1 - t0
         return (start, t1 - t0)
 
-    if grouped:
-        for gi in range(n_groups):
-            members = [b for b in range(B) if group_of[b] == gi]
-            pr = place(members[0], 0, PREFIX_TOKENS)
+    first = 0
+    for gi, (M, pre) in enumerate(groups):
+        members = range(first, first + M)
+        first += M
+        if shared[gi]:
+            pr = place(members[0], 0, pre)
             for b in members:
-                ranges[b] = [pr]
+                end_b = int(lens_np[b]) - 1 if has_new[b] else int(lens_np[b])
+                ranges[b] = [pr] + ([place(b, pre, end_b)] if end_b > pre else [])
+        else:
             for b in members:
-                ranges[b] = ranges[b] + [place(b, PREFIX_TOKENS, int(lens_np[b]) - 1)]
-    else:
-        for b in range(B):
-            ranges[b] = [place(b, 0, max(int(lens_np[b]) - 1, 0))]
+                ranges[b] = [place(b, 0, max(int(lens_np[b]) - 1, 0))]
     dst_blk = np.concatenate(dst_blk) if dst_blk else np.zeros(0, np.int64)
     dst_off = np.concatenate(dst_off) if dst_off else np.zeros(0, np.int64)
     n_rows = row
@@ -285,8 +311,11 @@ def make_batch(name, seed=0, poison=True, num_layers=None, keep_contig=False, de
         else:
             del k_past, v_past
         layers.append(Lr)
-    return Batch(w, lens_np, tables, pool, poison_block, slot, layers, n_unique,
-                 ranges if keep_contig else None, seed)
+    bt = Batch(w, lens_np, tables, pool, poison_block, slot, layers, n_unique,
+               ranges if keep_contig else None, seed)
+    bt.groups = list(groups)
+    bt.has_new = has_new
+    return bt
 
 
 def place_new_tokens(batch, layer):
@@ -309,7 +338,8 @@ def relabel_blocks(batch, seed):
     sigma = torch.randperm(batch.num_blocks, generator=g).numpy().astype(np.int32)
     new = Batch(batch.workload, batch.seq_lens.copy(), sigma[batch.block_tables],
                 batch.num_blocks, int(sigma[batch.poison_block]), None, [],
-                batch.num_unique_blocks, batch.past_ranges, batch.seed)
+                batch.num_unique_blocks, batch.past_ranges, batch.seed, batch.groups,
+                batch.has_new)
     s = batch.slot_mapping
     new.slot_mapping = np.where(s >= 0, sigma[np.maximum(s, 0) // BLOCK_SIZE].astype(np.int64)
                                 * BLOCK_SIZE + np.maximum(s, 0) % BLOCK_SIZE, -1)

@@ -61,6 +61,9 @@ def small_batches():
         W.make_batch("tiny", seed=0, keep_contig=True),
         W.make_batch("llama8b", seed=1, keep_contig=True, lens_override=[5, 16, 31, 200, 1]),
         W.make_batch("llama70b", seed=2, keep_contig=True, lens_override=[48, 3, 130]),
+        # three sequences sharing a 32-token prefix (one of them holds only the prefix)
+        W.make_batch("llama8b", seed=3, keep_contig=True, lens_override=[40, 33, 32, 100, 5],
+                     groups=[(3, 32), (1, 16), (1, 0)]),
     ]
 
 

@@ -74,6 +74,15 @@ def test_relabelled_blocks_give_identical_output(pa, name):
     assert np.array_equal(a, run(pa, r))
 
 
+@pytest.mark.parametrize("name", ["long", "llama70b"])
+def test_repeated_calls_are_bit_identical(pa, name):
+    """Work is handed out dynamically; the result must not depend on it."""
+    b = U.batch(name)
+    a = run(pa, b)
+    for _ in range(2):
+        assert np.array_equal(a, run(pa, b))
+
+
 EDGE_LENS = [1, 2, 15, 16, 17, 31, 32, 33, 511, 512, 513, 1023, 1024, 1025, 1537, 2048, 3]
 
 

@@ -2,17 +2,20 @@
 
 The kernel's producer warp streams blocks into S stages; consumer warps wait
 on a per-stage "full" mbarrier with a parity bit and release the stage on an
-"empty" mbarrier.  A parity wait only asks "has the phase of this parity
+"empty" mbarrier; at the end of every work item the consumers meet at a
+merge barrier.  A parity wait only asks "has the phase of this parity
 completed", so if two consecutive uses of one stage could be consumed by
-different warps, a warp waiting for round r+1 could pass on round r-1's
-completed phase and read the stage before its copy lands.  The kernel rules
-that out by giving block g of a CTA's stream to consumer g % NC with
-S % NC == 0.  This test runs a randomised discrete-event model of the
-protocol with exact mbarrier parity semantics (try_wait.parity(P) is true
-iff the barrier's current phase parity differs from P) and checks that no
-consumer ever reads a stage holding a block other than the one it waits for.
-The item-relative assignment the kernel used before is shown to fail with
-S = 6, NC = 4 (it reads stale stages or deadlocks)."""
+different warps without a barrier between them, a warp waiting for round
+r+1 could pass on round r-1's completed phase and read the stage before its
+copy lands.  The kernel gives block j of an item to consumer j % NC and
+requires S % NC == 0.  This test runs a randomised discrete-event model of
+the protocol with exact mbarrier parity semantics (try_wait.parity(P) is
+true iff the barrier's current phase parity differs from P) and checks that
+no consumer ever reads a stage holding another block: safe for every S that
+is a multiple of NC, unsafe (stale reads or deadlock) for S = 6 or 10 with
+NC = 4.  The alternative rule (block g of the CTA's whole stream to consumer
+g % NC) is safe too, but makes the per-warp grouping of sums depend on
+scheduling, so outputs would not be bit-reproducible."""
 import random
 
 import pytest
@@ -124,14 +127,16 @@ def random_items(rng, n):
     return [rng.randint(1, 40) for _ in range(n)]
 
 
+@pytest.mark.parametrize("rule", ["item", "global"])
 @pytest.mark.parametrize("S,NC", [(4, 4), (8, 4), (12, 4), (8, 2), (8, 8)])
-def test_global_assignment_never_reads_a_stale_stage(S, NC):
+def test_stage_multiple_of_consumers_never_reads_a_stale_stage(S, NC, rule):
     rng = random.Random(S * 100 + NC)
     for seed in range(40):
-        assert simulate(S, NC, "global", random_items(rng, 12), seed) == 0
+        assert simulate(S, NC, rule, random_items(rng, 12), seed) == 0
 
 
-def test_item_relative_assignment_with_six_stages_is_unsafe():
+@pytest.mark.parametrize("S", [6, 10])
+def test_stages_not_a_multiple_of_consumers_are_unsafe(S):
     rng = random.Random(7)
-    results = [simulate(6, 4, "item", random_items(rng, 12), seed) for seed in range(10)]
+    results = [simulate(S, 4, "item", random_items(rng, 12), seed) for seed in range(10)]
     assert any(r != 0 for r in results)     # stale reads or deadlock
