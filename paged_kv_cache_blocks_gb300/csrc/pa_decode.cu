@@ -55,7 +55,7 @@ struct DecodeParams {
   WsHeader* ws;
   PartInfo* parts;
   int2* seq_first;
-  int32_t* split;
+  MergeInfo* split;
   int4* seq_prefix;   // per sequence: first prefix partial, group size, chunks, prefix tokens
   int4* group_info;   // per group: prefix partial base, item base, chunks, row tiles
   int32_t* group_bad; // per group: shared prefix rejected
@@ -135,9 +135,12 @@ __device__ __forceinline__ int group_of(const DecodeParams& P, int b) {
 // 256-token chunks handled once per (group, KV head) by the prefix kernel for
 // all members together.  A group whose prefix is not a multiple of 16 or
 // longer than one of its members is flagged and decoded without sharing.
+constexpr int kPrepCache = 4096;  // sequences whose (length, start) prep keeps in shared memory
+
 __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint4,
                                                     int target_full_items) {
   __shared__ int sw[32];
+  __shared__ int2 s_ls[kPrepCache];  // (clamped length, first token of the partitions)
   __shared__ int s_full[3];
   __shared__ int s_hist[kMaxPartBlocks + 1];
   __shared__ int s_nsplit, s_total_tail, s_groups_ok;
@@ -182,11 +185,20 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
     }
   }
   __syncthreads();
-  auto suffix_start = [&](int b) -> int { return use_groups ? P.seq_prefix[b].w : 0; };
+  const bool cached = P.num_seqs <= kPrepCache;
+  if (cached) {
+    for (int b = tid; b < P.num_seqs; b += blockDim.x)
+      s_ls[b] = make_int2(clamp_len(P, b), use_groups ? P.seq_prefix[b].w : 0);
+    __syncthreads();
+  }
+  auto seq_len = [&](int b) -> int { return cached ? s_ls[b].x : clamp_len(P, b); };
+  auto suffix_start = [&](int b) -> int {
+    return cached ? s_ls[b].y : (use_groups ? P.seq_prefix[b].w : 0);
+  };
   // pass A: full partitions for each candidate size
   int f1 = 0, f2 = 0, f4 = 0;
   for (int b = tid; b < P.num_seqs; b += blockDim.x) {
-    const int n = clamp_len(P, b) - suffix_start(b);
+    const int n = seq_len(b) - suffix_start(b);
     f1 += n / kPartTokens;
     f2 += n / (2 * kPartTokens);
     f4 += n / (4 * kPartTokens);
@@ -205,18 +217,18 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
   }
   // tails by size (blocks), then start offsets in descending size order
   for (int b = tid; b < P.num_seqs; b += blockDim.x) {
-    const int r = (clamp_len(P, b) - suffix_start(b)) % pt;
+    const int r = (seq_len(b) - suffix_start(b)) % pt;
     if (r) atomicAdd(&s_hist[(r + kBlock - 1) / kBlock], 1);
   }
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int sz = pt / kBlock; sz >= 1; --sz) {
-      const int c = s_hist[sz];
-      s_hist[sz] = run;
-      run += c;
-    }
-    s_total_tail = run;
+  {  // start offsets in descending size order: a scan over the reversed bins
+    const int nbins = pt / kBlock;  // <= 128 <= blockDim.x
+    const int sz = nbins - tid;
+    const int c = (tid < nbins) ? s_hist[sz] : 0;
+    int total;
+    const int off = block_exclusive_scan(c, sw, &total);
+    if (tid < nbins) s_hist[sz] = off;
+    if (tid == 0) s_total_tail = total;
   }
   __syncthreads();
   const int n_suffix = total_full + s_total_tail;
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
     const int b = base + tid;
     int L = 0, st = 0;
     if (b < P.num_seqs) {
-      L = clamp_len(P, b);
+      L = seq_len(b);
       st = suffix_start(b);
     }
     const int nfull = (L - st) / pt;
@@ -277,7 +289,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
       P.seq_first[b] = make_int2(first, tail_idx);
       for (int p = 0; p < nfull; ++p) P.parts[first + p] = PartInfo{b, p, L, nparts, st, 0, 0, 0};
       if (r) P.parts[tail_idx] = PartInfo{b, nfull, L, nparts, st, 0, 0, 0};
-      if (nparts > 1 || sp.z > 0) P.split[atomicAdd(&s_nsplit, 1)] = b;
+      if (nparts > 1 || sp.z > 0)
+        P.split[atomicAdd(&s_nsplit, 1)] =
+            MergeInfo{b, first, tail_idx, nfull, nfull + (r != 0), sp.x, sp.y, sp.z};
       if (L == 0) {  // empty softmax: the output is defined as 0
         uint4* o = reinterpret_cast<uint4*>(P.out) + static_cast<int64_t>(b) * row_uint4;
         for (int i = 0; i < row_uint4; ++i) o[i] = make_uint4(0, 0, 0, 0);
@@ -800,59 +814,49 @@ __global__ void __launch_bounds__(32 * (NC + 1))
 // ---------------------------------------------------------------------------
 // 3. merge of split sequences
 //
-// One CTA per (split sequence, KV head), grid-stride.  The CTA's threads are
-// kMergeSlices slices of 128; slice s merges partitions s, s + kMergeSlices,
-// ... with a running maximum (the same online rule as inside a partition),
-// each thread owning up to kE float4 columns of the G x D block, so a
-// partition is one fully coalesced read of G*D*4 bytes per slice.  The
-// slices' (max, sum, output) are then combined in shared memory.
+// One 128-thread CTA per (sequence with several partial results, KV head),
+// up to 16 resident per SM so a whole batch's merges run in one wave.  The
+// prep kernel leaves everything a merge needs in one MergeInfo record.  Each
+// thread owns up to kE float4 columns of the G x D block (a partial is one
+// fully coalesced G*D*4-byte read), keeps U partials in flight and folds them
+// in with a running maximum, the same online rule as inside a partition.
 
-constexpr int kMergeSlices = 4;
-constexpr int kMergeThreads = 128 * kMergeSlices;
-
-template <typename T, int D>
-__global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodeParams P) {
-  constexpr int kE = (8 * D / 4 + 127) / 128;  // float4 columns per thread (G <= 8)
-  __shared__ float4 so[kMergeSlices][8 * D / 4];
-  __shared__ float sm[kMergeSlices][8], sl[kMergeSlices][8];
+template <typename T, int D, int kMergeThreads>
+__global__ void __launch_bounds__(kMergeThreads, 1024 / kMergeThreads) merge_kernel(const DecodeParams P) {
+  // one float4 column of the G x D block per thread; U partials in flight
+  constexpr int kE = 1;
+  constexpr int U = 8;
   const int n_work = *reinterpret_cast<volatile int32_t*>(&P.ws->n_split) * P.hkv;
-  const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
   const int G = P.G;
   const int n4 = G * D / 4;
-  const int tid = threadIdx.x, slice = tid >> 7, t = tid & 127;
+  const int t = threadIdx.x;
   const float4* acc4 = reinterpret_cast<const float4*>(P.acc);
   for (int wi = blockIdx.x; wi < n_work; wi += gridDim.x) {
-    const int b = P.split[wi / P.hkv];
+    const MergeInfo mi = P.split[wi / P.hkv];
     const int h = wi - (wi / P.hkv) * P.hkv;
     const int64_t head0 = static_cast<int64_t>(h) * G;
-    const int2 sf = P.seq_first[b];
-    const int4 sp = P.seq_prefix[b];  // shared-prefix partials: first, stride (group size), count
-    int L = P.seq_lens[b];
-    L = L < 0 ? 0 : (L > P.max_seq_len ? P.max_seq_len : L);
-    const int nfull = (L - sp.w) / pt;
-    const int nsuf = nfull + (((L - sp.w) % pt) != 0);
-    const int nparts = nsuf + sp.z;
+    const int nparts = mi.nsuf + mi.nchunks;
     int e4[kE], gk[kE];
     float m[kE], l[kE];
     float4 o[kE];
 #pragma unroll
     for (int k = 0; k < kE; ++k) {
-      e4[k] = t + 128 * k;
+      e4[k] = t + kMergeThreads * k;
       gk[k] = min(4 * e4[k] / D, 7);
       m[k] = -INFINITY;
       l[k] = 0.f;
       o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    constexpr int U = 4;
-    for (int p0 = slice; p0 < nparts; p0 += U * kMergeSlices) {
+    for (int p0 = 0; p0 < nparts; p0 += U) {
       float4 a[U][kE];
       float2 ml[U][kE];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int p = p0 + u * kMergeSlices;
+        const int p = p0 + u;
         if (p < nparts) {
-          const int64_t idx = p < nsuf ? (p < nfull ? sf.x + p : sf.y)
-                                       : static_cast<int64_t>(sp.x) + static_cast<int64_t>(p - nsuf) * sp.y;
+          const int64_t idx =
+              p < mi.nsuf ? (p < mi.nfull ? mi.first_full + p : mi.tail)
+                          : static_cast<int64_t>(mi.pfirst) + static_cast<int64_t>(p - mi.nsuf) * mi.pstride;
 #pragma unroll
           for (int k = 0; k < kE; ++k)
             if (e4[k] < n4) {
@@ -863,7 +867,7 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodePar
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (p0 + u * kMergeSlices < nparts) {
+        if (p0 + u < nparts) {
 #pragma unroll
           for (int k = 0; k < kE; ++k)
             if (e4[k] < n4) {
@@ -882,42 +886,13 @@ __global__ void __launch_bounds__(kMergeThreads, 2) merge_kernel(const DecodePar
 #pragma unroll
     for (int k = 0; k < kE; ++k)
       if (e4[k] < n4) {
-        so[slice][e4[k]] = o[k];
-        if ((4 * e4[k]) % D == 0) {  // one thread per head publishes (max, sum)
-          sm[slice][gk[k]] = m[k];
-          sl[slice][gk[k]] = l[k];
-        }
+        const float inv = 1.f / l[k];
+        T* dst = static_cast<T*>(P.out) + (static_cast<int64_t>(mi.b) * P.hq + head0) * D + 4 * e4[k];
+        uint2 pk;
+        pk.x = pack2<T>(o[k].x * inv, o[k].y * inv);
+        pk.y = pack2<T>(o[k].z * inv, o[k].w * inv);
+        *reinterpret_cast<uint2*>(dst) = pk;
       }
-    __syncthreads();
-    if (slice == 0) {
-#pragma unroll
-      for (int k = 0; k < kE; ++k)
-        if (e4[k] < n4) {
-          const int g = gk[k];
-          float M = -INFINITY;
-#pragma unroll
-          for (int s2 = 0; s2 < kMergeSlices; ++s2) M = fmaxf(M, sm[s2][g]);
-          float Ls = 0.f;
-          float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int s2 = 0; s2 < kMergeSlices; ++s2) {
-            const float wg = exp2f(sm[s2][g] - M);  // 0 for a slice without partitions
-            const float4 x = so[s2][e4[k]];
-            Ls = fmaf(sl[s2][g], wg, Ls);
-            O.x = fmaf(x.x, wg, O.x);
-            O.y = fmaf(x.y, wg, O.y);
-            O.z = fmaf(x.z, wg, O.z);
-            O.w = fmaf(x.w, wg, O.w);
-          }
-          const float inv = 1.f / Ls;
-          T* dst = static_cast<T*>(P.out) + (static_cast<int64_t>(b) * P.hq + head0) * D + 4 * e4[k];
-          uint2 pk;
-          pk.x = pack2<T>(O.x * inv, O.y * inv);
-          pk.y = pack2<T>(O.z * inv, O.w * inv);
-          *reinterpret_cast<uint2*>(dst) = pk;
-        }
-    }
-    __syncthreads();
   }
 }
 
@@ -1270,7 +1245,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   P.ws = reinterpret_cast<WsHeader*>(ws);
   P.parts = reinterpret_cast<PartInfo*>(ws + L.off_parts);
   P.seq_first = reinterpret_cast<int2*>(ws + L.off_seq_first);
-  P.split = reinterpret_cast<int32_t*>(ws + L.off_split);
+  P.split = reinterpret_cast<MergeInfo*>(ws + L.off_split);
   P.seq_prefix = reinterpret_cast<int4*>(ws + L.off_seq_prefix);
   P.group_info = reinterpret_cast<int4*>(ws + L.off_group);
   P.group_bad = reinterpret_cast<int32_t*>(ws + L.off_group_bad);
@@ -1343,16 +1318,28 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // one thread per float4 column of the G x D block: 256 threads for G = 8 at
+  // head_dim 128, else 128; a whole batch's merges fit in one wave
+  const bool wide = P.G * a.head_dim / 4 > 128;
+  const int mthreads = wide ? 256 : 128;
   int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  if (mgrid > 2 * sms) mgrid = 2 * sms;  // one wave at two CTAs per SM
+  if (mgrid > sms * (1024 / mthreads)) mgrid = sms * (1024 / mthreads);
   if (mgrid < 1) mgrid = 1;
   const unsigned mg = static_cast<unsigned>(mgrid);
   if (a.dtype == 1) {
-    if (a.head_dim == 128) merge_kernel<__nv_bfloat16, 128><<<mg, kMergeThreads, 0, s>>>(P);
-    else merge_kernel<__nv_bfloat16, 64><<<mg, kMergeThreads, 0, s>>>(P);
+    if (a.head_dim == 128) {
+      if (wide) merge_kernel<__nv_bfloat16, 128, 256><<<mg, 256, 0, s>>>(P);
+      else merge_kernel<__nv_bfloat16, 128, 128><<<mg, 128, 0, s>>>(P);
+    } else {
+      merge_kernel<__nv_bfloat16, 64, 128><<<mg, 128, 0, s>>>(P);
+    }
   } else {
-    if (a.head_dim == 128) merge_kernel<__half, 128><<<mg, kMergeThreads, 0, s>>>(P);
-    else merge_kernel<__half, 64><<<mg, kMergeThreads, 0, s>>>(P);
+    if (a.head_dim == 128) {
+      if (wide) merge_kernel<__half, 128, 256><<<mg, 256, 0, s>>>(P);
+      else merge_kernel<__half, 128, 128><<<mg, 128, 0, s>>>(P);
+    } else {
+      merge_kernel<__half, 64, 128><<<mg, 128, 0, s>>>(P);
+    }
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) {

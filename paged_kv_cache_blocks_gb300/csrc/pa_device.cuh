@@ -46,6 +46,13 @@ struct PartInfo {
   int32_t b, p, len, nparts, start, pad0, pad1, pad2;
 };
 
+// Everything the merge needs about one sequence with several partial results:
+// its partitions are first_full .. first_full+nfull-1, then tail (if nsuf >
+// nfull), then the shared-prefix chunks pfirst + c * pstride, c < nchunks.
+struct MergeInfo {
+  int32_t b, first_full, tail, nfull, nsuf, pfirst, pstride, nchunks;
+};
+
 // Shared-prefix chunks of grouped decode: 16 blocks (256 tokens) each.
 constexpr int kPrefixChunkBlocks = 16;
 constexpr int kPrefixChunkTokens = kPrefixChunkBlocks * kBlock;
@@ -54,7 +61,7 @@ constexpr int kPrefixRows = 128;  // query rows (members x heads) per prefix wor
 struct WsLayout {
   size_t off_parts;       // PartInfo[max_parts]
   size_t off_seq_first;   // int2[num_seqs]: first full partition, tail partition (-1: none)
-  size_t off_split;       // int32[num_seqs]: sequences whose partial results need a merge
+  size_t off_split;       // MergeInfo[num_seqs]: sequences whose partial results need a merge
   size_t off_seq_prefix;  // int4[num_seqs]: first prefix partial, group size, chunks, prefix tokens
   size_t off_group;       // int4[num_seqs]: per group: partial base, item base, chunks, row tiles
   size_t off_group_bad;   // int32[num_seqs]: per group: shared prefix rejected
@@ -80,7 +87,7 @@ inline WsLayout ws_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_di
   size_t o = sizeof(WsHeader);
   L.off_parts = o;       o = align_up(o + sizeof(PartInfo) * L.max_parts, 256);
   L.off_seq_first = o;   o = align_up(o + sizeof(int2) * num_seqs, 256);
-  L.off_split = o;       o = align_up(o + sizeof(int32_t) * num_seqs, 256);
+  L.off_split = o;       o = align_up(o + sizeof(MergeInfo) * num_seqs, 256);
   L.off_seq_prefix = o;  o = align_up(o + sizeof(int4) * num_seqs, 256);
   L.off_group = o;       o = align_up(o + (grouped ? sizeof(int4) * num_seqs : 0), 256);
   L.off_group_bad = o;   o = align_up(o + (grouped ? sizeof(int32_t) * num_seqs : 0), 256);
