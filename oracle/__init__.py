@@ -71,6 +71,16 @@ class OracleLib:
         lib.oracle_decode.argtypes = [P, P, P, ctypes.c_int, P, i32, P, i32, i32, i32, i32, i32,
                                       ctypes.c_double, P, ctypes.c_int]
         lib.oracle_decode.restype = ctypes.c_int
+        lib.oracle_e4m3_to_double.argtypes = [P, i64, P]
+        lib.oracle_e4m3_to_double.restype = None
+        lib.oracle_float_to_e4m3.argtypes = [P, i64, P]
+        lib.oracle_float_to_e4m3.restype = None
+        lib.oracle_cache_write_fp8.argtypes = [P, P, ctypes.c_int, P, i64, i32, i32, i32, P, P, P, P,
+                                               i64]
+        lib.oracle_cache_write_fp8.restype = i64
+        lib.oracle_decode_fp8.argtypes = [P, P, P, P, P, ctypes.c_int, P, i32, P, i32, i32, i32, i32,
+                                          i32, ctypes.c_double, P, ctypes.c_int]
+        lib.oracle_decode_fp8.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         self.lib = lib
@@ -117,6 +127,58 @@ def bits_to_double(bits, dtype, handle=None):
     bits = _c(np.asarray(bits), np.uint16)
     out = np.empty(bits.shape, np.float64)
     _load(handle).oracle_bits_to_double(_ptr(bits), bits.size, DTYPE_CODES[dtype], _ptr(out))
+    return out
+
+
+def e4m3_to_double(codes, handle=None):
+    """fp64 value of each E4M3 byte (NaN for the NaN codes)."""
+    codes = _c(np.asarray(codes), np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    _load(handle).oracle_e4m3_to_double(_ptr(codes), codes.size, _ptr(out))
+    return out
+
+
+def float_to_e4m3(x, handle=None):
+    """E4M3 code of each float32 (round to nearest even, saturate to +-448)."""
+    x = _c(np.asarray(x, np.float32), np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load(handle).oracle_float_to_e4m3(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def cache_write_fp8(k, v, dtype, slot_mapping, k_scale, v_scale, k_cache8, v_cache8, block_size=16,
+                    handle=None):
+    """Quantising scatter into copies of the FP8 caches (K [NB,H,16,D], V [NB,H,D,16])."""
+    k, v = _c(k, np.uint16), _c(v, np.uint16)
+    slot_mapping = _c(slot_mapping, np.int64)
+    ks, vs = _c(np.asarray(k_scale, np.float32), np.float32), _c(np.asarray(v_scale, np.float32), np.float32)
+    kc, vc = np.array(k_cache8, np.uint8, copy=True), np.array(v_cache8, np.uint8, copy=True)
+    T, Hkv, D = k.shape
+    nb = kc.shape[0]
+    assert kc.shape == (nb, Hkv, block_size, D) and vc.shape == (nb, Hkv, D, block_size)
+    bad = _load(handle).oracle_cache_write_fp8(_ptr(k), _ptr(v), DTYPE_CODES[dtype], _ptr(slot_mapping),
+                                               T, Hkv, D, block_size, _ptr(ks), _ptr(vs), _ptr(kc),
+                                               _ptr(vc), nb)
+    return kc, vc, int(bad)
+
+
+def decode_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_lens, scale, dtype,
+               block_size=16, threads=0, handle=None):
+    """fp64 attention over dequantised FP8 K/V (see decode)."""
+    q = _c(q, np.uint16)
+    k8, v8 = _c(k_cache8, np.uint8), _c(v_cache8, np.uint8)
+    ks, vs = _c(np.asarray(k_scale, np.float32), np.float32), _c(np.asarray(v_scale, np.float32), np.float32)
+    block_tables, seq_lens = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    B, Hq, D = q.shape
+    nb, Hkv, bs, D2 = k8.shape
+    assert D2 == D and bs == block_size and v8.shape == (nb, Hkv, D, block_size)
+    out = np.empty((B, Hq, D), np.float64)
+    rc = _load(handle).oracle_decode_fp8(_ptr(q), _ptr(k8), _ptr(v8), _ptr(ks), _ptr(vs),
+                                         DTYPE_CODES[dtype], _ptr(block_tables), block_tables.shape[1],
+                                         _ptr(seq_lens), B, Hq, Hkv, D, block_size, float(scale),
+                                         _ptr(out), int(threads))
+    if rc != 0:
+        raise MemoryError("oracle_decode_fp8 could not allocate its gather buffers")
     return out
 
 

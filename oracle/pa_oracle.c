@@ -43,7 +43,7 @@
  * No online softmax, no partitions, no blocking.
  *
  * Element types are passed as raw 16-bit patterns: dtype 0 = IEEE binary16,
- * dtype 1 = bfloat16.
+ * dtype 1 = bfloat16; FP8 caches as E4M3 bytes with per-KV-head scales.
  */
 #include <math.h>
 #include <stdint.h>
@@ -96,6 +96,69 @@ void oracle_bits_to_double(const uint16_t* bits, int64_t n, int dtype, double* o
     for (int64_t i = 0; i < n; ++i) out[i] = to_double(bits[i], dtype);
 }
 
+/* ---- FP8 (E4M3) KV cache ----
+ *
+ * An FP8 cache halves the bytes per token at some accuracy risk ("Yerel LLM
+ * sistemlerinde backpressure ve olcekleme", section "1. KV cache tuketimi
+ * ve GPU bellek tasmasi", the FP8 KV cache paragraph).  E4M3 ("fn"): 1 sign
+ * bit, 4 exponent bits with bias 7, 3 fraction bits, no infinities, the
+ * code S.1111.111 is NaN, largest finite 448.  Stored code =
+ * E4M3(fp32(x) * fp32(1 / scale)), rounded to nearest-even and saturated to
+ * +-448; value = code * scale.  Scales are per KV head, for K and for V.
+ * Our layout reading: K blocks [num_blocks][Hkv][16][D] bytes as for 16-bit
+ * caches, V blocks stored dimension-major [num_blocks][Hkv][D][16].
+ */
+static double e4m3_to_double(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xf;
+    int f = c & 7;
+    double mag;
+    if (e == 15 && f == 7) return NAN;
+    if (e == 0) mag = ldexp((double)f, -9);              /* f/8 * 2^-6 */
+    else mag = ldexp((double)(8 + f), e - 10);           /* (1 + f/8) * 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+/* Round a float to the nearest E4M3 code (ties to even), saturating. */
+static uint8_t double_to_e4m3(double x) {
+    if (isnan(x)) return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 464.0) return sign | 0x7e;                  /* 464 ties to 448; above saturates */
+    if (a < ldexp(1.0, -6)) {                            /* subnormal grid: k * 2^-9 */
+        double k = a * 512.0;
+        double r = nearbyint(k);                          /* default mode: ties to even */
+        return sign | (uint8_t)r;                        /* r == 8 is the code of 2^-6 */
+    }
+    int e2;
+    frexp(a, &e2);                                       /* a = m * 2^e2, m in [0.5, 1) */
+    int e = e2 - 1;                                      /* a in [2^e, 2^(e+1)) */
+    double k = ldexp(a, 3 - e) - 8.0;                    /* fraction in eighths, [0, 8) */
+    double r = nearbyint(k);
+    if (r >= 8.0) { r = 0.0; e += 1; }
+    if (e > 8) return sign | 0x7e;
+    return sign | (uint8_t)(((e + 7) << 3) | (int)r);
+}
+
+void oracle_e4m3_to_double(const uint8_t* codes, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(codes[i]);
+}
+
+void oracle_float_to_e4m3(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = double_to_e4m3((double)x[i]);
+}
+
+/*
+ * FP8 cache write: like oracle_cache_write, with every value quantised as
+ * E4M3(fp32(value) * fp32(1 / scale[h])), K row-major per token, V written
+ * into the dimension-major V block.
+ */
+int64_t oracle_cache_write_fp8(const uint16_t* k, const uint16_t* v, int dtype,
+                               const int64_t* slot_mapping, int64_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               const float* k_scale, const float* v_scale, uint8_t* k_cache,
+                               uint8_t* v_cache, int64_t num_blocks);
+
 /* ---- cache write ---- */
 
 /*
@@ -122,6 +185,35 @@ int64_t oracle_cache_write(const uint16_t* k, const uint16_t* v, const int64_t* 
             for (int32_t d = 0; d < head_dim; ++d) {
                 k_cache[dst + d] = k[src + d];
                 v_cache[dst + d] = v[src + d];
+            }
+        }
+    }
+    return out_of_range;
+}
+
+int64_t oracle_cache_write_fp8(const uint16_t* k, const uint16_t* v, int dtype,
+                               const int64_t* slot_mapping, int64_t num_tokens,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               const float* k_scale, const float* v_scale, uint8_t* k_cache,
+                               uint8_t* v_cache, int64_t num_blocks) {
+    int64_t out_of_range = 0;
+    for (int64_t t = 0; t < num_tokens; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0) continue;
+        int64_t blk = s / block_size;
+        int64_t off = s % block_size;
+        if (blk >= num_blocks) { ++out_of_range; continue; }
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            float inv_k = 1.0f / k_scale[h];
+            float inv_v = 1.0f / v_scale[h];
+            int64_t src = (t * num_kv_heads + h) * (int64_t)head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                float xk = (float)to_double(k[src + d], dtype) * inv_k;
+                float xv = (float)to_double(v[src + d], dtype) * inv_v;
+                k_cache[((blk * num_kv_heads + h) * block_size + off) * (int64_t)head_dim + d] =
+                    double_to_e4m3((double)xk);
+                v_cache[((blk * num_kv_heads + h) * (int64_t)head_dim + d) * block_size + off] =
+                    double_to_e4m3((double)xv);
             }
         }
     }
@@ -249,6 +341,87 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_
             }
         }
         free(K); free(V); free(s); free(qd);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Decode over an FP8 cache: the same textbook attention as oracle_decode on
+ * the dequantised values K = code * k_scale[h], V = code * v_scale[h]
+ * (V read from its dimension-major blocks).  q is 16-bit (dtype).
+ */
+int oracle_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                      const float* k_scale, const float* v_scale, int dtype,
+                      const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, double scale, double* out,
+                      int num_threads) {
+    const int32_t G = num_q_heads / num_kv_heads;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+    int64_t n_pairs = (int64_t)num_seqs * num_kv_heads;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t pair = 0; pair < n_pairs; ++pair) {
+        int32_t b = (int32_t)(pair / num_kv_heads);
+        int32_t h = (int32_t)(pair % num_kv_heads);
+        int32_t L = seq_lens[b];
+        if (L <= 0) {
+            for (int32_t g = 0; g < G; ++g) {
+                double* o = out + ((int64_t)b * num_q_heads + (int64_t)h * G + g) * head_dim;
+                for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+            }
+            continue;
+        }
+        double* K = (double*)malloc(sizeof(double) * (size_t)L * head_dim);
+        double* V = (double*)malloc(sizeof(double) * (size_t)L * head_dim);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)L);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        if (!K || !V || !sc || !qd) {
+            free(K); free(V); free(sc); free(qd);
+            failed |= 1;
+            continue;
+        }
+        const int32_t* row = block_tables + (int64_t)b * max_blocks;
+        for (int32_t t = 0; t < L; ++t) {
+            int64_t phys = row[t / block_size];
+            int64_t off = t % block_size;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                K[(int64_t)t * head_dim + d] =
+                    e4m3_to_double(k_cache[((phys * num_kv_heads + h) * block_size + off) * head_dim + d]) *
+                    (double)k_scale[h];
+                V[(int64_t)t * head_dim + d] =
+                    e4m3_to_double(v_cache[((phys * num_kv_heads + h) * head_dim + d) * block_size + off]) *
+                    (double)v_scale[h];
+            }
+        }
+        for (int32_t g = 0; g < G; ++g) {
+            int32_t i = h * G + g;
+            const uint16_t* qi = q + ((int64_t)b * num_q_heads + i) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) qd[d] = to_double(qi[d], dtype);
+            double smax = -INFINITY;
+            for (int32_t t = 0; t < L; ++t) {
+                double acc = 0.0;
+                for (int32_t d = 0; d < head_dim; ++d) acc += qd[d] * K[(int64_t)t * head_dim + d];
+                sc[t] = scale * acc;
+                if (sc[t] > smax) smax = sc[t];
+            }
+            double denom = 0.0;
+            for (int32_t t = 0; t < L; ++t) {
+                sc[t] = exp(sc[t] - smax);
+                denom += sc[t];
+            }
+            double* o = out + ((int64_t)b * num_q_heads + i) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                double acc = 0.0;
+                for (int32_t t = 0; t < L; ++t) acc += sc[t] * V[(int64_t)t * head_dim + d];
+                o[d] = acc / denom;
+            }
+        }
+        free(K); free(V); free(sc); free(qd);
     }
     return failed ? -1 : 0;
 }

@@ -135,6 +135,71 @@ def pin_copy_blocks_golden(oracle, handle=None):
         assert np.array_equal(v2[blk], vc[srcb]), (blk, g["cite"])
 
 
+def pin_e4m3_codes(oracle, handle=None):
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_to_double(codes, handle=handle)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], ref[~nan])
+    # rounding: every float in [-464, 464] to its nearest code, ties to even,
+    # like torch; beyond that the code saturates to +-448 (torch gives NaN)
+    rng = np.random.default_rng(3)
+    vals = ref[~nan]
+    mids = (np.sort(vals)[1:] + np.sort(vals)[:-1]) / 2
+    x = np.concatenate([vals, mids, rng.uniform(-464, 464, 20000), rng.normal(0, 1, 20000),
+                        rng.normal(0, 1e-2, 5000), [464.0, -464.0]]).astype(np.float32)
+    x = x[np.abs(x) <= 464]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.float_to_e4m3(x, handle=handle)
+    assert np.array_equal(got, want)
+    sat = oracle.float_to_e4m3(np.array([470.0, 1e9, -500.0, np.nan], np.float32), handle=handle)
+    assert sat.tolist() == [0x7E, 0x7E, 0xFE, 0x7F]
+
+
+def pin_cache_write_fp8_golden(oracle, handle=None):
+    g = json.load(open(os.path.join(GOLD, "cache_write_fp8_example.json")))
+    nb, D = g["num_blocks"], g["head_dim"]
+    f = lambda x: torch.tensor(x, dtype=torch.float32).to(torch.bfloat16).view(torch.int16) \
+        .numpy().view(np.uint16)
+    k8 = np.full((nb, 1, 16, D), 0xAA, np.uint8)
+    v8 = np.full((nb, 1, D, 16), 0xAA, np.uint8)
+    kc, vc, bad = oracle.cache_write_fp8(f(g["k"]), f(g["v"]), "bf16", np.array(g["slots"], np.int64),
+                                         [g["k_scale"]], [g["v_scale"]], k8, v8, handle=handle)
+    assert bad == 0
+    ek, ev = k8.copy(), v8.copy()
+    for e in g["expect_k"]:
+        ek[e["block"], 0, e["row"], :] = e["codes"]
+    for e in g["expect_v"]:
+        ev[e["block"], 0, :, e["row"]] = e["codes"]
+    assert np.array_equal(kc, ek), g["cite"]
+    assert np.array_equal(vc, ev), g["cite"]
+
+
+def pin_decode_fp8_reduces_to_decode(oracle, handle=None):
+    """With power-of-two scales every dequantised value is exact in bf16, so
+    FP8 decode must equal the (pinned) 16-bit decode on those values."""
+    rng = np.random.default_rng(8)
+    nb, H, D, G = 12, 2, 128, 4
+    k8 = rng.integers(0, 256, (nb, H, 16, D), dtype=np.uint8)
+    v8 = rng.integers(0, 256, (nb, H, D, 16), dtype=np.uint8)
+    for a in (k8, v8):   # no NaN codes; keep magnitudes moderate (exponent <= 8)
+        a[(a & 0x7F) >= 0x78] &= 0x37
+    ks, vs = np.array([0.25, 2.0], np.float32), np.array([0.5, 4.0], np.float32)
+    lens = np.array([1, 16, 40, 130], np.int32)
+    tab = np.array([[3, 0, 0, 0, 0, 0, 0, 0, 0], [7, 0, 0, 0, 0, 0, 0, 0, 0],
+                    [1, 9, 4, 0, 0, 0, 0, 0, 0], [2, 5, 8, 10, 11, 0, 6, 1, 9]], np.int32)
+    q = torch.randn((4, H * G, D), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    to_bf16 = lambda codes, sc: (torch.from_numpy(codes).view(torch.float8_e4m3fn).double()
+                                 * torch.from_numpy(sc.astype(np.float64)).view(1, -1, 1, 1)) \
+        .to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    kc = to_bf16(k8, ks)
+    vc = to_bf16(np.ascontiguousarray(v8.transpose(0, 1, 3, 2)), vs)
+    got = oracle.decode_fp8(q, k8, v8, ks, vs, tab, lens, 0.09, "bf16", handle=handle)
+    ref = oracle.decode(q, kc, vc, tab, lens, 0.09, "bf16", handle=handle)
+    assert np.array_equal(got, ref)
+
+
 def pin_gather_is_contiguous_source(oracle, handle=None):
     for batch in small_batches():
         w = batch.workload
@@ -232,5 +297,6 @@ def pin_closed_forms(oracle, handle=None):
 
 
 ALL_PINS = [pin_kv_bytes, pin_bits, pin_cache_write_golden, pin_copy_blocks_golden,
+            pin_e4m3_codes, pin_cache_write_fp8_golden, pin_decode_fp8_reduces_to_decode,
             pin_gather_is_contiguous_source,
             pin_matches_sdpa, pin_relabel_invariance, pin_closed_forms]

@@ -27,6 +27,12 @@ MUTANTS = {
     "write_row_reversed": ("* block_size + off) * (int64_t)head_dim",
                            "* block_size + (block_size - 1 - off)) * (int64_t)head_dim"),
     "negative_slot_written": ("if (s < 0) continue;", "if (s < 0) s = 0;"),
+    "e4m3_exponent_bias": ("else mag = ldexp((double)(8 + f), e - 10);",
+                           "else mag = ldexp((double)(8 + f), e - 9);"),
+    "e4m3_round_up": ("double r = nearbyint(k);\n    if (r >= 8.0)", "double r = ceil(k);\n    if (r >= 8.0)"),
+    "fp8_v_token_major": ("v_cache[((blk * num_kv_heads + h) * (int64_t)head_dim + d) * block_size + off] =",
+                          "v_cache[((blk * num_kv_heads + h) * block_size + off) * (int64_t)head_dim + d] ="),
+    "fp8_scale_not_applied": ("(double)k_scale[h];\n                V[", "1.0;\n                V["),
     "copy_v_from_k": ("v_cache[dst[i] * per_block + e] = v_cache[src[i] * per_block + e];",
                       "v_cache[dst[i] * per_block + e] = k_cache[src[i] * per_block + e];"),
     "copy_direction": ("k_cache[dst[i] * per_block + e] = k_cache[src[i] * per_block + e];",
@@ -34,14 +40,31 @@ MUTANTS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_some_pin_catches_mutant(oracle_mod, tmp_path, name):
-    src = open(os.path.join(os.path.dirname(oracle_mod.__file__), "pa_oracle.c")).read()
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "pa_oracle.c")
+
+
+def _cases():
+    """One mutant per (mistake, occurrence): a line the 16-bit and the FP8
+    paths both contain is broken in each copy separately."""
+    src = open(SRC).read()
+    out = []
+    for name in sorted(MUTANTS):
+        n = src.count(MUTANTS[name][0])
+        out += [(name, k) for k in range(max(n, 1))]
+    return out
+
+
+@pytest.mark.parametrize("name,occurrence", _cases(), ids=lambda v: str(v))
+def test_some_pin_catches_mutant(oracle_mod, tmp_path, name, occurrence):
+    src = open(SRC).read()
     old, new = MUTANTS[name]
-    assert src.count(old) == 1, f"mutation anchor for {name} not unique in the oracle source"
-    mpath = tmp_path / f"mut_{name}.c"
-    mpath.write_text(src.replace(old, new))
-    lib = oracle_mod.compile_source(str(mpath), str(tmp_path / f"mut_{name}.so"))
+    assert src.count(old) >= 1, f"mutation anchor for {name} missing from the oracle source"
+    at = -1
+    for _ in range(occurrence + 1):
+        at = src.index(old, at + 1)
+    mpath = tmp_path / f"mut_{name}_{occurrence}.c"
+    mpath.write_text(src[:at] + new + src[at + len(old):])
+    lib = oracle_mod.compile_source(str(mpath), str(tmp_path / f"mut_{name}_{occurrence}.so"))
     handle = oracle_mod.OracleLib(lib)
     caught = []
     for pin in P.ALL_PINS:
