@@ -67,22 +67,27 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def algorithmic_bytes(lens, hq, hkv, d, elem=2, part_tokens=512):
-    """Bytes the attention kernel must move: K/V of every token once per KV
-    head, block ids, q, and either the output (one partition) or the fp32
-    partial (max, sum, head_dim values) of every partition."""
+def algorithmic_bytes(lens, hq, hkv, d, elem=2, part_tokens=512, kv_elem=None, starts=None):
+    """Bytes the attention kernel must move: K/V of every token it covers
+    once per KV head, block ids, q, and either the output (one partition) or
+    the fp32 partial (max, sum, head_dim values) of every partition.
+    ``starts``: first token each sequence's attention kernel covers (the
+    shared prefix of a grouped decode, whose partials always merge)."""
     L = np.asarray(lens, np.int64)
-    kv = int(L.sum()) * hkv * d * elem * 2
-    ids = int(((L + 15) // 16).sum()) * 4
+    st = np.zeros_like(L) if starts is None else np.asarray(starts, np.int64)
+    n = L - st
+    kv = int(n.sum()) * hkv * d * (elem if kv_elem is None else kv_elem) * 2
+    ids = int(((n + 15) // 16).sum()) * 4
     q = len(L) * hq * d * elem
-    nparts = (L + part_tokens - 1) // part_tokens
-    single = nparts == 1
-    out = int(single.sum()) * hq * d * elem
-    partial = int(nparts[~single].sum()) * hq * (d + 2) * 4
+    nparts = (n + part_tokens - 1) // part_tokens
+    direct = (nparts == 1) & (st == 0)
+    out = int(direct.sum()) * hq * d * elem
+    partial = int(nparts[~direct].sum()) * hq * (d + 2) * 4
     return kv + ids + q + out + partial
 
 
 def logical_kv_bytes(lens, hkv, d, elem=2):
+    """Sum over sequences of len x kv_heads x head_dim x 2 (K, V) x bytes."""
     return int(np.asarray(lens, np.int64).sum()) * hkv * d * elem * 2
 
 
@@ -298,6 +303,21 @@ def run_pa(args, rank, world, local_rank):
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     layers = [(Lr.q.view(dt), Lr.k_cache.view(dt), Lr.v_cache.view(dt), Lr.new_k.view(dt),
                Lr.new_v.view(dt)) for Lr in b.layers]
+    kv_elem = 2
+    if args.fp8:   # E4M3 caches (K token-major, V dimension-major), per-KV-head scales
+        kv_elem = 1
+        k_sc = torch.tensor([0.02 + 0.005 * h for h in range(w.num_kv_heads)], device=dev)
+        v_sc = torch.tensor([0.03 + 0.004 * h for h in range(w.num_kv_heads)], device=dev)
+        q8 = []
+        for (q, kc, vc, nk, nv) in layers:
+            k8 = (kc.float() / k_sc.view(1, -1, 1, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
+            v8 = (vc.float() / v_sc.view(1, -1, 1, 1)).to(torch.float8_e4m3fn).view(torch.uint8) \
+                .transpose(2, 3).contiguous()
+            q8.append((q, k8, v8, nk, nv))
+        layers = q8
+        for Lr in b.layers:
+            Lr.k_cache = Lr.v_cache = None
+        torch.cuda.empty_cache()
     nl = len(layers)
     tab = torch.from_numpy(b.block_tables).to(dev)
     lens = torch.from_numpy(b.seq_lens).to(dev)
@@ -316,13 +336,19 @@ def run_pa(args, rank, world, local_rank):
 
     def step(evs=None):
         for li, (q, kc, vc, nk, nv) in enumerate(layers):
+            ev = evs[li] if evs else None
+            if args.fp8:
+                pa.pa_cache_write_fp8(nk, nv, slots, k_sc, v_sc, kc, vc)
+                pa.pa_decode_fp8(q, kc, vc, k_sc, v_sc, tab, lens, w.scale, max_seq_len=msl,
+                                 out=out, workspace=ws, events=ev)
+                continue
             pa.pa_cache_write(nk, nv, slots, kc, vc)
             if grouped:
                 pa.pa_decode_grouped(q, kc, vc, tab, lens, w.scale, goff, gpre, max_seq_len=msl,
-                                     out=out, workspace=ws)
+                                     out=out, workspace=ws, variant=variant, events=ev)
             else:
                 pa.pa_decode(q, kc, vc, tab, lens, w.scale, max_seq_len=msl, out=out, workspace=ws,
-                             variant=variant, events=evs[li] if evs else None)
+                             variant=variant, events=ev)
 
     for _ in range(args.warmup):
         step()
@@ -352,19 +378,24 @@ def run_pa(args, rank, world, local_rank):
         time.sleep(0.15)
         sampler.stop()
     ms_total = start.elapsed_time(stop)
-    kern_ms = [a.elapsed_time(z) for row in ev_pairs for a, z in row] if not grouped else [float("nan")]
+    kern_ms = [a.elapsed_time(z) for row in ev_pairs for a, z in row]
     ms_step = reduce_max(ms_total / args.steps, dist, dev)
 
-    kvb = logical_kv_bytes(b.seq_lens, Hkv, D) * nl
+    kvb = logical_kv_bytes(b.seq_lens, Hkv, D, elem=kv_elem) * nl
     kv_gbs = job_throughput(kvb, world, ms_step * 1e-3) / 1e9
     part_tokens = int(ws[24:28].view(torch.int32).item())   # chosen by the prep kernel
-    alg = algorithmic_bytes(b.seq_lens, Hq, Hkv, D, part_tokens=part_tokens)
+    starts = None
+    if grouped:   # the attention kernel covers each member's tokens past the shared prefix
+        starts = np.repeat([p for _, p in b.groups], [m for m, _ in b.groups])
+    alg = algorithmic_bytes(b.seq_lens, Hq, Hkv, D, part_tokens=part_tokens, kv_elem=kv_elem,
+                            starts=starts)
     kern_avg = statistics.fmean(kern_ms)
     peak, peak_kind = measured_peaks()
     achieved = alg / (kern_avg * 1e-3) / 1e9
 
     # ---- end to end through the public API, host buffers -------------------------
-    e2e = run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist) \
+    e2e = run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped,
+                  (k_sc, v_sc) if args.fp8 else None) \
         if not args.no_e2e else None
 
     if rank != 0:
@@ -376,17 +407,19 @@ def run_pa(args, rank, world, local_rank):
         except Exception as ex:  # report, do not hide
             cpu = {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle",
                    "sample": f"failed: {ex!r}"}
-    traffic = load_traffic(args.workload, args.variant)
+    traffic = load_traffic(args.workload, "fp8" if args.fp8 else
+                           ("grouped" if grouped else args.variant))
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
     line = {
         "metric": METRIC, "value": kv_gbs, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.dtype == "bf16" else "f16", "data": "synthetic",
+        "dtype": ("fp8-e4m3 KV, " if args.fp8 else "") + ("bf16" if w.dtype == "bf16" else "f16"),
+        "data": "synthetic",
         "config": {"workload": DESCR.get(args.workload, args.workload),
                    "num_seqs": B, "layers": nl, "kv_tokens": int(b.seq_lens.sum()),
                    "logical_kv_bytes_per_step": kvb,
-                   "unique_kv_bytes_per_step": b.unique_kv_bytes() * nl,
+                   "unique_kv_bytes_per_step": b.unique_kv_bytes() * nl * kv_elem // 2,
                    "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV per step vs 129 MB L2; "
                          "no flush",
                    "step": f"{nl} x (pa_cache_write of one new token per sequence + pa_decode)",
@@ -414,12 +447,12 @@ def run_pa(args, rank, world, local_rank):
 # the ncu captures summarised in profiles/ (file named below), keyed by the
 # hash of the kernel sources they were taken on: a changed kernel reports null.
 TRAFFIC = {
-    ("llama70b", "auto"): {"bytes": 3.77e9 + 19.24e6, "kernel_src": "89dc4da88bac4115",
+    ("llama70b", "auto"): {"bytes": 3774.50e6 + 16.41e6, "kernel_src": "a120a382bf5025c3",
                            "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "mma"): {"bytes": 3.77e9 + 19.24e6, "kernel_src": "89dc4da88bac4115",
+    ("llama70b", "mma"): {"bytes": 3774.50e6 + 16.41e6, "kernel_src": "a120a382bf5025c3",
                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama8b", "auto"): {"bytes": 321.78e6 + 4.74e6, "kernel_src": "89dc4da88bac4115",
-                          "profile": "profiles/attend_kernel_llama70b_dram.md"},
+    ("llama70b", "fp8"): {"bytes": 1892.65e6 + 17.27e6, "kernel_src": "a120a382bf5025c3",
+                          "profile": "profiles/decode_step_llama70b_fp8_launches.md"},
 }
 
 
@@ -441,8 +474,11 @@ def load_traffic(workload, variant):
     return ent["bytes"]
 
 
-def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
-    """Same step through the public API from pinned host memory."""
+def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped=False,
+            scales=None):
+    """Same step through the public API from pinned host memory (E4M3 caches
+    with ``args.fp8``; shared-prefix groups decoded by pa_decode_grouped when
+    ``grouped``)."""
     import ctypes
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     nl = len(b.layers)
@@ -492,8 +528,13 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
     v_h = [torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory() for _ in range(nl)]
     out_h = [torch.empty((B, Hq, D), dtype=dt).pin_memory() for _ in range(nl)]
     slots_h = torch.empty(B, dtype=torch.int64).pin_memory()
-    caches = [(torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev),
-               torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev)) for _ in range(nl)]
+    if args.fp8:   # K token-major, V dimension-major bytes
+        caches = [(torch.zeros((nb, Hkv, 16, D), dtype=torch.uint8, device=dev),
+                   torch.zeros((nb, Hkv, D, 16), dtype=torch.uint8, device=dev)) for _ in range(nl)]
+        k_sc, v_sc = scales
+    else:
+        caches = [(torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev),
+                   torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev)) for _ in range(nl)]
     q_d = [torch.empty((B, Hq, D), dtype=dt, device=dev) for _ in range(nl)]
     k_d = [torch.empty((B, Hkv, D), dtype=dt, device=dev) for _ in range(nl)]
     v_d = [torch.empty((B, Hkv, D), dtype=dt, device=dev) for _ in range(nl)]
@@ -502,10 +543,18 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
     table_d = torch.empty((B, mb), dtype=torch.int32, device=dev)
     lens_d = torch.empty(B, dtype=torch.int32, device=dev)
     msl = mb * 16
-    ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
+    meta_h = [slots_h, table_h, lens_h]
+    if grouped:
+        groups_h = [torch.from_numpy(x).pin_memory() for x in b.group_arrays()]
+        groups_d = [torch.empty_like(x, device=dev) for x in groups_h]
+        meta_h += groups_h
+        ws = torch.empty(pa.pa_decode_grouped_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8,
+                         device=dev)
+    else:
+        ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
     slots_np, table_np, lens_np = slots_h.numpy(), table_h.numpy(), lens_h.numpy()
     nbytes = lambda t: t.numel() * t.element_size()
-    h2d = sum(nbytes(t) for t in q_h + k_h + v_h) + sum(nbytes(t) for t in (slots_h, table_h, lens_h))
+    h2d = sum(nbytes(t) for t in q_h + k_h + v_h) + sum(nbytes(t) for t in meta_h)
     d2h = sum(nbytes(t) for t in out_h)
     kv_bytes = []
 
@@ -517,17 +566,31 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
         slots_d.copy_(slots_h, non_blocking=True)
         table_d.copy_(table_h, non_blocking=True)
         lens_d.copy_(lens_h, non_blocking=True)
+        if grouped:
+            for hx, dx in zip(groups_h, groups_d):
+                dx.copy_(hx, non_blocking=True)
         for li in range(nl):
             q_d[li].copy_(q_h[li], non_blocking=True)
             k_d[li].copy_(k_h[li], non_blocking=True)
             v_d[li].copy_(v_h[li], non_blocking=True)
             kc, vc = caches[li]
-            pa.pa_cache_write(k_d[li], v_d[li], slots_d, kc, vc)
-            pa.pa_decode(q_d[li], kc, vc, table_d, lens_d, w.scale, max_seq_len=msl, out=out_d[li],
-                         workspace=ws, variant=variant)
+            if args.fp8:
+                pa.pa_cache_write_fp8(k_d[li], v_d[li], slots_d, k_sc, v_sc, kc, vc)
+                pa.pa_decode_fp8(q_d[li], kc, vc, k_sc, v_sc, table_d, lens_d, w.scale,
+                                 max_seq_len=msl, out=out_d[li], workspace=ws)
+            else:
+                pa.pa_cache_write(k_d[li], v_d[li], slots_d, kc, vc)
+                if grouped:
+                    pa.pa_decode_grouped(q_d[li], kc, vc, table_d, lens_d, w.scale, *groups_d,
+                                         max_seq_len=msl, out=out_d[li], workspace=ws,
+                                         variant=variant)
+                else:
+                    pa.pa_decode(q_d[li], kc, vc, table_d, lens_d, w.scale, max_seq_len=msl,
+                                 out=out_d[li], workspace=ws, variant=variant)
             out_h[li].copy_(out_d[li], non_blocking=True)
         torch.cuda.current_stream().synchronize()
-        kv_bytes.append(int(lens_np.astype(np.int64).sum()) * Hkv * D * 2 * 2 * nl)
+        kv_bytes.append(int(lens_np.astype(np.int64).sum()) * Hkv * D * 2 * (1 if args.fp8 else 2)
+                        * nl)
 
     for _ in range(args.warmup):
         one_step()
@@ -542,8 +605,11 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist):
     return {"value": job_throughput(statistics.fmean(kv_bytes), world, sec) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": sec * 1e3,
-            "path": "host allocator append_slots -> H2D (pinned) slots,table,lens and per layer "
-                    "q,k,v -> pa_cache_write -> pa_decode -> D2H out, then sync"}
+            "path": "host allocator append_slots -> H2D (pinned) slots,table,lens"
+                    + (",group offsets/prefixes" if grouped else "") + " and per layer q,k,v -> "
+                    + ("pa_cache_write_fp8 -> pa_decode_fp8" if args.fp8 else
+                       "pa_cache_write -> " + ("pa_decode_grouped" if grouped else "pa_decode"))
+                    + " -> D2H out, then sync"}
 
 
 def main():
@@ -557,9 +623,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="E4M3 KV caches: pa_cache_write_fp8 + pa_decode_fp8")
     ap.add_argument("--grouped", action="store_true",
                     help="decode shared-prefix groups with pa_decode_grouped (fullstep)")
     args = ap.parse_args()
+    if args.fp8 and args.grouped:
+        ap.error("--fp8 and --grouped do not combine (the shared-prefix kernel reads 16-bit caches)")
     if args.warmup < 3:
         args.warmup = 3
     rank = int(os.environ.get("RANK", "0"))

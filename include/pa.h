@@ -247,6 +247,9 @@ int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache,
  *                         allocator's forks guarantee it).
  *   workspace             >= pa_decode_grouped_workspace_bytes(...)
  *
+ * opts: as for pa_decode_ex (NULL = defaults); the events bracket the
+ * attention kernel over the members' own tokens, not the prefix kernel.
+ *
  * Invalid offsets or prefixes are flagged (PA_DEVERR_GROUP) and the affected
  * sequences are decoded without sharing -- still the correct result. */
 size_t pa_decode_grouped_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
@@ -258,7 +261,39 @@ int pa_decode_grouped(const void* d_q, const void* d_k_cache, const void* d_v_ca
                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
                       int32_t dtype, const int32_t* d_group_offsets,
                       const int32_t* d_group_prefix_tokens, int32_t num_groups, void* d_out,
-                      void* d_workspace, size_t workspace_bytes, void* stream);
+                      void* d_workspace, size_t workspace_bytes, void* stream,
+                      const pa_decode_opts* opts);
+
+/* ------------------------------------------------------------------------
+ * FP8 (E4M3) KV cache: half the bytes per token of a 16-bit cache, at some
+ * accuracy risk.  [P1] section "1. KV cache tuketimi ve GPU bellek
+ * tasmasi", the FP8 KV cache paragraph.  head_dim 128 only.
+ *
+ * Layout (bytes): K cache [num_blocks][num_kv_heads][16][128] as for 16-bit
+ * caches; V cache dimension-major [num_blocks][num_kv_heads][128][16] (the
+ * 16 tokens of one dimension are contiguous).  Scales: d_k_scale, d_v_scale
+ * [num_kv_heads] float, device; a stored byte is
+ * E4M3(fp32(x) * fp32(1 / scale[h])) -- rounded to nearest even, saturated to
+ * +-448 -- and stands for byte * scale[h].
+ *
+ * pa_cache_write_fp8 quantises and scatters new tokens exactly like
+ * pa_cache_write (k, v 16-bit of `dtype`).  pa_decode_fp8 is pa_decode over
+ * the dequantised caches: q and out are 16-bit of `dtype`, q is rounded to
+ * fp16 for the tensor cores (|q| must stay below 65504), accumulation fp32;
+ * workspace as for pa_decode (pa_decode_workspace_bytes).  opts may be NULL;
+ * its events work as for pa_decode_ex, variant must be 0 or 2 (the FP8 path
+ * has only the tensor-core math; 1 gives PA_ERR_UNSUPPORTED). */
+int pa_cache_write_fp8(const void* d_k, const void* d_v, const int64_t* d_slot_mapping,
+                       int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                       const float* d_k_scale, const float* d_v_scale, void* d_k_cache8,
+                       void* d_v_cache8, int64_t num_blocks, int32_t dtype, void* stream);
+
+int pa_decode_fp8(const void* d_q, const void* d_k_cache8, const void* d_v_cache8,
+                  const float* d_k_scale, const float* d_v_scale, int64_t num_blocks,
+                  const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
+                  int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                  int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
+                  size_t workspace_bytes, void* stream, const pa_decode_opts* opts);
 
 /* Waits for `stream`, then reads the device error bits the last decode
  * using this workspace left (PA_DEVERR_*; 0 = clean) into *error_bits.

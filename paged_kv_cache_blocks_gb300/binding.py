@@ -42,6 +42,21 @@ class PaDecodeOpts(ctypes.Structure):
 
 _lib = None
 
+
+def _opts(variant, events, stream):
+    """pa_decode_opts for a call, or None for the defaults."""
+    if not (variant or events):
+        return None
+    o = PaDecodeOpts()
+    o.variant = variant
+    if events:
+        for e in events:       # torch creates the CUDA event lazily, on first record
+            if not e.cuda_event:
+                e.record(torch.cuda.current_stream() if stream is None else stream)
+        o.event_before_main = events[0].cuda_event
+        o.event_after_main = events[1].cuda_event
+    return ctypes.byref(o)
+
 P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
     "pa_last_error_string": ([], ctypes.c_char_p),
@@ -62,9 +77,12 @@ _SIGS = {
     "pa_decode_ex": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, SZ, P, P],
                      ctypes.c_int),
     "pa_decode_check": ([P, P, P], ctypes.c_int),
+    "pa_cache_write_fp8": ([P, P, P, I32, I32, I32, P, P, P, P, I64, I32, P], ctypes.c_int),
+    "pa_decode_fp8": ([P, P, P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, SZ, P, P],
+                      ctypes.c_int),
     "pa_decode_grouped_workspace_bytes": ([I32, I32, I32, I32], SZ),
     "pa_decode_grouped": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P, I32, P,
-                           P, SZ, P], ctypes.c_int),
+                           P, SZ, P, P], ctypes.c_int),
     "pa_decode_noalloc": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P],
                           ctypes.c_int),
 }
@@ -163,17 +181,7 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0,
     need = pa_decode_workspace_bytes(B, Hq, D, msl)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    opts = None
-    if variant or events:
-        o = PaDecodeOpts()
-        o.variant = variant
-        if events:
-            for e in events:       # torch creates the CUDA event lazily, on first record
-                if not e.cuda_event:
-                    e.record(torch.cuda.current_stream() if stream is None else stream)
-            o.event_before_main = events[0].cuda_event
-            o.event_after_main = events[1].cuda_event
-        opts = ctypes.byref(o)
+    opts = _opts(variant, events, stream)
     rc = lib().pa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), mb,
                             _ptr(seq_lens), B, msl, Hq, Hkv, D, float(scale), _dtype_code(q, dtype),
                             _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream), opts)
@@ -198,15 +206,52 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, max_se
     return out
 
 
+def pa_cache_write_fp8(k, v, slot_mapping, k_scale, v_scale, k_cache8, v_cache8, dtype=None,
+                       stream=None):
+    """Quantise k/v [T, Hkv, 128] (16-bit) to E4M3 into k_cache8 [NB, Hkv, 16, 128]
+    and the dimension-major v_cache8 [NB, Hkv, 128, 16] (uint8 tensors)."""
+    _need_cuda(k, v, slot_mapping, k_scale, v_scale, k_cache8, v_cache8)
+    assert k_cache8.dtype == torch.uint8 and v_cache8.dtype == torch.uint8
+    assert k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32
+    T, H, D = k.shape
+    rc = lib().pa_cache_write_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), T, H, D, _ptr(k_scale),
+                                  _ptr(v_scale), _ptr(k_cache8), _ptr(v_cache8), k_cache8.shape[0],
+                                  _dtype_code(k, dtype), _stream(stream))
+    _check(rc, "pa_cache_write_fp8")
+
+
+def pa_decode_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_lens, scale,
+                  max_seq_len=0, out=None, workspace=None, dtype=None, stream=None, events=None):
+    """pa_decode over E4M3 caches (see pa_cache_write_fp8 for the layout);
+    ``events`` as for pa_decode."""
+    _need_cuda(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_lens)
+    B, Hq, D = q.shape
+    NB, Hkv = k_cache8.shape[0], k_cache8.shape[1]
+    mb = block_tables.shape[1]
+    msl = max_seq_len if max_seq_len > 0 else mb * BLOCK_SIZE
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(max(pa_decode_workspace_bytes(B, Hq, D, msl), 256),
+                                dtype=torch.uint8, device=q.device)
+    rc = lib().pa_decode_fp8(_ptr(q), _ptr(k_cache8), _ptr(v_cache8), _ptr(k_scale), _ptr(v_scale), NB,
+                             _ptr(block_tables), mb, _ptr(seq_lens), B, msl, Hq, Hkv, D, float(scale),
+                             _dtype_code(q, dtype), _ptr(out), _ptr(workspace), workspace.numel(),
+                             _stream(stream), _opts(0, events, stream))
+    _check(rc, "pa_decode_fp8")
+    return out
+
+
 def pa_decode_grouped_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len):
     return int(lib().pa_decode_grouped_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len))
 
 
 def pa_decode_grouped(q, k_cache, v_cache, block_tables, seq_lens, scale, group_offsets,
                       group_prefix_tokens, max_seq_len=0, out=None, workspace=None, dtype=None,
-                      stream=None):
+                      stream=None, variant=0, events=None):
     """pa_decode where contiguous groups of sequences share a prefix:
-    group_offsets [G+1] and group_prefix_tokens [G] are int32 CUDA tensors."""
+    group_offsets [G+1] and group_prefix_tokens [G] are int32 CUDA tensors.
+    ``events`` bracket the attention kernel over the members' own tokens."""
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens, group_offsets, group_prefix_tokens)
     assert group_offsets.dtype == torch.int32 and group_prefix_tokens.dtype == torch.int32
     B, Hq, D = q.shape
@@ -222,7 +267,8 @@ def pa_decode_grouped(q, k_cache, v_cache, block_tables, seq_lens, scale, group_
                                  _ptr(seq_lens), B, msl, Hq, Hkv, D, float(scale),
                                  _dtype_code(q, dtype), _ptr(group_offsets),
                                  _ptr(group_prefix_tokens), group_prefix_tokens.numel(), _ptr(out),
-                                 _ptr(workspace), workspace.numel(), _stream(stream))
+                                 _ptr(workspace), workspace.numel(), _stream(stream),
+                                 _opts(variant, events, stream))
     _check(rc, "pa_decode_grouped")
     return out
 

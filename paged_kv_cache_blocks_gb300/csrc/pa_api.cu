@@ -58,6 +58,28 @@ int pa_cache_write(const void* d_k, const void* d_v, const int64_t* d_slot_mappi
   return rc ? fail(rc, why) : PA_OK;
 }
 
+int pa_cache_write_fp8(const void* d_k, const void* d_v, const int64_t* d_slot_mapping,
+                       int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                       const float* d_k_scale, const float* d_v_scale, void* d_k_cache8,
+                       void* d_v_cache8, int64_t num_blocks, int32_t dtype, void* stream) {
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "pa_cache_write_fp8: num_tokens < 0");
+  if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_cache_write_fp8: dtype");
+  if (head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "pa_cache_write_fp8: head_dim must be 128");
+  if (num_kv_heads <= 0 || num_blocks <= 0)
+    return fail(PA_ERR_INVALID, "pa_cache_write_fp8: num_kv_heads and num_blocks must be > 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!d_k || !d_v || !d_slot_mapping || !d_k_cache8 || !d_v_cache8 || !d_k_scale || !d_v_scale)
+    return fail(PA_ERR_INVALID, "pa_cache_write_fp8: NULL pointer");
+  if (!aligned(d_k, 16) || !aligned(d_v, 16) || !aligned(d_k_cache8, 16) || !aligned(d_v_cache8, 16) ||
+      !aligned(d_slot_mapping, 8) || !aligned(d_k_scale, 4) || !aligned(d_v_scale, 4))
+    return fail(PA_ERR_INVALID, "pa_cache_write_fp8: k, v and caches must be 16-byte aligned");
+  std::string why;
+  int rc = pa::cache_write_fp8_launch(d_k, d_v, d_slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                      d_k_scale, d_v_scale, d_k_cache8, d_v_cache8, num_blocks, dtype,
+                                      stream, &why);
+  return rc ? fail(rc, why) : PA_OK;
+}
+
 int pa_copy_blocks(void* d_k_cache, void* d_v_cache, int64_t num_blocks, int32_t num_kv_heads,
                    int32_t head_dim, const int32_t* d_src, const int32_t* d_dst, int32_t n_pairs,
                    void* stream) {
@@ -93,7 +115,9 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
                   int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
                   size_t workspace_bytes, void* stream, const pa_decode_opts* opts,
                   const int32_t* d_group_offsets, const int32_t* d_group_prefix_tokens,
-                  int32_t num_groups) {
+                  int32_t num_groups, const float* d_k_scale = nullptr,
+                  const float* d_v_scale = nullptr) {
+  const bool fp8 = d_k_scale != nullptr;
   if (num_seqs < 0) return fail(PA_ERR_INVALID, "pa_decode: num_seqs < 0");
   if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_decode: dtype");
   if (!supported_head_dim(head_dim))
@@ -107,6 +131,12 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
     return fail(PA_ERR_INVALID, "pa_decode: num_blocks and max_blocks_per_seq must be > 0");
   if (num_blocks * num_kv_heads * PA_BLOCK_SIZE > INT32_MAX)
     return fail(PA_ERR_UNSUPPORTED, "pa_decode: num_blocks * num_kv_heads * 16 must be < 2^31");
+  if (fp8 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: head_dim must be 128");
+  if (fp8 && num_blocks * num_kv_heads * head_dim > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: num_blocks * num_kv_heads * 128 must be < 2^31");
+  if (fp8 && (!d_v_scale || !aligned(d_k_scale, 4) || !aligned(d_v_scale, 4)))
+    return fail(PA_ERR_INVALID, "pa_decode_fp8: k_scale and v_scale must be device float arrays");
   if (static_cast<int64_t>(max_blocks_per_seq) * PA_BLOCK_SIZE > INT32_MAX)
     return fail(PA_ERR_INVALID, "pa_decode: max_blocks_per_seq too large");
   const int32_t cap = max_blocks_per_seq * PA_BLOCK_SIZE;
@@ -161,6 +191,9 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
   a.group_off = d_group_offsets;
   a.group_prefix = d_group_prefix_tokens;
   a.num_groups = num_groups;
+  a.fp8 = fp8;
+  a.k_scale = d_k_scale;
+  a.v_scale = d_v_scale;
   std::string why;
   int rc = pa::decode_launch(a, &why);
   return rc ? fail(rc, why) : PA_OK;
@@ -186,18 +219,34 @@ size_t pa_decode_grouped_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, 
   return pa::decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len, true);
 }
 
+int pa_decode_fp8(const void* d_q, const void* d_k_cache8, const void* d_v_cache8,
+                  const float* d_k_scale, const float* d_v_scale, int64_t num_blocks,
+                  const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
+                  int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                  int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
+                  size_t workspace_bytes, void* stream, const pa_decode_opts* opts) {
+  if (!d_k_scale) return fail(PA_ERR_INVALID, "pa_decode_fp8: NULL k_scale");
+  if (opts && opts->variant == 1)
+    return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: only the tensor-core variant exists");
+  return decode_common(d_q, d_k_cache8, d_v_cache8, num_blocks, d_block_tables, max_blocks_per_seq,
+                       d_seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, scale,
+                       dtype, d_out, d_workspace, workspace_bytes, stream, opts, nullptr, nullptr,
+                       0, d_k_scale, d_v_scale);
+}
+
 int pa_decode_grouped(const void* d_q, const void* d_k_cache, const void* d_v_cache,
                       int64_t num_blocks, const int32_t* d_block_tables, int32_t max_blocks_per_seq,
                       const int32_t* d_seq_lens, int32_t num_seqs, int32_t max_seq_len,
                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, float scale,
                       int32_t dtype, const int32_t* d_group_offsets,
                       const int32_t* d_group_prefix_tokens, int32_t num_groups, void* d_out,
-                      void* d_workspace, size_t workspace_bytes, void* stream) {
+                      void* d_workspace, size_t workspace_bytes, void* stream,
+                      const pa_decode_opts* opts) {
   if (num_groups <= 0 && num_seqs > 0)
     return fail(PA_ERR_INVALID, "pa_decode_grouped: num_groups must be >= 1");
   return decode_common(d_q, d_k_cache, d_v_cache, num_blocks, d_block_tables, max_blocks_per_seq,
                        d_seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, scale,
-                       dtype, d_out, d_workspace, workspace_bytes, stream, nullptr, d_group_offsets,
+                       dtype, d_out, d_workspace, workspace_bytes, stream, opts, d_group_offsets,
                        d_group_prefix_tokens, num_groups);
 }
 

@@ -60,6 +60,78 @@ int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping
   return 0;
 }
 
+// FP8 cache write: the same scatter, each value quantised to E4M3 as
+// E4M3(fp32(x) * fp32(1 / scale[h])) (round to nearest even, saturated).
+// K rows stay token-major ([block][head][16][D]); V is stored dimension-major
+// ([block][head][D][16]) so the decode kernel can feed it to the tensor cores
+// without a transpose.  One thread per 8 values of a (token, head) row.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    cache_write_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                           const int64_t* __restrict__ slot_mapping, int64_t n_chunks, int hkv, int D,
+                           const float* __restrict__ k_scale, const float* __restrict__ v_scale,
+                           uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                           int64_t num_blocks) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n_chunks) return;
+  const int cpr = D / 8;
+  const int64_t t = i / (static_cast<int64_t>(hkv) * cpr);
+  const int rem = static_cast<int>(i - t * hkv * cpr);
+  const int h = rem / cpr, c = rem - h * cpr;
+  const int64_t s = slot_mapping[t];
+  if (s < 0) return;
+  const int64_t blk = s / kBlock;
+  if (blk >= num_blocks) return;
+  const int64_t off = s - blk * kBlock;
+  const float ik = 1.0f / k_scale[h], iv = 1.0f / v_scale[h];
+  const uint4 kv = *reinterpret_cast<const uint4*>(k + (t * hkv + h) * D + 8 * c);
+  const uint4 vv = *reinterpret_cast<const uint4*>(v + (t * hkv + h) * D + 8 * c);
+  const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w}, vw[4] = {vv.x, vv.y, vv.z, vv.w};
+  uint16_t kq[4], vq[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 a = unpack2<T>(kw[e]), b = unpack2<T>(vw[e]);
+    kq[e] = float2_to_e4m3x2(a.x * ik, a.y * ik);
+    vq[e] = float2_to_e4m3x2(b.x * iv, b.y * iv);
+  }
+  uint2 kout;
+  kout.x = static_cast<uint32_t>(kq[0]) | (static_cast<uint32_t>(kq[1]) << 16);
+  kout.y = static_cast<uint32_t>(kq[2]) | (static_cast<uint32_t>(kq[3]) << 16);
+  *reinterpret_cast<uint2*>(k_cache + ((blk * hkv + h) * kBlock + off) * D + 8 * c) = kout;
+  uint8_t* vrow = v_cache + ((blk * hkv + h) * D + 8 * c) * kBlock + off;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    vrow[(2 * e) * kBlock] = static_cast<uint8_t>(vq[e] & 0xff);
+    vrow[(2 * e + 1) * kBlock] = static_cast<uint8_t>(vq[e] >> 8);
+  }
+}
+
+int cache_write_fp8_launch(const void* k, const void* v, const int64_t* slot_mapping,
+                           int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                           const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,
+                           int64_t num_blocks, int32_t dtype, void* stream, std::string* why) {
+  const int64_t n_chunks = static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim / 8);
+  if (n_chunks == 0) return 0;
+  const int64_t blocks = (n_chunks + 255) / 256;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == 1)
+    cache_write_fp8_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), slot_mapping,
+        n_chunks, num_kv_heads, head_dim, k_scale, v_scale, static_cast<uint8_t*>(k_cache),
+        static_cast<uint8_t*>(v_cache), num_blocks);
+  else
+    cache_write_fp8_kernel<__half><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        static_cast<const __half*>(k), static_cast<const __half*>(v), slot_mapping, n_chunks,
+        num_kv_heads, head_dim, k_scale, v_scale, static_cast<uint8_t*>(k_cache),
+        static_cast<uint8_t*>(v_cache), num_blocks);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("cache_write_fp8 launch: ") + cudaGetErrorString(e);
+    return 5;
+  }
+  return 0;
+}
+
 // Copy-on-write block copy ("vLLM ve Triton ile maliyet optimizasyonu",
 // section 03: a shared block is copied when one holder writes into it).
 // One CTA per (pair, K or V): the whole block -- every KV head's 16 rows -- is

@@ -12,13 +12,15 @@
 //   1. prep   (1 CTA)    clamps lengths, cuts every sequence into 512-token
 //                        partitions, lists them (full partitions first) in
 //                        the workspace and resets the work counters;
-//   2. attend (persistent, one or two CTAs per SM)
-//                        one work item = (partition, KV head).  Warp 0 is the
-//                        producer: it takes items from an atomic counter,
-//                        reads the partition's block ids and streams each
-//                        block's K and V tiles into a ring of shared-memory
-//                        stages with TMA (128-byte swizzle), completion on
-//                        mbarriers.  The other warps consume blocks
+//   2. attend (persistent, two or three CTAs per SM)
+//                        one work item = (partition, KV head).  Warp 0
+//                        schedules: it takes items from an atomic counter
+//                        (one ahead) and stages each item's partition record
+//                        and block ids in a two-slot item ring.  Warp 1 (one
+//                        thread) streams each block's K and V tiles into a
+//                        ring of shared-memory stages with TMA (128-byte
+//                        swizzle), completion on mbarriers, without ever
+//                        waiting on global memory.  The other warps consume blocks
 //                        round-robin, each keeping an online softmax (running
 //                        max and sum, fp32) for the G heads; at the end of an
 //                        item they merge their states through shared memory
@@ -63,6 +65,8 @@ struct DecodeParams {
   const int32_t* group_off;     // [num_groups + 1] or null
   const int32_t* group_prefix;  // [num_groups] or null
   int32_t num_groups;
+  const float* k_scale;         // FP8 caches: per KV head dequantisation scales
+  const float* v_scale;
   float2* ml;
   float* acc;
   int64_t num_blocks;
@@ -604,13 +608,165 @@ struct FmaState {
   }
 };
 
+// ---- FP8 math ------------------------------------------------------------------
+// Caches hold E4M3 bytes: K tiles [16 tokens][D] (128-byte swizzle), V tiles
+// dimension-major [D][16 tokens].  ldmatrix on byte rows hands each lane four
+// consecutive bytes per 8x8 matrix of 16-bit cells; cvt.f16x2.e4m3x2 turns
+// them into fp16 exactly.  The four bytes land on the mma fragment slots
+// (k = 2t, 2t+1, 2t+8, 2t+9), so both reductions run in a permuted order:
+//   QK: k slot (2t, 2t+1, 2t+8, 2t+9) <-> head_dim (4t .. 4t+3) of the 16-dim
+//       step; q is loaded in that order.  A-row r of the K operand is token
+//       sigma(r) (chosen by the ldmatrix row addresses), sigma = (0 1 4 5 8 9
+//       12 13 | 2 3 6 7 10 11 14 15), so that after movmatrix the P operand's
+//       k slots hold tokens 4t .. 4t+3 --
+//   PV: exactly the tokens the V rows deliver in those slots.
+// The scales fold in: scores use scale * k_scale[h], outputs are * v_scale[h].
+
+__device__ __forceinline__ int fp8_sigma(int r) {
+  return r < 8 ? 4 * (r >> 1) + (r & 1) : 4 * ((r - 8) >> 1) + 2 + (r & 1);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <typename T, int D>
+struct Fp8State {
+  uint32_t qb[D / 16][2];
+  float m[2], l[2];
+  float o[D / 16][4];
+  float sl, vs;
+
+  __device__ __forceinline__ void begin(const DecodeParams& P, const ItemInfo& it, int lane, float*) {
+    const int g = lane >> 2, t = lane & 3;
+    const T* q = static_cast<const T*>(P.q) +
+                 (static_cast<int64_t>(it.b) * P.hq + it.h * P.G + g) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      if (g < P.G) {
+        const uint2 w = *reinterpret_cast<const uint2*>(q + 16 * ks + 4 * t);
+        const float2 a = unpack2<T>(w.x), b = unpack2<T>(w.y);
+        qb[ks][0] = pack_half2(a.x, a.y);
+        qb[ks][1] = pack_half2(b.x, b.y);
+      } else {
+        qb[ks][0] = qb[ks][1] = 0u;
+      }
+    }
+    sl = P.scale_log2 * P.k_scale[it.h];
+    vs = P.v_scale[it.h];
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  }
+
+  __device__ __forceinline__ void block(uint32_t sK, uint32_t sV, int nvalid, float, int lane,
+                                        float*) {
+    const int g = lane >> 2, t = lane & 3;
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      // two independent accumulation chains (even / odd k-steps) halve the
+      // dependent mma latency of a block
+      float s2[4] = {0.f, 0.f, 0.f, 0.f};
+      const int tok = fp8_sigma((lane & 7) + 8 * ((lane >> 3) & 1));
+      const int cofs = lane >> 4;
+#pragma unroll
+      for (int kk = 0; kk < D / 32; ++kk) {
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4(r0, r1, r2, r3, sK + swz128(tok, 2 * kk + cofs));
+        Mma<__half>::run(s, e4m3x2_to_half2(r0 & 0xffff), e4m3x2_to_half2(r1 & 0xffff),
+                         e4m3x2_to_half2(r0 >> 16), e4m3x2_to_half2(r1 >> 16), qb[2 * kk][0],
+                         qb[2 * kk][1]);
+        Mma<__half>::run(s2, e4m3x2_to_half2(r2 & 0xffff), e4m3x2_to_half2(r3 & 0xffff),
+                         e4m3x2_to_half2(r2 >> 16), e4m3x2_to_half2(r3 >> 16), qb[2 * kk + 1][0],
+                         qb[2 * kk + 1][1]);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s[c] += s2[c];
+    }
+    const bool v0 = fp8_sigma(g) < nvalid, v1 = fp8_sigma(g + 8) < nvalid;
+    const float x0 = v0 ? s[0] * sl : -INFINITY;
+    const float x1 = v0 ? s[1] * sl : -INFINITY;
+    const float x2 = v1 ? s[2] * sl : -INFINITY;
+    const float x3 = v1 ? s[3] * sl : -INFINITY;
+    float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o2));
+      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o2));
+    }
+    const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);
+    const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
+    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+    l[0] = l[0] * al0 + (p0 + p2);
+    l[1] = l[1] * al1 + (p1 + p3);
+    m[0] = mn0;
+    m[1] = mn1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+    const uint32_t b0 = movmatrix_trans(pack_half2(p0, p1));
+    const uint32_t b1 = movmatrix_trans(pack_half2(p2, p3));
+    uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+    if (nvalid < 16) {
+      mk0 = (4 * t < nvalid ? 0x0000ffffu : 0u) | (4 * t + 1 < nvalid ? 0xffff0000u : 0u);
+      mk1 = (4 * t + 2 < nvalid ? 0x0000ffffu : 0u) | (4 * t + 3 < nvalid ? 0xffff0000u : 0u);
+    }
+    {
+      const int row = (lane & 7) + 8 * ((lane >> 3) & 1) + 16 * (lane >> 4);
+#pragma unroll
+      for (int mm = 0; mm < D / 32; ++mm) {
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4(r0, r1, r2, r3, sV + (32 * mm + row) * 16);
+        Mma<__half>::run(o[2 * mm], e4m3x2_to_half2(r0 & 0xffff) & mk0,
+                         e4m3x2_to_half2(r1 & 0xffff) & mk0, e4m3x2_to_half2(r0 >> 16) & mk1,
+                         e4m3x2_to_half2(r1 >> 16) & mk1, b0, b1);
+        Mma<__half>::run(o[2 * mm + 1], e4m3x2_to_half2(r2 & 0xffff) & mk0,
+                         e4m3x2_to_half2(r3 & 0xffff) & mk0, e4m3x2_to_half2(r2 >> 16) & mk1,
+                         e4m3x2_to_half2(r3 >> 16) & mk1, b0, b1);
+      }
+    }
+  }
+
+  template <int NC>
+  __device__ __forceinline__ void store(MergeSlot<D, NC>& ms, int w, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float L0 = l[0], L1 = l[1];
+#pragma unroll
+    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+      L0 += __shfl_xor_sync(0xffffffffu, L0, o2);
+      L1 += __shfl_xor_sync(0xffffffffu, L1, o2);
+    }
+    if (g == 0) {
+      ms.m[w][2 * t] = m[0];
+      ms.m[w][2 * t + 1] = m[1];
+      ms.l[w][2 * t] = L0;
+      ms.l[w][2 * t + 1] = L1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      ms.acc[w][2 * t][16 * mt + g] = o[mt][0] * vs;
+      ms.acc[w][2 * t + 1][16 * mt + g] = o[mt][1] * vs;
+      ms.acc[w][2 * t][16 * mt + g + 8] = o[mt][2] * vs;
+      ms.acc[w][2 * t + 1][16 * mt + g + 8] = o[mt][3] * vs;
+    }
+  }
+};
+
 constexpr size_t align_up_c(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-template <typename T, int D, int NC, int S, bool kFma>
+template <typename T, int D, int NC, int S, bool kFma, bool kFp8 = false>
 struct AttendCfg {
   static_assert(S % NC == 0, "within an item, each ring stage must be consumed by one warp");
-  static constexpr int kThreads = 32 * (NC + 1);
-  static constexpr int kStageBytes = Tile<D>::kStageBytes;
+  static constexpr int kThreads = 32 * (NC + 2);  // scheduler, TMA, NC consumers
+  static constexpr int kKBytes = kFp8 ? kBlock * D : Tile<D>::kKVBytes;  // K part of a stage
+  static constexpr int kStageBytes = kFp8 ? 2 * kBlock * D : Tile<D>::kStageBytes;
   static constexpr size_t kStagesOff = 0;
   static constexpr size_t kMergeOff = static_cast<size_t>(S) * kStageBytes;
   static constexpr size_t kScrOff = kMergeOff + 2 * sizeof(MergeSlot<D, NC>);
@@ -623,12 +779,14 @@ struct AttendCfg {
   static constexpr size_t kBytes = kAbortOff + 16 + 1024;  // + slack to 1024-align the base
 };
 
-template <typename T, int D, int NC, int S, bool kFma, int HPG>
-__global__ void __launch_bounds__(32 * (NC + 1))
+template <typename T, int D, int NC, int S, bool kFma, int HPG, bool kFp8 = false>
+__global__ void __launch_bounds__(32 * (NC + 2))
     attend_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeParams P) {
-  using Cfg = AttendCfg<T, D, NC, S, kFma>;
-  using State = typename std::conditional<kFma, FmaState<T, D, HPG>, MmaState<T, D>>::type;
+  using Cfg = AttendCfg<T, D, NC, S, kFma, kFp8>;
+  using State = typename std::conditional<
+      kFp8, Fp8State<T, D>,
+      typename std::conditional<kFma, FmaState<T, D, HPG>, MmaState<T, D>>::type>::type;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -653,7 +811,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&item_full[s], 1);
-      mbar_init(&item_empty[s], NC);
+      mbar_init(&item_empty[s], NC + 1);  // consumers + the TMA thread
       mbar_init(&merge_full[s], NC);
     }
     *abort_flag = 0;
@@ -662,26 +820,24 @@ __global__ void __launch_bounds__(32 * (NC + 1))
   __syncthreads();
 
   if (warp == 0) {
-    // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-    }
+    // ------------------------------------------------------------ scheduler
+    // Takes work items from the atomic counter one item ahead and stages each
+    // item's partition record and block ids in the item ring, so the TMA warp
+    // never waits on global memory between items.
     const int32_t n_items = *reinterpret_cast<volatile int32_t*>(&P.ws->n_items);
     const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
-    const int64_t y_oob = P.num_blocks * P.hkv * kBlock;  // one past the pool: reads as zeros
-    uint32_t g = 0;  // blocks issued by this CTA
-    bool ok = true;
-    for (uint32_t it = 0; ok; ++it) {
+    uint32_t g = 0;  // blocks of this CTA's stream before the next item
+    int next = 0;
+    if (lane == 0) next = atomicAdd(&P.ws->next_item, 1);
+    for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
-      int item = 0;
+      const int item = __shfl_sync(0xffffffffu, next, 0);
+      bool ok = true;
       if (lane == 0) {
-        item = atomicAdd(&P.ws->next_item, 1);
         ok = mbar_wait(&item_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, err);
+        if (ok && item < n_items) next = atomicAdd(&P.ws->next_item, 1);
       }
-      item = __shfl_sync(0xffffffffu, item, 0);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (item >= n_items) {
         if (lane == 0) {
           info[slot].b = -1;
@@ -707,14 +863,44 @@ __global__ void __launch_bounds__(32 * (NC + 1))
         info[slot] = ItemInfo{pi.b, h, pi.p, pi.len, pi.nparts, nblk, static_cast<int32_t>(g), part,
                               pi.start, 0};
         mbar_arrive(&item_full[slot]);
-        for (int j = 0; j < nblk && ok; ++j, ++g) {
-          const int st = g % S;
-          ok = mbar_wait(&empty[st], ((g / S) & 1) ^ 1, abort_flag, err);
-          if (!ok) break;
-          const int32_t id = ids[slot * kMaxPartBlocks + j];
-          const int32_t y = static_cast<int32_t>(id < 0 ? y_oob : (static_cast<int64_t>(id) * P.hkv + h) * kBlock);
-          uint8_t* dst = stages + static_cast<size_t>(st) * Cfg::kStageBytes;
-          mbar_arrive_expect_tx(&full[st], Cfg::kStageBytes);
+      }
+      g += nblk;
+    }
+    return;
+  }
+
+  if (warp == 1) {
+    // ---------------------------------------------------------------- TMA
+    // One thread streams every block of every item into the stage ring.
+    if (lane != 0) return;
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    const int64_t y_oob = P.num_blocks * P.hkv * kBlock;  // one past the pool: reads as zeros
+    uint32_t g = 0;  // blocks issued by this CTA
+    bool ok = true;
+    for (uint32_t it = 0; ok; ++it) {
+      const int slot = it & 1;
+      ok = mbar_wait(&item_full[slot], (it >> 1) & 1, abort_flag, err);
+      if (!ok) break;
+      const ItemInfo inf = info[slot];
+      if (inf.b < 0) {
+        mbar_arrive(&item_empty[slot]);
+        break;
+      }
+      for (int j = 0; j < inf.nblk; ++j, ++g) {
+        const int st = g % S;
+        ok = mbar_wait(&empty[st], ((g / S) & 1) ^ 1, abort_flag, err);
+        if (!ok) break;
+        const int32_t id = ids[slot * kMaxPartBlocks + j];
+        const int32_t y = static_cast<int32_t>(id < 0 ? y_oob : (static_cast<int64_t>(id) * P.hkv + inf.h) * kBlock);
+        uint8_t* dst = stages + static_cast<size_t>(st) * Cfg::kStageBytes;
+        mbar_arrive_expect_tx(&full[st], Cfg::kStageBytes);
+        if constexpr (kFp8) {
+          // K and V tiles: one box of 16 rows x D bytes each (V's rows are
+          // groups of D/16 dimensions of 16 tokens)
+          tma_load_2d(dst, &tm_k, 0, y, &full[st]);
+          tma_load_2d(dst + Cfg::kKBytes, &tm_v, 0, y, &full[st]);
+        } else {
 #pragma unroll
           for (int hf = 0; hf < Tile<D>::kHalves; ++hf) {
             tma_load_2d(dst + hf * Tile<D>::kHalfBytes, &tm_k, hf * 64, y, &full[st]);
@@ -722,10 +908,9 @@ __global__ void __launch_bounds__(32 * (NC + 1))
           }
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      g = __shfl_sync(0xffffffffu, g, 0);
+      if (ok) mbar_arrive(&item_empty[slot]);
     }
-    if (!ok && lane == 0) {
+    if (!ok) {
       // Abort: let the copies this CTA issued land before it exits.
       const uint32_t lo = g > static_cast<uint32_t>(S) ? g - S : 0;
       for (uint32_t k = lo; k < g; ++k) {
@@ -739,7 +924,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
   }
 
   // ---------------------------------------------------------------- consumers
-  const int w = warp - 1;
+  const int w = warp - 2;
   const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
   float* scr = scratch + (kFma ? w * FmaScratch<D>::kFloats : 0);
   State st;
@@ -770,7 +955,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       }
       const uint32_t sK = smem_u32(stages + static_cast<size_t>(s) * Cfg::kStageBytes);
       const int nvalid = min(kBlock, inf.len - (inf.start + inf.p * pt + j * kBlock));
-      st.block(sK, sK + Tile<D>::kKVBytes, nvalid, P.scale_log2, lane, scr);
+      st.block(sK, sK + Cfg::kKBytes, nvalid, P.scale_log2, lane, scr);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -1101,6 +1286,37 @@ EncodeTiledFn get_encode_fn(std::string* why) {
   return fn;
 }
 
+// FP8 caches: K as rows of D bytes (box 16 rows, 128-byte swizzle); V tiles
+// are contiguous, read as 16 rows of D bytes without swizzle (ldmatrix reads
+// its 16-byte dimension rows conflict-free).
+bool encode_fp8_maps(CUtensorMap* mk, CUtensorMap* mv, const void* kbase, const void* vbase,
+                     int64_t num_blocks, int hkv, int D, std::string* why) {
+  EncodeTiledFn fn = get_encode_fn(why);
+  if (!fn) return false;
+  const cuuint32_t estr[2] = {1, 1};
+  cuuint64_t kd[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_blocks) * hkv * kBlock};
+  cuuint64_t ks[1] = {static_cast<cuuint64_t>(D)};
+  cuuint32_t kb[2] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(kBlock)};
+  CUresult r = fn(mk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kbase), kd, ks, kb, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r == CUDA_SUCCESS) {
+    // A V tile (D dims x 16 bytes) is one contiguous run of 16 * D bytes; it is
+    // described as 16 rows of D bytes so TMA moves it in 16 long requests.
+    cuuint64_t vd[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(num_blocks) * hkv * kBlock};
+    cuuint64_t vs[1] = {static_cast<cuuint64_t>(D)};
+    cuuint32_t vb[2] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(kBlock)};
+    r = fn(mv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(vbase), vd, vs, vb, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled (FP8) failed with CUresult " + std::to_string(static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
 bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D,
                       std::string* why) {
   EncodeTiledFn fn = get_encode_fn(why);
@@ -1125,11 +1341,11 @@ struct LaunchShape {
   size_t smem;
 };
 
-template <typename T, int D, int NC, int S, bool kFma, int HPG>
+template <typename T, int D, int NC, int S, bool kFma, int HPG, bool kFp8 = false>
 bool launch_attend(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& P,
                    int64_t max_items, cudaStream_t stream, std::string* why) {
-  using Cfg = AttendCfg<T, D, NC, S, kFma>;
-  auto kern = attend_kernel<T, D, NC, S, kFma, HPG>;
+  using Cfg = AttendCfg<T, D, NC, S, kFma, kFp8>;
+  auto kern = attend_kernel<T, D, NC, S, kFma, HPG, kFp8>;
   static int occ_cache[64] = {0};  // per device ordinal
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1264,10 +1480,16 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   P.G = a.num_q_heads / a.num_kv_heads;
   P.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
 
+  P.k_scale = a.k_scale;
+  P.v_scale = a.v_scale;
   CUtensorMap tk, tv;
-  if (!encode_cache_map(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why) ||
-      !encode_cache_map(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why))
+  if (a.fp8) {
+    if (!encode_fp8_maps(&tk, &tv, a.k_cache, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why))
+      return 5;
+  } else if (!encode_cache_map(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why) ||
+             !encode_cache_map(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why)) {
     return 5;
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const int row_uint4 = a.num_q_heads * a.head_dim * 2 / 16;
@@ -1303,7 +1525,11 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   const int64_t max_items = L.max_parts * a.num_kv_heads;
   const int variant = a.variant == 0 ? 2 : a.variant;
   bool ok;
-  if (a.dtype == 1) {
+  if (a.fp8) {  // head_dim 128 only; 8 stages of 4 KB let three CTAs share an SM
+    ok = a.dtype == 1
+             ? launch_attend<__nv_bfloat16, 128, 4, 8, false, 1, true>(tk, tv, P, max_items, s, why)
+             : launch_attend<__half, 128, 4, 8, false, 1, true>(tk, tv, P, max_items, s, why);
+  } else if (a.dtype == 1) {
     ok = a.head_dim == 128
              ? dispatch_attend<__nv_bfloat16, 128>(variant, P.G, tk, tv, P, max_items, s, why)
              : dispatch_attend<__nv_bfloat16, 64>(variant, P.G, tk, tv, P, max_items, s, why);

@@ -225,6 +225,21 @@ struct Mma<__half> {
   }
 };
 
+// Two E4M3 bytes (low byte -> low half) -> two fp16, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t x) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(x));
+  return d;
+}
+
+// Two fp32 -> two E4M3 bytes (lo -> low byte), round to nearest even,
+// saturated to +-448.
+__device__ __forceinline__ uint16_t float2_to_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 // Two fp32 -> one packed pair of 16-bit values (lo in the low half), RNE.
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi);

@@ -35,6 +35,9 @@ struct DecodeArgs {
   const int32_t* group_off = nullptr;     // grouped decode: [num_groups + 1] (device)
   const int32_t* group_prefix = nullptr;  // [num_groups] shared prefix tokens (device)
   int32_t num_groups = 0;
+  bool fp8 = false;                       // E4M3 caches (K token-major, V dim-major)
+  const float* k_scale = nullptr;         // [num_kv_heads] (device), FP8 only
+  const float* v_scale = nullptr;
 };
 
 // Both return 0 on success or a pa_status code, with *why set on failure.
@@ -45,6 +48,11 @@ size_t decode_workspace_bytes(int64_t num_seqs, int64_t num_q_heads, int64_t hea
 int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
                        int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
                        int64_t num_blocks, void* stream, std::string* why);
+
+int cache_write_fp8_launch(const void* k, const void* v, const int64_t* slot_mapping,
+                           int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
+                           const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,
+                           int64_t num_blocks, int32_t dtype, void* stream, std::string* why);
 
 int copy_blocks_launch(void* k_cache, void* v_cache, int64_t num_blocks, int32_t num_kv_heads,
                        int32_t head_dim, const int32_t* src, const int32_t* dst, int32_t n_pairs,
