@@ -81,6 +81,9 @@ class OracleLib:
         lib.oracle_decode_fp8.argtypes = [P, P, P, P, P, ctypes.c_int, P, i32, P, i32, i32, i32, i32,
                                           i32, ctypes.c_double, P, ctypes.c_int]
         lib.oracle_decode_fp8.restype = ctypes.c_int
+        lib.oracle_prefill.argtypes = [P, P, P, ctypes.c_int, P, i32, P, P, i32, P, i64, i32, i32,
+                                       i32, i32, ctypes.c_double, P, ctypes.c_int]
+        lib.oracle_prefill.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = ctypes.c_int
         self.lib = lib
@@ -247,4 +250,40 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, dtype, block_size
                                Hkv, D, block_size, float(scale), _ptr(out), int(threads))
     if rc != 0:
         raise MemoryError("oracle_decode could not allocate its gather buffers")
+    return out
+
+
+def prefill(q, k_cache, v_cache, block_tables, seq_lens, q_offsets, scale, dtype, rows=None,
+            block_size=16, threads=0, handle=None):
+    """fp64 causal attention of every query token of each sequence's piece
+    (chunked prefill) over the sequence's paged K/V.
+
+    q [Tq, Hq, D] uint16 patterns, the pieces back to back; q_offsets
+    [B + 1] int32 with q_offsets[-1] = Tq; seq_lens [B] int32 counts the
+    piece's tokens (already in the cache).  ``rows``: query token indices to
+    compute (default all).  Returns out [len(rows), Hq, D] float64.
+    """
+    q = _c(q, np.uint16)
+    k_cache, v_cache = _c(k_cache, np.uint16), _c(v_cache, np.uint16)
+    block_tables, seq_lens = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    q_offsets = _c(q_offsets, np.int32)
+    Tq, Hq, D = q.shape
+    nb, Hkv, bs, D2 = k_cache.shape
+    B = seq_lens.shape[0]
+    assert D2 == D and bs == block_size and v_cache.shape == k_cache.shape
+    assert Hq % Hkv == 0 and block_tables.shape[0] == B and q_offsets.shape == (B + 1,)
+    assert q_offsets[-1] == Tq
+    rows_c = None if rows is None else _c(rows, np.int64)
+    n = Tq if rows is None else rows_c.shape[0]
+    out = np.empty((n, Hq, D), np.float64)
+    rc = _load(handle).oracle_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), DTYPE_CODES[dtype],
+                                      _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                      _ptr(q_offsets), B, None if rows_c is None else _ptr(rows_c),
+                                      n, Hq, Hkv, D, block_size, float(scale), _ptr(out),
+                                      int(threads))
+    if rc == -2:
+        raise ValueError("oracle_prefill: a piece is longer than its sequence, q_offsets is "
+                         "not non-decreasing from 0, or a row is out of range")
+    if rc != 0:
+        raise MemoryError("oracle_prefill could not allocate its gather buffers")
     return out

@@ -25,6 +25,9 @@
  *   - Copy-on-write: a shared block is copied to a fresh block before one of
  *     its holders writes into it.  "vLLM ve Triton", section 03.
  *
+ *   - Chunked prefill: several query tokens of one sequence (the last piece
+ *     of its prompt) attend causally over its paged K/V; see oracle_prefill.
+ *
  *   - Attention: the maths of scaled dot-product attention is unchanged by
  *     paging, only where K and V are read from changes:
  *       out = softmax(q K^T / sqrt(d_k)) V  over the sequence's tokens.
@@ -423,6 +426,108 @@ int oracle_decode_fp8(const uint16_t* q, const uint8_t* k_cache, const uint8_t* 
         }
         free(K); free(V); free(sc); free(qd);
     }
+    return failed ? -1 : 0;
+}
+
+/* ---- multi-query (chunked prefill) attention ---- */
+
+/*
+ * Chunked prefill: a long prompt is not processed in one iteration but cut
+ * into pieces that fit the step's token budget; each iteration computes one
+ * piece together with the running sequences' single decode tokens, and the
+ * piece's K/V fill the sequence's blocks over several steps.
+ *   "Yerel LLM sistemlerinde backpressure ve olcekleme", section
+ *   "4. Prefill ve decode" (the chunked prefill paragraph and diagram);
+ *   "vLLM Nedir? PagedAttention ile Production LLM Serving", section
+ *   "Chunked prefill".
+ * Our reading of what one iteration's attention computes: sequence b holds
+ * seq_lens[b] tokens in its blocks after the piece's K/V were written; its
+ * piece is the last Qn = q_offsets[b+1] - q_offsets[b] of them (a decode
+ * token is a piece of one), so query j of the piece sits at position
+ * p = seq_lens[b] - Qn + j and attends causally to tokens 0 .. p.
+ *
+ * q:          [num_q_tokens][num_q_heads][head_dim] 16-bit patterns, the
+ *             pieces of all sequences back to back (q_offsets[num_seqs] =
+ *             num_q_tokens)
+ * rows:       the query tokens to compute (indices into q), or NULL for all
+ * out:        [n_rows][num_q_heads][head_dim] fp64
+ * Returns 0; -1 if scratch memory could not be allocated; -2 if a piece is
+ * longer than its sequence or q_offsets is not non-decreasing from 0.
+ */
+int oracle_prefill(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, int dtype,
+                   const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                   const int32_t* q_offsets, int32_t num_seqs, const int64_t* rows, int64_t n_rows,
+                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                   double scale, double* out, int num_threads) {
+    const int32_t G = num_q_heads / num_kv_heads;
+    const int64_t num_q_tokens = q_offsets[num_seqs];
+    if (q_offsets[0] != 0) return -2;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int32_t piece = q_offsets[b + 1] - q_offsets[b];
+        if (piece < 0 || piece > seq_lens[b]) return -2;
+    }
+    if (!rows) n_rows = num_q_tokens;
+    int failed = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#else
+    (void)num_threads;
+#endif
+    int64_t n_tasks = n_rows * num_kv_heads;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+    for (int64_t task = 0; task < n_tasks; ++task) {
+        int64_t r = task / num_kv_heads;
+        int32_t h = (int32_t)(task % num_kv_heads);
+        int64_t tok = rows ? rows[r] : r;
+        if (tok < 0 || tok >= num_q_tokens) {
+            failed |= 2;
+            continue;
+        }
+        /* the sequence whose piece holds query token tok */
+        int32_t b = 0;
+        while (q_offsets[b + 1] <= tok) ++b;
+        int32_t piece_len = q_offsets[b + 1] - q_offsets[b];
+        int32_t j = (int32_t)(tok - q_offsets[b]);
+        int32_t pos = seq_lens[b] - piece_len + j;
+        int32_t n_visible = pos + 1; /* causal: tokens 0 .. pos */
+        double* K = (double*)malloc(sizeof(double) * (size_t)n_visible * head_dim);
+        double* V = (double*)malloc(sizeof(double) * (size_t)n_visible * head_dim);
+        double* sc = (double*)malloc(sizeof(double) * (size_t)n_visible);
+        double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        if (!K || !V || !sc || !qd) {
+            free(K); free(V); free(sc); free(qd);
+            failed |= 1;
+            continue;
+        }
+        const int32_t* trow = block_tables + (int64_t)b * max_blocks;
+        oracle_gather(k_cache, dtype, trow, n_visible, num_kv_heads, h, head_dim, block_size, K);
+        oracle_gather(v_cache, dtype, trow, n_visible, num_kv_heads, h, head_dim, block_size, V);
+        for (int32_t g = 0; g < G; ++g) {
+            int32_t head = h * G + g; /* query head reads KV head head / G */
+            const uint16_t* qrow = q + (tok * num_q_heads + head) * (int64_t)head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) qd[d] = to_double(qrow[d], dtype);
+            double smax = -INFINITY;
+            for (int32_t t = 0; t < n_visible; ++t) {
+                double acc = 0.0;
+                for (int32_t d = 0; d < head_dim; ++d) acc += qd[d] * K[(int64_t)t * head_dim + d];
+                sc[t] = scale * acc;
+                if (sc[t] > smax) smax = sc[t];
+            }
+            double denom = 0.0;
+            for (int32_t t = 0; t < n_visible; ++t) {
+                sc[t] = exp(sc[t] - smax);
+                denom += sc[t];
+            }
+            double* o = out + (r * num_q_heads + head) * (int64_t)head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                double acc = 0.0;
+                for (int32_t t = 0; t < n_visible; ++t) acc += sc[t] * V[(int64_t)t * head_dim + d];
+                o[d] = acc / denom;
+            }
+        }
+        free(K); free(V); free(sc); free(qd);
+    }
+    if (failed & 2) return -2;
     return failed ? -1 : 0;
 }
 

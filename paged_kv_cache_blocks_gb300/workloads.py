@@ -22,6 +22,10 @@ long           32 q / 8 KV heads, head_dim 128, bf16, 8 sequences of
 fullstep       32 layers of the 8B shape, 128 sequences in 4 groups of 32;
                each group shares a 1024-token prefix (64 full blocks);
                lengths 1024+U{256..7168}
+chunked        (make_prefill_batch) Llama-3-70B-shaped layer: a
+               30000-token document prompt prefilled in 8 pieces of
+               3750 tokens, each iteration together with one decode
+               token of 20 running chats of 300+U{1..100} tokens
 =============  =======================================================
 
 Pools hold the needed blocks plus 25% (the tiny one holds 24 blocks); the
@@ -79,9 +83,17 @@ WORKLOADS = {
     "fullstep": Workload("fullstep", 128, 32, 8, 128, "bf16", 32, 1.0 / math.sqrt(128),
                          "32 layers of the 8B shape, 128 seqs in 4 groups of 32 sharing a "
                          "1024-token prefix, lens 1024+U{256..7168}"),
+    "chunked": Workload("chunked", 21, 64, 8, 128, "bf16", 1, 1.0 / math.sqrt(128),
+                        "Llama-3-70B-shaped layer, chunked prefill: a 30000-token prompt in 8 "
+                        "pieces of 3750 tokens, each with the decode tokens of 20 chats of "
+                        "300+U{1..100} tokens"),
 }
+CHUNK_DOC_TOKENS = 30000
+CHUNK_PIECES = 8
+CHUNK_CHATS = 20
 
-_SEED_SALT = {"tiny": 11, "llama8b": 22, "llama70b": 33, "long": 44, "fullstep": 55}
+_SEED_SALT = {"tiny": 11, "llama8b": 22, "llama70b": 33, "long": 44, "fullstep": 55,
+              "chunked": 66}
 PREFIX_TOKENS = 1024
 PREFIX_GROUPS = 4
 
@@ -351,3 +363,136 @@ def relabel_blocks(batch, seed):
         n = Layer(Lr.q, Lr.k_cache[ix], Lr.v_cache[ix], Lr.new_k, Lr.new_v, Lr.k_past, Lr.v_past)
         new.layers.append(n)
     return new
+
+
+# ----------------------------------------------------------------------------------
+# Multi-query batches (chunked prefill)
+
+@dataclass
+class PrefillBatch:
+    workload: Workload
+    seq_lens: np.ndarray         # int32 [B], the piece's tokens included
+    pieces: np.ndarray           # int32 [B], query tokens of each sequence (>= 1)
+    q_offsets: np.ndarray        # int32 [B + 1], pieces back to back
+    block_tables: np.ndarray     # int32 [B, max_blocks], padded with poison_block
+    num_blocks: int
+    poison_block: int
+    slot_mapping: np.ndarray     # int64 [Tq], slots of the pieces' tokens
+    q: torch.Tensor              # int16 [Tq, Hq, D] bit patterns
+    k_cache: torch.Tensor        # int16 [NB, Hkv, 16, D], the L - piece past tokens placed
+    v_cache: torch.Tensor
+    new_k: torch.Tensor          # int16 [Tq, Hkv, D], the pieces' keys and values
+    new_v: torch.Tensor
+    k_past: torch.Tensor = None  # int16 [rows, Hkv, D] contiguous past draw (keep_contig)
+    v_past: torch.Tensor = None
+    past_start: np.ndarray = None  # int64 [B], first row of each sequence's past draw
+
+    @property
+    def num_q_tokens(self):
+        return int(self.q_offsets[-1])
+
+    def contiguous_kv(self, b):
+        """Contiguous [L_b, Hkv, D] uint16 K and V of sequence b (keep_contig)."""
+        n_past = int(self.seq_lens[b] - self.pieces[b])
+        s0, q0, q1 = int(self.past_start[b]), int(self.q_offsets[b]), int(self.q_offsets[b + 1])
+        f = lambda a, n: torch.cat([a[s0:s0 + n_past], n[q0:q1]]).numpy().view(np.uint16)
+        return f(self.k_past, self.new_k), f(self.v_past, self.new_v)
+
+    def placed_pools(self):
+        """Pool copies with the pieces' tokens placed at their slots (layout
+        only; the inputs of an attention call that follows the cache write)."""
+        kc, vc = self.k_cache.clone(), self.v_cache.clone()
+        s = torch.from_numpy(self.slot_mapping).to(kc.device)
+        kc[s // BLOCK_SIZE, :, s % BLOCK_SIZE, :] = self.new_k
+        vc[s // BLOCK_SIZE, :, s % BLOCK_SIZE, :] = self.new_v
+        return kc, vc
+
+
+def chunked_iteration_shape(iteration, seed=0):
+    """(lens, pieces) of iteration k (1..8) of the chunked workload: the
+    document (sequence 0) holds k pieces of 3750 tokens, the last of them
+    its query; each chat holds its drawn length + k tokens, one query."""
+    if not 1 <= iteration <= CHUNK_PIECES:
+        raise ValueError("iteration must be in 1..8")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed) * 1000 + _SEED_SALT["chunked"])
+    chats = 300 + torch.randint(1, 101, (CHUNK_CHATS,), generator=g).numpy()
+    piece = CHUNK_DOC_TOKENS // CHUNK_PIECES
+    lens = np.concatenate([[piece * iteration], chats + iteration]).astype(np.int32)
+    pieces = np.concatenate([[piece], np.ones(CHUNK_CHATS, np.int64)]).astype(np.int32)
+    return lens, pieces
+
+
+def make_prefill_batch(name, seed=0, iteration=CHUNK_PIECES, poison=True, keep_contig=False,
+                       device="cpu", lens=None, pieces=None):
+    """One multi-query batch: sequence b holds lens[b] tokens once its piece
+    of pieces[b] query tokens is written; the lens[b] - pieces[b] earlier
+    tokens are already in the pool.  Defaults: the chunked workload at
+    ``iteration``; ``lens``/``pieces`` override the shape (any workload's
+    head layout).  Draw order: permutation, q, contiguous past K, past V,
+    the pieces' k, v."""
+    w = WORKLOADS[name]
+    if lens is None:
+        if name != "chunked":
+            raise ValueError("lens/pieces are required for workloads other than chunked")
+        lens, pieces = chunked_iteration_shape(iteration, seed)
+    lens = np.asarray(lens, np.int64)
+    pieces = np.asarray(pieces, np.int64)
+    if lens.shape != pieces.shape or (pieces < 1).any() or (pieces > lens).any():
+        raise ValueError("every piece must hold 1..len tokens")
+    gseed = int(seed) * 1000 + _SEED_SALT[name] + 500 + int(iteration)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(gseed)
+    B = lens.shape[0]
+    nblk = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
+    n_unique = int(nblk.sum())
+    pool = max(int(math.ceil(1.25 * n_unique)), n_unique + 1)
+    perm = torch.randperm(pool, generator=g).numpy().astype(np.int32)
+    poison_block = int(perm[n_unique])
+    tables = np.full((B, max(1, int(nblk.max()))), poison_block, np.int32)
+    first = np.concatenate([[0], np.cumsum(nblk)])
+    for b in range(B):
+        tables[b, :nblk[b]] = perm[first[b]:first[b + 1]]
+    q_off = np.concatenate([[0], np.cumsum(pieces)]).astype(np.int32)
+    Tq = int(q_off[-1])
+    # slots: the past tokens (pool placement) and the pieces' tokens (written by the step)
+    past_blk, past_off, new_slot = [], [], []
+    past_start = np.zeros(B, np.int64)
+    rows = 0
+    for b in range(B):
+        n_past = int(lens[b] - pieces[b])
+        t = np.arange(n_past, dtype=np.int64)
+        past_blk.append(tables[b, t // BLOCK_SIZE].astype(np.int64))
+        past_off.append(t % BLOCK_SIZE)
+        past_start[b] = rows
+        rows += n_past
+        t = np.arange(n_past, int(lens[b]), dtype=np.int64)
+        new_slot.append(tables[b, t // BLOCK_SIZE].astype(np.int64) * BLOCK_SIZE + t % BLOCK_SIZE)
+    past_blk = np.concatenate(past_blk)
+    past_off = np.concatenate(past_off)
+    slots = np.concatenate(new_slot)
+
+    H, Hq, D = w.num_kv_heads, w.num_q_heads, w.head_dim
+    dev = torch.device(device)
+    gv = g
+    if dev.type == "cuda":
+        gv = torch.Generator(device=dev)
+        gv.manual_seed(gseed + 7)
+    fill = _NAN_BITS[w.dtype] if poison else 0
+    fill_i16 = fill - 65536 if fill >= 32768 else fill
+    q = _bits(torch.randn((Tq, Hq, D), generator=gv, device=dev), w.dtype)
+    k_past = _bits(torch.randn((rows, H, D), generator=gv, device=dev), w.dtype)
+    v_past = _bits(torch.randn((rows, H, D), generator=gv, device=dev), w.dtype)
+    new_k = _bits(torch.randn((Tq, H, D), generator=gv, device=dev), w.dtype)
+    new_v = _bits(torch.randn((Tq, H, D), generator=gv, device=dev), w.dtype)
+    kc = torch.full((pool, H, BLOCK_SIZE, D), fill_i16, dtype=torch.int16, device=dev)
+    vc = torch.full((pool, H, BLOCK_SIZE, D), fill_i16, dtype=torch.int16, device=dev)
+    if rows:
+        tb, to = torch.from_numpy(past_blk).to(dev), torch.from_numpy(past_off).to(dev)
+        kc[tb, :, to, :] = k_past
+        vc[tb, :, to, :] = v_past
+    pb = PrefillBatch(w, lens.astype(np.int32), pieces.astype(np.int32), q_off, tables, pool,
+                      poison_block, slots, q, kc, vc, new_k, new_v)
+    if keep_contig:
+        pb.k_past, pb.v_past, pb.past_start = k_past, v_past, past_start
+    return pb

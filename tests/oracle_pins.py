@@ -10,7 +10,8 @@ the mathematics fix:
   heads repeated for grouped-query attention);
 * closed forms (one token, constant values, identical keys, one dominant key);
 * invariants (the gather returns the contiguous source exactly; relabelling
-  the physical blocks leaves the output bit-identical).
+  the physical blocks leaves the output bit-identical; a query never sees a
+  token after its own position).
 
 test_oracle.py runs every pin on the oracle; test_oracle_mutants.py plants
 mistakes in copies of the oracle's source and checks that some pin fails.
@@ -296,7 +297,132 @@ def pin_closed_forms(oracle, handle=None):
     assert np.array_equal(o, np.zeros_like(o))
 
 
+# ---- multi-query (chunked prefill) attention -------------------------------------
+
+def prefill_batches():
+    """Multi-query batches with pieces in the middle of a prompt, whole
+    prompts, single decode tokens, and pieces crossing block boundaries."""
+    return [
+        W.make_prefill_batch("tiny", seed=0, keep_contig=True, lens=[1, 17, 33, 100],
+                             pieces=[1, 17, 9, 40]),
+        W.make_prefill_batch("llama8b", seed=1, keep_contig=True, lens=[37, 300, 50, 16, 129],
+                             pieces=[37, 1, 16, 3, 64]),
+        W.make_prefill_batch("llama70b", seed=2, keep_contig=True, lens=[70, 5, 33],
+                             pieces=[20, 5, 1]),
+    ]
+
+
+def sdpa_prefill_reference(pb, whole_prompt_causal=False):
+    """Per-sequence attention by the library routine, fp64, GQA by repeat;
+    query j of a piece of Qn tokens over L sees tokens t <= L - Qn + j (an
+    explicit boolean mask, or is_causal=True when the piece is the whole
+    prompt and ``whole_prompt_causal``)."""
+    w = pb.workload
+    G = w.group_size
+    q = lib_f64(pb.q.numpy().view(np.uint16), w.dtype)
+    out = np.zeros((pb.num_q_tokens, w.num_q_heads, w.head_dim))
+    for b, L in enumerate(pb.seq_lens):
+        L = int(L)
+        n = int(pb.pieces[b])
+        kb, vb = pb.contiguous_kv(b)
+        K = torch.from_numpy(lib_f64(kb, w.dtype)).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        V = torch.from_numpy(lib_f64(vb, w.dtype)).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        q0 = int(pb.q_offsets[b])
+        qb = torch.from_numpy(q[q0:q0 + n]).permute(1, 0, 2)            # [Hq, n, D]
+        if whole_prompt_causal and n == L:
+            o = F.scaled_dot_product_attention(qb, K, V, is_causal=True, scale=w.scale)
+        else:
+            mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+            o = F.scaled_dot_product_attention(qb, K, V, attn_mask=mask, scale=w.scale)
+        out[q0:q0 + n] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+def _prefill(oracle, pb, handle, rows=None, pools=None):
+    w = pb.workload
+    kc, vc = pb.placed_pools() if pools is None else pools
+    return oracle.prefill(pb.q.numpy().view(np.uint16), kc.numpy().view(np.uint16),
+                          vc.numpy().view(np.uint16), pb.block_tables, pb.seq_lens, pb.q_offsets,
+                          w.scale, w.dtype, rows=rows, handle=handle)
+
+
+def pin_prefill_matches_sdpa(oracle, handle=None):
+    for pb in prefill_batches():
+        got = _prefill(oracle, pb, handle)
+        for causal in (False, True):
+            err = np.max(np.abs(got - sdpa_prefill_reference(pb, causal)))
+            assert err <= 1e-12, (pb.workload.name, causal, err)
+
+
+def pin_prefill_causal_and_rows(oracle, handle=None):
+    """A query never sees a later token: changing the K/V of a sequence's
+    last token changes only that token's own query row.  Computing a subset
+    of rows gives those rows bit-identically.  A piece of one token is the
+    decode of that token (an independent SDPA pin holds the decode)."""
+    pb = prefill_batches()[1]
+    kc, vc = pb.placed_pools()
+    full = _prefill(oracle, pb, handle, pools=(kc, vc))
+    b = 4                                   # 129 tokens, piece of 64 (positions 65..128)
+    last = int(pb.seq_lens[b]) - 1
+    s = int(pb.block_tables[b, last // 16]) * 16 + last % 16
+    kc2, vc2 = kc.clone(), vc.clone()
+    kc2[s // 16, :, s % 16, :] = pb.new_k[0]          # some other key
+    vc2[s // 16, :, s % 16, :] = -vc2[s // 16, :, s % 16, :]
+    mod = _prefill(oracle, pb, handle, pools=(kc2, vc2))
+    q1 = int(pb.q_offsets[b + 1])
+    same = np.ones(pb.num_q_tokens, bool)
+    same[q1 - 1] = False
+    assert np.array_equal(full[same], mod[same]), "a query saw a later token"
+    assert not np.allclose(full[q1 - 1], mod[q1 - 1]), "the last query missed its own token"
+    rows = np.array([q1 - 1, 0, 37, 38, 53, q1 - 64], np.int64)
+    assert np.array_equal(_prefill(oracle, pb, handle, rows=rows), full[rows])
+    # pieces of one token: the decode of each sequence's last token
+    lens = np.array([5, 16, 200], np.int32)
+    one = W.make_prefill_batch("llama8b", seed=4, lens=lens, pieces=[1, 1, 1])
+    okc, ovc = one.placed_pools()
+    dec = oracle.decode(one.q.numpy().view(np.uint16), okc.numpy().view(np.uint16),
+                        ovc.numpy().view(np.uint16), one.block_tables, lens,
+                        one.workload.scale, one.workload.dtype, handle=handle)
+    assert np.array_equal(_prefill(oracle, one, handle), dec)
+
+
+def pin_prefill_closed_forms(oracle, handle=None):
+    """The first token of a prompt sees only itself: out = its v.  Constant
+    values give that constant for every query of every piece."""
+    pb = prefill_batches()[0]                          # tiny: fp16, d 64, G 2
+    w = pb.workload
+    got = _prefill(oracle, pb, handle)
+    for b in range(len(pb.seq_lens)):
+        if pb.pieces[b] == pb.seq_lens[b]:             # a whole prompt: row 0 is position 0
+            q0 = int(pb.q_offsets[b])
+            _, vb = pb.contiguous_kv(b)
+            v0 = lib_f64(vb[0], w.dtype)               # [Hkv, D]
+            for i in range(w.num_q_heads):
+                assert np.array_equal(got[q0, i], v0[i // w.group_size]), ("position 0", b, i)
+    kc, vc = pb.placed_pools()
+    vc = torch.full_like(vc, int(np.float16(-1.25).view(np.int16)))
+    got = _prefill(oracle, pb, handle, pools=(kc, vc))
+    assert np.allclose(got, -1.25, rtol=0, atol=1e-14), "constant V"
+
+
+def pin_prefill_relabel_invariance(oracle, handle=None):
+    pb = prefill_batches()[1]
+    a = _prefill(oracle, pb, handle)
+    kc, vc = pb.placed_pools()
+    rng = np.random.default_rng(9)
+    perm = rng.permutation(pb.num_blocks)                # old id -> new id
+    inv = np.argsort(perm)
+    kc2, vc2 = kc[torch.from_numpy(inv)], vc[torch.from_numpy(inv)]
+    pb2 = W.PrefillBatch(**{**pb.__dict__, "block_tables": perm[pb.block_tables].astype(np.int32)})
+    b = oracle.prefill(pb.q.numpy().view(np.uint16), kc2.numpy().view(np.uint16),
+                       vc2.numpy().view(np.uint16), pb2.block_tables, pb.seq_lens, pb.q_offsets,
+                       pb.workload.scale, pb.workload.dtype, handle=handle)
+    assert np.array_equal(a, b)
+
+
 ALL_PINS = [pin_kv_bytes, pin_bits, pin_cache_write_golden, pin_copy_blocks_golden,
             pin_e4m3_codes, pin_cache_write_fp8_golden, pin_decode_fp8_reduces_to_decode,
             pin_gather_is_contiguous_source,
-            pin_matches_sdpa, pin_relabel_invariance, pin_closed_forms]
+            pin_matches_sdpa, pin_relabel_invariance, pin_closed_forms,
+            pin_prefill_matches_sdpa, pin_prefill_causal_and_rows, pin_prefill_closed_forms,
+            pin_prefill_relabel_invariance]

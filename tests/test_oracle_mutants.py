@@ -35,6 +35,14 @@ MUTANTS = {
     "fp8_scale_not_applied": ("(double)k_scale[h];\n                V[", "1.0;\n                V["),
     "copy_v_from_k": ("v_cache[dst[i] * per_block + e] = v_cache[src[i] * per_block + e];",
                       "v_cache[dst[i] * per_block + e] = k_cache[src[i] * per_block + e];"),
+    "prefill_diagonal_dropped": ("int32_t n_visible = pos + 1;", "int32_t n_visible = pos + 1 - (pos > 0);"),
+    "prefill_position_base": ("int32_t pos = seq_lens[b] - piece_len + j;", "int32_t pos = j;"),
+    "prefill_gqa_mapping": ("int32_t head = h * G + g;", "int32_t head = g * num_kv_heads + h;"),
+    "prefill_rows_ignored": ("int64_t tok = rows ? rows[r] : r;", "int64_t tok = r;"),
+    "prefill_query_row": ("q + (tok * num_q_heads + head) * (int64_t)head_dim;",
+                          "q + ((int64_t)j * num_q_heads + head) * (int64_t)head_dim;"),
+    "prefill_v_head": ("oracle_gather(v_cache, dtype, trow, n_visible, num_kv_heads, h,",
+                       "oracle_gather(v_cache, dtype, trow, n_visible, num_kv_heads, 0,"),
     "copy_direction": ("k_cache[dst[i] * per_block + e] = k_cache[src[i] * per_block + e];",
                        "k_cache[src[i] * per_block + e] = k_cache[dst[i] * per_block + e];"),
 }
