@@ -50,6 +50,11 @@ DESCR = {
     "fullstep": "full decode step: 32 layers of the Llama-3-8B shape, 128 seqs in 4 groups of 32 "
                 "sharing a 1024-token prefix (ref-counted blocks), lens 1024+U{256..7168}, bf16",
 }
+DESCR["chunked"] = ("chunked prefill, Llama-3-70B-shaped layer (64 q / 8 kv heads, head_dim 128, "
+                    "bf16): a 30000-token prompt prefilled in 8 pieces of 3750 tokens, each "
+                    "iteration with the decode tokens of 20 chats of 300+U{1..100} tokens; one step "
+                    "= the 8 iterations (pa_cache_write of the pieces + pa_prefill)")
+PREFILL_METRIC = "paged chunked-prefill attention TFLOP/s (causal, dense-equivalent 4*q*k*d per head)"
 VARIANTS = {"auto": 0, "fma": 1, "mma": 2}
 
 
@@ -230,6 +235,206 @@ def cpu_baseline(workload, budget_s=12.0):
                       f"({int((np.asarray(lens) > 10 * np.median(lens_all)).sum())} long, same "
                       f"length draw), {int(np.sum(lens))} tokens, one decode step, fp64, "
                       f"{threads} OpenMP threads; excludes input generation"}
+
+
+def prefill_flops(lens, pieces, hq, d):
+    """Causal attention FLOPs of a multi-query batch: 2 (QK) + 2 (PV) per
+    (query token, visible key, head, dim)."""
+    total = 0
+    for L, n in zip(np.asarray(lens, np.int64), np.asarray(pieces, np.int64)):
+        # query j sees L - n + j + 1 keys
+        total += int(n * (L - n) + n * (n + 1) // 2)
+    return 4 * total * hq * d
+
+
+def prefill_cpu_baseline(threads=None, n_rows=None, seed=0, budget_s=12.0):
+    """The fp64 oracle on query rows spread over the last iteration's prompt
+    piece (the most expensive rows), scaled to FLOP/s; ``n_rows=None`` sizes
+    the sample to about ``budget_s`` seconds from an 8-row probe."""
+    if n_rows is None:
+        v, sec, cores, _ = prefill_cpu_baseline(threads, 8, seed)
+        n_rows = int(max(8, min(3750, round(8 * budget_s / max(sec, 1e-3)))))
+    import oracle
+    oracle.build()
+    from paged_kv_cache_blocks_gb300 import workloads as W
+    threads = threads or len(os.sched_getaffinity(0))
+    pb = W.make_prefill_batch("chunked", seed=seed, iteration=W.CHUNK_PIECES, poison=False)
+    w = pb.workload
+    kc, vc = pb.placed_pools()
+    n = int(pb.pieces[0])
+    rows = np.linspace(0, n - 1, n_rows).astype(np.int64)
+    q = pb.q.numpy().view(np.uint16)
+    kcn, vcn = kc.numpy().view(np.uint16), vc.numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.prefill(q, kcn, vcn, pb.block_tables, pb.seq_lens, pb.q_offsets, w.scale, w.dtype,
+                   rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    base = int(pb.seq_lens[0]) - n
+    fl = sum(4 * (base + int(r) + 1) * w.num_q_heads * w.head_dim for r in rows)
+    return fl / dt / 1e12, dt, threads, (f"{n_rows} query tokens of the 8th piece of the "
+                                         f"30000-token prompt (positions {base + rows[0]}.."
+                                         f"{base + rows[-1]}, all 64 heads), fp64, "
+                                         f"{threads} OpenMP threads")
+
+
+def run_prefill(args, rank, world, local_rank):
+    """The chunked-prefill workload: one step = the 8 iterations of the
+    prompt, each pa_cache_write of the iteration's new tokens + pa_prefill."""
+    from paged_kv_cache_blocks_gb300 import build as pb_build
+    pb_build.build()
+    from paged_kv_cache_blocks_gb300 import binding as pa
+    from paged_kv_cache_blocks_gb300 import workloads as W
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    w = W.WORKLOADS["chunked"]
+    dt = torch.bfloat16
+    its = []
+    flops = 0
+    q_tokens = 0
+    for k in range(1, W.CHUNK_PIECES + 1):
+        b = W.make_prefill_batch("chunked", seed=rank, iteration=k, poison=False, device="cuda")
+        ws = torch.empty(pa.pa_prefill_workspace_bytes(len(b.seq_lens), b.num_q_tokens,
+                                                       w.num_q_heads, w.num_kv_heads),
+                         dtype=torch.uint8, device=dev)
+        its.append(dict(q=b.q.view(dt), kc=b.k_cache.view(dt), vc=b.v_cache.view(dt),
+                        nk=b.new_k.view(dt), nv=b.new_v.view(dt),
+                        slots=torch.from_numpy(b.slot_mapping).to(dev),
+                        tab=torch.from_numpy(b.block_tables).to(dev),
+                        lens=torch.from_numpy(b.seq_lens).to(dev),
+                        qoff=torch.from_numpy(b.q_offsets).to(dev), ws=ws,
+                        out=torch.empty_like(b.q.view(dt)), msl=int(b.seq_lens.max()), host=b))
+        flops += prefill_flops(b.seq_lens, b.pieces, w.num_q_heads, w.head_dim)
+        q_tokens += b.num_q_tokens
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        for i, it in enumerate(its):
+            pa.pa_cache_write(it["nk"], it["nv"], it["slots"], it["kc"], it["vc"])
+            pa.pa_prefill(it["q"], it["kc"], it["vc"], it["tab"], it["lens"], it["qoff"], w.scale,
+                          max_seq_len=it["msl"], out=it["out"], workspace=it["ws"],
+                          events=evs[i] if evs else None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for it in its:
+        bits = pa.pa_decode_check(it["ws"])
+        if bits:
+            raise RuntimeError(f"device error bits {bits} during warm-up")
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in its] for _ in range(args.steps)]
+    for row in ev:
+        for a, z in row:
+            a.record(stream)
+            z.record(stream)
+    sampler = ClockSampler(gpu_identity(local_rank)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(ev[i])
+    stop.record(stream)
+    barrier()
+    t_host1 = time.time()
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    ms_step = reduce_max(start.elapsed_time(stop) / args.steps, dist, dev)
+    kern_ms = sum(statistics.fmean(a.elapsed_time(z) for row in ev for a, z in [row[i]])
+                  for i in range(len(its)))
+    tflops = job_throughput(flops, world, ms_step * 1e-3) / 1e12
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(peaks.get("bf16_tflops_sustained", 1700.0))
+    peak_src = "measured bf16_tflops_sustained (cuBLAS bf16, seconds-long loop)" if peaks \
+        else "fallback 1.7 PFLOP/s sustained"
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_prefill_e2e(args, pa, its, w, dev, barrier, dist, world, flops)
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, sec, cores, sample = prefill_cpu_baseline()
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "seconds": sec,
+               "sample": sample}
+    line = {
+        "metric": PREFILL_METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": DESCR["chunked"], "iterations": len(its),
+                   "query_tokens_per_step": q_tokens, "flops_per_step": flops,
+                   "kv_tokens_last_iteration": int(its[-1]["host"].seq_lens.sum()),
+                   "l2": "K/V per iteration <= 155 MB, re-read by every 16-token query tile: "
+                         "compute-bound; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "query_tokens_per_s": job_throughput(q_tokens, world, ms_step * 1e-3),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "prefill_kernel",
+                     "kernel_ms": kern_ms, "algorithmic_flops": flops, "peak_source": peak_src},
+        "e2e": e2e,
+        "gpu_launches": 3 * len(its) * args.steps,
+        "clocks": sampler.summary(t_host0, t_host1) if sampler else None,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_prefill_e2e(args, pa, its, w, dev, barrier, dist, world, flops):
+    """The 8 iterations through the public API from pinned host buffers:
+    H2D of each iteration's q, new k/v, slots, table, lengths and offsets,
+    cache write, prefill, D2H of the output, then synchronise."""
+    steps = max(1, min(args.steps, max(1, args.e2e_steps // 20)))
+    host = []
+    for it in its:
+        h = {k: it[k].cpu().pin_memory() for k in ("q", "nk", "nv", "slots", "tab", "lens", "qoff")}
+        h["out"] = torch.empty_like(it["out"], device="cpu").pin_memory()
+        d = {k: torch.empty_like(it[k]) for k in ("q", "nk", "nv", "slots", "tab", "lens", "qoff")}
+        host.append((h, d))
+    nbytes = lambda t: t.numel() * t.element_size()
+    h2d = sum(nbytes(h[k]) for h, _ in host for k in ("q", "nk", "nv", "slots", "tab", "lens", "qoff"))
+    d2h = sum(nbytes(h["out"]) for h, _ in host)
+
+    def one():
+        for it, (h, d) in zip(its, host):
+            for k in d:
+                d[k].copy_(h[k], non_blocking=True)
+            pa.pa_cache_write(d["nk"], d["nv"], d["slots"], it["kc"], it["vc"])
+            pa.pa_prefill(d["q"], it["kc"], it["vc"], d["tab"], d["lens"], d["qoff"], w.scale,
+                          max_seq_len=it["msl"], out=it["out"], workspace=it["ws"])
+            h["out"].copy_(it["out"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(2):
+        one()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    barrier()
+    sec = reduce_max((time.perf_counter() - t0) / steps, dist, dev)
+    return {"value": job_throughput(flops, world, sec) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": sec * 1e3,
+            "path": "per iteration: H2D (pinned) q, new k/v, slots, table, lens, offsets -> "
+                    "pa_cache_write -> pa_prefill -> D2H out; sync at the end of the step"}
 
 
 def run_reference(args, rank, world):
@@ -612,6 +817,34 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped=F
                     + " -> D2H out, then sync"}
 
 
+def run_reference_prefill(args, rank, world):
+    """The oracle as the reference arm of the chunked workload: each step a
+    bounded sample of query rows, FLOP/s scaled from that sample."""
+    if rank != 0:
+        return 0
+    threads = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        prefill_cpu_baseline(threads, n_rows=1)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, sec, cores, sample = prefill_cpu_baseline(threads, n_rows=1)
+        vals.append(v)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    val = statistics.fmean(vals)
+    line = {"impl": "reference", "metric": PREFILL_METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": DESCR["chunked"], "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -636,7 +869,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
+        if args.workload == "chunked":
+            return run_reference_prefill(args, rank, world)
         return run_reference(args, rank, world)
+    if args.workload == "chunked":
+        return run_prefill(args, rank, world, local_rank)
     return run_pa(args, rank, world, local_rank)
 
 

@@ -295,9 +295,51 @@ int pa_decode_fp8(const void* d_q, const void* d_k_cache8, const void* d_v_cache
                   int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
                   size_t workspace_bytes, void* stream, const pa_decode_opts* opts);
 
-/* Waits for `stream`, then reads the device error bits the last decode
- * using this workspace left (PA_DEVERR_*; 0 = clean) into *error_bits.
- * Returns PA_ERR_DEVICE when any bit is set. */
+/* ------------------------------------------------------------------------
+ * Multi-query paged attention: chunked prefill with decode tokens in the
+ * same call.  "Yerel LLM sistemlerinde backpressure ve olcekleme", section
+ * "4. Prefill ve decode", and "vLLM Nedir? PagedAttention ile Production LLM
+ * Serving", section "Chunked prefill": a long prompt is cut into pieces that
+ * fit a step's token budget and each iteration computes one piece together
+ * with the running sequences' decode tokens; the piece's K/V fill the
+ * sequence's blocks over several steps.
+ *
+ * Sequence b holds seq_lens[b] tokens in its blocks after the piece's K/V
+ * were written (pa_cache_write); its piece is the last
+ * Q_b = q_offsets[b+1] - q_offsets[b] of them (a decode token is a piece of
+ * one).  Query j of the piece sits at position seq_lens[b] - Q_b + j and
+ * attends causally to tokens 0 .. seq_lens[b] - Q_b + j:
+ *   out[t, i] = softmax_j(scale * q[t, i] . K[j, i / G]) V[j, i / G].
+ *
+ *   d_q, d_out     [num_q_tokens][num_q_heads][head_dim] 16-bit, the pieces
+ *                  back to back (16-byte aligned)
+ *   d_q_offsets    [num_seqs + 1] int32, device: q_offsets[0] = 0,
+ *                  non-decreasing, q_offsets[num_seqs] = num_q_tokens
+ *   caches, d_block_tables, d_seq_lens, max_seq_len, scale, dtype: as for
+ *                  pa_decode (max_seq_len bounds every seq_lens[b])
+ *   d_workspace    >= pa_prefill_workspace_bytes(...) bytes, 256-byte
+ *                  aligned, caller-owned; calls sharing it must not overlap
+ *   opts           NULL, or events recorded around the attention kernel
+ *                  (variant must be 0 or 2)
+ *
+ * fp32 accumulation, one rounding to dtype.  Bad device data never faults: a
+ * length outside [0, max_seq_len], a piece longer than its sequence or
+ * offsets out of order are flagged (PA_DEVERR_SEQ_LEN) and clamped, block
+ * ids outside the pool read as zeros (PA_DEVERR_BLOCK_ID); the error bits
+ * are read with pa_decode_check on this workspace. */
+size_t pa_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
+                                  int32_t num_kv_heads);
+
+int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,
+               const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
+               const int32_t* d_q_offsets, int32_t num_seqs, int32_t num_q_tokens,
+               int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+               float scale, int32_t dtype, void* d_out, void* d_workspace, size_t workspace_bytes,
+               void* stream, const pa_decode_opts* opts);
+
+/* Waits for `stream`, then reads the device error bits the last decode (or
+ * prefill) using this workspace left (PA_DEVERR_*; 0 = clean) into
+ * *error_bits.  Returns PA_ERR_DEVICE when any bit is set. */
 int pa_decode_check(const void* d_workspace, void* stream, int32_t* error_bits);
 
 /* ------------------------------------------------------------------------

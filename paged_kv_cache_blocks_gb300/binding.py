@@ -85,6 +85,9 @@ _SIGS = {
                            P, SZ, P, P], ctypes.c_int),
     "pa_decode_noalloc": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P],
                           ctypes.c_int),
+    "pa_prefill_workspace_bytes": ([I32, I32, I32, I32], SZ),
+    "pa_prefill": ([P, P, P, I64, P, I32, P, P, I32, I32, I32, I32, I32, I32, F32, I32, P, P, SZ, P,
+                    P], ctypes.c_int),
 }
 
 
@@ -270,6 +273,40 @@ def pa_decode_grouped(q, k_cache, v_cache, block_tables, seq_lens, scale, group_
                                  _ptr(workspace), workspace.numel(), _stream(stream),
                                  _opts(variant, events, stream))
     _check(rc, "pa_decode_grouped")
+    return out
+
+
+def pa_prefill_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads):
+    return int(lib().pa_prefill_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads))
+
+
+def pa_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_offsets, scale, max_seq_len=0,
+               out=None, workspace=None, dtype=None, stream=None, events=None):
+    """Causal attention of each sequence's piece of query tokens (chunked
+    prefill; a decode token is a piece of one) over its paged K/V.
+
+    q [Tq, Hq, D], the pieces back to back; q_offsets [B + 1] int32 (device)
+    with q_offsets[-1] = Tq; seq_lens [B] int32 count the piece's tokens,
+    whose K/V are already in the cache.  Returns out [Tq, Hq, D].
+    """
+    _need_cuda(q, k_cache, v_cache, block_tables, seq_lens, q_offsets)
+    assert block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    assert q_offsets.dtype == torch.int32
+    Tq, Hq, D = q.shape
+    NB, Hkv = k_cache.shape[0], k_cache.shape[1]
+    B = seq_lens.shape[0]
+    mb = block_tables.shape[1]
+    msl = max_seq_len if max_seq_len > 0 else mb * BLOCK_SIZE
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(max(pa_prefill_workspace_bytes(B, Tq, Hq, Hkv), 256),
+                                dtype=torch.uint8, device=q.device)
+    rc = lib().pa_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), mb,
+                          _ptr(seq_lens), _ptr(q_offsets), B, Tq, msl, Hq, Hkv, D, float(scale),
+                          _dtype_code(q, dtype), _ptr(out), _ptr(workspace), workspace.numel(),
+                          _stream(stream), _opts(0, events, stream))
+    _check(rc, "pa_prefill")
     return out
 
 

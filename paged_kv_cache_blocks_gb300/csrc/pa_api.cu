@@ -260,6 +260,81 @@ int pa_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int
                       dtype, d_out, d_workspace, workspace_bytes, stream, nullptr);
 }
 
+size_t pa_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
+                                  int32_t num_kv_heads) {
+  if (num_seqs < 0 || num_q_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads != 0)
+    return 0;
+  return pa::prefill_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads);
+}
+
+int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, int64_t num_blocks,
+               const int32_t* d_block_tables, int32_t max_blocks_per_seq, const int32_t* d_seq_lens,
+               const int32_t* d_q_offsets, int32_t num_seqs, int32_t num_q_tokens,
+               int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+               float scale, int32_t dtype, void* d_out, void* d_workspace, size_t workspace_bytes,
+               void* stream, const pa_decode_opts* opts) {
+  if (num_seqs < 0 || num_q_tokens < 0)
+    return fail(PA_ERR_INVALID, "pa_prefill: num_seqs and num_q_tokens must be >= 0");
+  if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_prefill: dtype");
+  if (!supported_head_dim(head_dim))
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill: head_dim must be 64 or 128");
+  if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "pa_prefill: num_q_heads must be a positive multiple of num_kv_heads");
+  const int32_t G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill: query heads per KV head must be 1, 2, 4 or 8");
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID, "pa_prefill: num_blocks and max_blocks_per_seq must be > 0");
+  if (num_blocks * num_kv_heads * PA_BLOCK_SIZE > INT32_MAX)
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill: num_blocks * num_kv_heads * 16 must be < 2^31");
+  if (static_cast<int64_t>(max_blocks_per_seq) * PA_BLOCK_SIZE > INT32_MAX)
+    return fail(PA_ERR_INVALID, "pa_prefill: max_blocks_per_seq too large");
+  const int32_t cap = max_blocks_per_seq * PA_BLOCK_SIZE;
+  if (max_seq_len <= 0) max_seq_len = cap;
+  if (max_seq_len > cap)
+    return fail(PA_ERR_INVALID, "pa_prefill: max_seq_len exceeds max_blocks_per_seq * 16");
+  if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_prefill: scale is not finite");
+  if (opts && opts->variant != 0 && opts->variant != 2)
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill: only the tensor-core variant exists");
+  if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;
+  if (!d_q || !d_k_cache || !d_v_cache || !d_block_tables || !d_seq_lens || !d_q_offsets || !d_out ||
+      !d_workspace)
+    return fail(PA_ERR_INVALID, "pa_prefill: NULL pointer");
+  if (!aligned(d_k_cache, 16) || !aligned(d_v_cache, 16) || !aligned(d_q, 16) || !aligned(d_out, 16) ||
+      !aligned(d_workspace, 256) || !aligned(d_block_tables, 4) || !aligned(d_seq_lens, 4) ||
+      !aligned(d_q_offsets, 4))
+    return fail(PA_ERR_INVALID,
+                "pa_prefill: q, out and caches must be 16-byte aligned, the workspace 256-byte aligned");
+  if (workspace_bytes < pa::prefill_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads))
+    return fail(PA_ERR_INVALID, "pa_prefill: workspace smaller than pa_prefill_workspace_bytes()");
+  pa::PrefillArgs a;
+  a.q = d_q;
+  a.k_cache = d_k_cache;
+  a.v_cache = d_v_cache;
+  a.num_blocks = num_blocks;
+  a.block_tables = d_block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.seq_lens = d_seq_lens;
+  a.q_offsets = d_q_offsets;
+  a.num_seqs = num_seqs;
+  a.num_q_tokens = num_q_tokens;
+  a.max_seq_len = max_seq_len;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
+  a.scale = scale;
+  a.dtype = dtype;
+  a.out = d_out;
+  a.workspace = d_workspace;
+  a.stream = stream;
+  a.ev_before = opts ? opts->event_before_main : nullptr;
+  a.ev_after = opts ? opts->event_after_main : nullptr;
+  std::string why;
+  int rc = pa::prefill_launch(a, &why);
+  return rc ? fail(rc, why) : PA_OK;
+}
+
 int pa_decode_check(const void* d_workspace, void* stream, int32_t* error_bits) {
   if (!d_workspace || !error_bits) return fail(PA_ERR_INVALID, "pa_decode_check: NULL argument");
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

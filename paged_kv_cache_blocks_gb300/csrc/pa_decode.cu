@@ -90,31 +90,6 @@ __device__ __forceinline__ int clamp_len(const DecodeParams& P, int b) {
 }
 
 // Exclusive scan over the 1024 threads of the block; *total = sum.
-__device__ int block_exclusive_scan(int v, int* sw, int* total) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sw[w] = x;
-  __syncthreads();
-  if (w == 0) {
-    int t = lane < nw ? sw[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += y;
-    }
-    sw[lane] = t;
-  }
-  __syncthreads();
-  int res = (w ? sw[w - 1] : 0) + x - v;
-  *total = sw[nw - 1];
-  __syncthreads();
-  return res;
-}
 
 // Group of sequence b: the last g with group_off[g] <= b.
 __device__ __forceinline__ int group_of(const DecodeParams& P, int b) {
@@ -1317,6 +1292,8 @@ bool encode_fp8_maps(CUtensorMap* mk, CUtensorMap* mv, const void* kbase, const 
   return true;
 }
 
+}  // namespace
+
 bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D,
                       std::string* why) {
   EncodeTiledFn fn = get_encode_fn(why);
@@ -1335,6 +1312,8 @@ bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int 
   }
   return true;
 }
+
+namespace {
 
 struct LaunchShape {
   int grid;

@@ -3,10 +3,13 @@
 // 16-bit <-> fp32 conversions, and the decode workspace layout.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <string>
 
 namespace pa {
 
@@ -294,5 +297,38 @@ __device__ __forceinline__ float to_float<__half>(__half x) {
 __device__ __forceinline__ uint32_t swz128(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
+
+// Exclusive prefix sum of one int per thread over the whole CTA; *total gets
+// the sum.  sw: 32 ints of shared scratch.  Every thread must call it.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* sw, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sw[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < nw ? sw[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    sw[lane] = t;
+  }
+  __syncthreads();
+  int res = (w ? sw[w - 1] : 0) + x - v;
+  *total = sw[nw - 1];
+  __syncthreads();
+  return res;
+}
+
+// Tensor map over a 16-bit cache [num_blocks][hkv][16][D] viewed as rows of D
+// elements: box 64 elements x 16 rows, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D,
+                      std::string* why);
 
 }  // namespace pa

@@ -45,6 +45,34 @@ int decode_launch(const DecodeArgs& a, std::string* why);
 size_t decode_workspace_bytes(int64_t num_seqs, int64_t num_q_heads, int64_t head_dim,
                               int64_t max_seq_len, bool grouped = false);
 
+struct PrefillArgs {
+  const void* q;              // [num_q_tokens][num_q_heads][head_dim]
+  const void* k_cache;
+  const void* v_cache;
+  int64_t num_blocks;
+  const int32_t* block_tables;
+  int32_t max_blocks_per_seq;
+  const int32_t* seq_lens;
+  const int32_t* q_offsets;   // [num_seqs + 1]
+  int32_t num_seqs;
+  int32_t num_q_tokens;
+  int32_t max_seq_len;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  float scale;
+  int32_t dtype;
+  void* out;
+  void* workspace;
+  void* stream;
+  void* ev_before;
+  void* ev_after;
+};
+
+int prefill_launch(const PrefillArgs& a, std::string* why);
+size_t prefill_workspace_bytes(int64_t num_seqs, int64_t num_q_tokens, int64_t num_q_heads,
+                               int64_t num_kv_heads);
+
 int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
                        int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
                        int64_t num_blocks, void* stream, std::string* why);

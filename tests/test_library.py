@@ -79,3 +79,38 @@ def test_workspace_size_grows_with_partitions(L):
     # partial results: (max, sum) + head_dim floats per (partition, query head)
     assert b - a >= 8 * 32 * (128 + 2) * 4
     assert L.pa_decode_workspace_bytes(-1, 32, 128, 512) == 0
+
+
+def _prefill_args(**kw):
+    from paged_kv_cache_blocks_gb300 import binding as b
+    a = dict(q=1 << 20, k=1 << 20, v=1 << 20, nb=100, tab=1 << 20, mb=8, lens=1 << 20,
+             qoff=1 << 20, B=4, Tq=40, msl=0, hq=8, hkv=2, d=128, scale=0.1, dtype=b.PA_BF16,
+             out=1 << 20, ws=1 << 20, wsb=1 << 30, stream=None, opts=None)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return (P(a["q"]), P(a["k"]), P(a["v"]), a["nb"], P(a["tab"]), a["mb"], P(a["lens"]),
+            P(a["qoff"]), a["B"], a["Tq"], a["msl"], a["hq"], a["hkv"], a["d"], a["scale"],
+            a["dtype"], P(a["out"]), P(a["ws"]), a["wsb"], a["stream"], a["opts"])
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(d=96), 3), (dict(dtype=7), 3), (dict(hq=6, hkv=4), 1), (dict(hq=32, hkv=2), 3),
+    (dict(nb=0), 1), (dict(mb=0), 1), (dict(msl=8 * 16 + 1), 1), (dict(scale=float("nan")), 1),
+    (dict(qoff=0), 1), (dict(ws=1 << 20 | 8), 1), (dict(out=(1 << 20) + 2), 1), (dict(wsb=16), 1),
+    (dict(B=-1), 1), (dict(Tq=-1), 1), (dict(nb=1 << 27, hkv=2, hq=2), 3),
+])
+def test_prefill_rejects_bad_arguments(L, bad, code):
+    rc = L.pa_prefill(*_prefill_args(**bad))
+    assert rc == code, L.pa_last_error_string()
+    assert L.pa_last_error_string()
+
+
+def test_prefill_empty_is_a_noop_and_workspace_sizes(L):
+    assert L.pa_prefill(*_prefill_args(B=0)) == 0
+    assert L.pa_prefill(*_prefill_args(Tq=0)) == 0
+    # one (sequence, tile) record of 16 bytes per 128 query rows, plus one per sequence
+    a = L.pa_prefill_workspace_bytes(4, 1000, 64, 8)
+    b = L.pa_prefill_workspace_bytes(4, 100000, 64, 8)
+    assert b > a > 0
+    assert b - a >= (100000 - 1000) // 16 * 16 - 256
+    assert L.pa_prefill_workspace_bytes(4, 100, 6, 4) == 0

@@ -1,0 +1,153 @@
+"""Multi-query paged attention (chunked prefill) on the GPU against the fp64
+oracle: pa_cache_write puts each piece's K/V into the pool, then pa_prefill
+attends causally; the oracle computes the same rows from the same pool."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as U
+import oracle
+from paged_kv_cache_blocks_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pa():
+    return U.require_gpu()
+
+
+def _u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run(pa, pb, rows=None, pools=None, tables=None, write=True):
+    """GPU output (all rows) and the oracle's rows of one multi-query batch."""
+    w = pb.workload
+    dt = U.TORCH_DT[w.dtype]
+    if pools is None:
+        kc, vc = U.to_dev(pb.k_cache, w.dtype), U.to_dev(pb.v_cache, w.dtype)
+        if write:
+            pa.pa_cache_write(U.to_dev(pb.new_k, w.dtype), U.to_dev(pb.new_v, w.dtype),
+                              torch.from_numpy(pb.slot_mapping).cuda(), kc, vc)
+        else:
+            pk, pv = pb.placed_pools()
+            kc, vc = U.to_dev(pk, w.dtype), U.to_dev(pv, w.dtype)
+    else:
+        kc, vc = pools
+    tab = pb.block_tables if tables is None else tables
+    ws = torch.empty(max(pa.pa_prefill_workspace_bytes(len(pb.seq_lens), pb.num_q_tokens,
+                                                       w.num_q_heads, w.num_kv_heads), 256),
+                     dtype=torch.uint8, device="cuda")
+    out = pa.pa_prefill(U.to_dev(pb.q, w.dtype), kc, vc, torch.from_numpy(tab).cuda(),
+                        torch.from_numpy(pb.seq_lens).cuda(), torch.from_numpy(pb.q_offsets).cuda(),
+                        w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_decode_check(ws) == 0
+    got = out.double().cpu().numpy()
+    ref = oracle.prefill(_u16(pb.q), _u16(kc), _u16(vc), tab, pb.seq_lens, pb.q_offsets, w.scale,
+                         w.dtype, rows=rows)
+    return (got if rows is None else got[rows]), ref, out
+
+
+SMALL = [
+    # (workload, lens, pieces): whole prompts, pieces mid-prompt, decode tokens,
+    # pieces crossing blocks and spanning several 128-row tiles
+    ("tiny", [1, 17, 33, 100], [1, 17, 9, 40]),
+    ("llama8b", [37, 300, 50, 16, 129, 700], [37, 1, 16, 3, 64, 300]),
+    ("llama70b", [70, 5, 33, 600, 1000], [20, 5, 1, 200, 17]),
+]
+
+
+@pytest.mark.parametrize("name,lens,pieces", SMALL, ids=[s[0] for s in SMALL])
+def test_prefill_small_all_rows(pa, name, lens, pieces):
+    pb = W.make_prefill_batch(name, seed=3, lens=lens, pieces=pieces)
+    got, ref, _ = run(pa, pb)
+    U.assert_close_rounded(got, ref, pb.workload.dtype, f"prefill {name}")
+
+
+def test_prefill_one_query_head_per_kv_head(pa):
+    """G = 1 (tiles of 128 query tokens), fp16, head_dim 64."""
+    lens, pieces = [300, 129, 64, 1], [260, 129, 1, 1]
+    w = W.WORKLOADS["tiny"]
+    import dataclasses
+    W.WORKLOADS["g1"] = dataclasses.replace(w, name="g1", num_q_heads=2, num_kv_heads=2)
+    W._SEED_SALT["g1"] = 77
+    try:
+        pb = W.make_prefill_batch("g1", seed=1, lens=lens, pieces=pieces)
+        got, ref, _ = run(pa, pb)
+        U.assert_close_rounded(got, ref, "f16", "prefill G=1")
+    finally:
+        del W.WORKLOADS["g1"], W._SEED_SALT["g1"]
+
+
+@pytest.mark.parametrize("iteration", [1, 8])
+def test_prefill_chunked_workload_sampled(pa, iteration):
+    """The full chunked workload (30000-token prompt, piece k of 8, plus 20
+    decode tokens): rows across the piece (first, last, tile edges) and every
+    decode token, computed one by one by the oracle."""
+    pb = W.make_prefill_batch("chunked", seed=0, iteration=iteration)
+    n = int(pb.pieces[0])
+    rows = np.unique(np.concatenate([[0, 1, 15, 16, 17, n // 2, n - 17, n - 16, n - 2, n - 1],
+                                     np.arange(n, pb.num_q_tokens)])).astype(np.int64)
+    got, ref, _ = run(pa, pb, rows=rows)
+    U.assert_close_rounded(got, ref, "bf16", f"chunked iteration {iteration}")
+
+
+def test_prefill_decode_tokens_match_pa_decode(pa):
+    """Pieces of one token are decode steps: pa_prefill and pa_decode agree."""
+    pb = W.make_prefill_batch("llama8b", seed=6, lens=[1, 16, 17, 511, 2000, 33],
+                              pieces=[1] * 6)
+    got, ref, out = run(pa, pb)
+    U.assert_close_rounded(got, ref, "bf16", "decode-shaped prefill")
+    kc, vc = pb.placed_pools()
+    dec = pa.pa_decode(U.to_dev(pb.q, "bf16"), U.to_dev(kc, "bf16"), U.to_dev(vc, "bf16"),
+                       torch.from_numpy(pb.block_tables).cuda(),
+                       torch.from_numpy(pb.seq_lens).cuda(), pb.workload.scale)
+    torch.cuda.synchronize()
+    assert (out.double() - dec.double()).abs().max().item() <= 2e-2
+
+
+def test_prefill_deterministic_and_relabel_invariant(pa):
+    """Every row is one warp's sum in block order: repeated calls and a
+    relabelling of the physical blocks give bit-identical outputs."""
+    pb = W.make_prefill_batch("llama70b", seed=8, lens=[900, 40, 333], pieces=[400, 1, 100])
+    _, _, a = run(pa, pb, rows=np.array([0], np.int64), write=False)
+    _, _, b = run(pa, pb, rows=np.array([0], np.int64), write=False)
+    assert torch.equal(a, b)
+    pk, pv = pb.placed_pools()
+    perm = np.random.default_rng(2).permutation(pb.num_blocks)
+    inv = torch.from_numpy(np.argsort(perm))
+    pools = (U.to_dev(pk[inv], "bf16"), U.to_dev(pv[inv], "bf16"))
+    _, _, c = run(pa, pb, rows=np.array([0], np.int64), pools=pools,
+                  tables=perm[pb.block_tables].astype(np.int32))
+    assert torch.equal(a, c)
+
+
+def test_prefill_flags_bad_input_without_faulting(pa):
+    """A piece longer than its sequence and a block id outside the pool are
+    flagged; the call completes."""
+    pb = W.make_prefill_batch("llama8b", seed=9, lens=[40, 20], pieces=[10, 4])
+    w = pb.workload
+    kc, vc = pb.placed_pools()
+    kc, vc = U.to_dev(kc, w.dtype), U.to_dev(vc, w.dtype)
+    ws = torch.empty(pa.pa_prefill_workspace_bytes(2, pb.num_q_tokens, w.num_q_heads,
+                                                   w.num_kv_heads), dtype=torch.uint8, device="cuda")
+    q = U.to_dev(pb.q, w.dtype)
+    tab = torch.from_numpy(pb.block_tables).cuda()
+    bad_lens = torch.tensor([40, 3], dtype=torch.int32, device="cuda")     # piece of 4 > 3
+    pa.pa_prefill(q, kc, vc, tab, bad_lens, torch.from_numpy(pb.q_offsets).cuda(), w.scale,
+                  workspace=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_decode_check(ws) & 1
+    tab2 = tab.clone()
+    tab2[0, 1] = pb.num_blocks + 5
+    out = pa.pa_prefill(q, kc, vc, tab2, torch.from_numpy(pb.seq_lens).cuda(),
+                        torch.from_numpy(pb.q_offsets).cuda(), w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert pa.pa_decode_check(ws) & 2
+    # rows of the sequence with the good table are unaffected
+    ref = oracle.prefill(_u16(pb.q), _u16(kc), _u16(vc), pb.block_tables, pb.seq_lens,
+                         pb.q_offsets, w.scale, w.dtype)
+    U.assert_close_rounded(out[10:].double().cpu().numpy(), ref[10:], "bf16",
+                           "rows after a bad block id")
