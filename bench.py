@@ -55,7 +55,7 @@ DESCR["chunked"] = ("chunked prefill, Llama-3-70B-shaped layer (64 q / 8 kv head
                     "iteration with the decode tokens of 20 chats of 300+U{1..100} tokens; one step "
                     "= the 8 iterations (pa_cache_write of the pieces + pa_prefill)")
 PREFILL_METRIC = "paged chunked-prefill attention TFLOP/s (causal, dense-equivalent 4*q*k*d per head)"
-VARIANTS = {"auto": 0, "fma": 1, "mma": 2}
+VARIANTS = {"auto": 0, "fma": 1, "mma": 2, "tc": 3}
 
 
 # --------------------------------------------------------------------------- helpers
@@ -322,7 +322,7 @@ def run_prefill(args, rank, world, local_rank):
             pa.pa_cache_write(it["nk"], it["nv"], it["slots"], it["kc"], it["vc"])
             pa.pa_prefill(it["q"], it["kc"], it["vc"], it["tab"], it["lens"], it["qoff"], w.scale,
                           max_seq_len=it["msl"], out=it["out"], workspace=it["ws"],
-                          events=evs[i] if evs else None)
+                          events=evs[i] if evs else None, variant=VARIANTS[args.variant])
 
     for _ in range(args.warmup):
         step()
@@ -380,12 +380,15 @@ def run_prefill(args, rank, world, local_rank):
         "config": {"workload": DESCR["chunked"], "iterations": len(its),
                    "query_tokens_per_step": q_tokens, "flops_per_step": flops,
                    "kv_tokens_last_iteration": int(its[-1]["host"].seq_lens.sum()),
+                   "variant": args.variant,
                    "l2": "K/V per iteration <= 155 MB, re-read by every 16-token query tile: "
                          "compute-bound; no flush",
                    "parallelism": f"replicas x{world}"},
         "query_tokens_per_s": job_throughput(q_tokens, world, ms_step * 1e-3),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "prefill_kernel",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "prefill_kernel (mma.sync)" if args.variant == "mma"
+                     else "prefill_tc_kernel (tcgen05)",
                      "kernel_ms": kern_ms, "algorithmic_flops": flops, "peak_source": peak_src},
         "e2e": e2e,
         "gpu_launches": 3 * len(its) * args.steps,
@@ -418,7 +421,8 @@ def run_prefill_e2e(args, pa, its, w, dev, barrier, dist, world, flops):
                 d[k].copy_(h[k], non_blocking=True)
             pa.pa_cache_write(d["nk"], d["nv"], d["slots"], it["kc"], it["vc"])
             pa.pa_prefill(d["q"], it["kc"], it["vc"], d["tab"], d["lens"], d["qoff"], w.scale,
-                          max_seq_len=it["msl"], out=it["out"], workspace=it["ws"])
+                          max_seq_len=it["msl"], out=it["out"], workspace=it["ws"],
+                          variant=VARIANTS[args.variant])
             h["out"].copy_(it["out"], non_blocking=True)
         torch.cuda.current_stream().synchronize()
 

@@ -214,7 +214,9 @@ int pa_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int
 
 /* Options for pa_decode_ex.  Zero-initialised = the pa_decode behaviour. */
 typedef struct {
-    int32_t variant;         /* 0 auto, 1 CUDA-core FMA + warp shuffles, 2 tensor-core mma */
+    int32_t variant;         /* 0 auto, 1 CUDA-core FMA + warp shuffles, 2 tensor-core
+                                mma.sync, 3 tcgen05 with tensor-memory accumulators
+                                (pa_prefill at head_dim 128 only) */
     int32_t reserved0;
     void* event_before_main; /* optional cudaEvent_t recorded just before the attention */
     void* event_after_main;  /* kernel and just after it, on the same stream */
@@ -319,8 +321,9 @@ int pa_decode_fp8(const void* d_q, const void* d_k_cache8, const void* d_v_cache
  *                  pa_decode (max_seq_len bounds every seq_lens[b])
  *   d_workspace    >= pa_prefill_workspace_bytes(...) bytes, 256-byte
  *                  aligned, caller-owned; calls sharing it must not overlap
- *   opts           NULL, or events recorded around the attention kernel
- *                  (variant must be 0 or 2)
+ *   opts           NULL, or events recorded around the attention kernel;
+ *                  variant 0 = tcgen05 at head_dim 128 and mma.sync at 64,
+ *                  2 = mma.sync, 3 = tcgen05 (head_dim 128)
  *
  * fp32 accumulation, one rounding to dtype.  Bad device data never faults: a
  * length outside [0, max_seq_len], a piece longer than its sequence or

@@ -280,14 +280,18 @@ def pa_prefill_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads
     return int(lib().pa_prefill_workspace_bytes(num_seqs, num_q_tokens, num_q_heads, num_kv_heads))
 
 
+PREFILL_VARIANTS = {"auto": 0, "mma": 2, "tc": 3}
+
+
 def pa_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_offsets, scale, max_seq_len=0,
-               out=None, workspace=None, dtype=None, stream=None, events=None):
+               out=None, workspace=None, dtype=None, stream=None, events=None, variant=0):
     """Causal attention of each sequence's piece of query tokens (chunked
     prefill; a decode token is a piece of one) over its paged K/V.
 
     q [Tq, Hq, D], the pieces back to back; q_offsets [B + 1] int32 (device)
     with q_offsets[-1] = Tq; seq_lens [B] int32 count the piece's tokens,
-    whose K/V are already in the cache.  Returns out [Tq, Hq, D].
+    whose K/V are already in the cache.  ``variant``: 0 auto (tcgen05 at
+    head_dim 128), 2 mma.sync, 3 tcgen05.  Returns out [Tq, Hq, D].
     """
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens, q_offsets)
     assert block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
@@ -305,7 +309,7 @@ def pa_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_offsets, scale, ma
     rc = lib().pa_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), mb,
                           _ptr(seq_lens), _ptr(q_offsets), B, Tq, msl, Hq, Hkv, D, float(scale),
                           _dtype_code(q, dtype), _ptr(out), _ptr(workspace), workspace.numel(),
-                          _stream(stream), _opts(0, events, stream))
+                          _stream(stream), _opts(variant, events, stream))
     _check(rc, "pa_prefill")
     return out
 

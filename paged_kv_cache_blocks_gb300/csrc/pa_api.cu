@@ -295,8 +295,10 @@ int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, in
   if (max_seq_len > cap)
     return fail(PA_ERR_INVALID, "pa_prefill: max_seq_len exceeds max_blocks_per_seq * 16");
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_prefill: scale is not finite");
-  if (opts && opts->variant != 0 && opts->variant != 2)
-    return fail(PA_ERR_UNSUPPORTED, "pa_prefill: only the tensor-core variant exists");
+  if (opts && opts->variant != 0 && opts->variant != 2 && opts->variant != 3)
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill: variant must be 0 (auto), 2 (mma.sync) or 3 (tcgen05)");
+  if (opts && opts->variant == 3 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "pa_prefill: the tcgen05 variant needs head_dim 128");
   if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;
   if (!d_q || !d_k_cache || !d_v_cache || !d_block_tables || !d_seq_lens || !d_q_offsets || !d_out ||
       !d_workspace)
@@ -330,6 +332,7 @@ int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, in
   a.stream = stream;
   a.ev_before = opts ? opts->event_before_main : nullptr;
   a.ev_after = opts ? opts->event_after_main : nullptr;
+  a.variant = opts ? opts->variant : 0;
   std::string why;
   int rc = pa::prefill_launch(a, &why);
   return rc ? fail(rc, why) : PA_OK;

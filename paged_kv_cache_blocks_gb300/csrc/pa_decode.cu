@@ -1294,6 +1294,8 @@ bool encode_fp8_maps(CUtensorMap* mk, CUtensorMap* mv, const void* kbase, const 
 
 }  // namespace
 
+void* tensor_map_encoder(std::string* why) { return reinterpret_cast<void*>(get_encode_fn(why)); }
+
 bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D,
                       std::string* why) {
   EncodeTiledFn fn = get_encode_fn(why);

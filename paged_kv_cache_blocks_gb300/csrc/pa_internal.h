@@ -67,6 +67,7 @@ struct PrefillArgs {
   void* stream;
   void* ev_before;
   void* ev_after;
+  int32_t variant = 0;        // 0 auto, 2 mma.sync, 3 tcgen05 (head_dim 128)
 };
 
 int prefill_launch(const PrefillArgs& a, std::string* why);

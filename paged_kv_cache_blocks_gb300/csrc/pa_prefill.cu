@@ -31,6 +31,8 @@
 //                            position, and writes its rows' outputs.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -380,6 +382,473 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 version (head_dim 128).  One work item = (KV head, tile of 128 query
+// rows) as above.  Per CTA (one per SM, 6 warps):
+//   warp 0     takes items from the atomic counter and publishes them in a
+//              two-slot item ring; TMA-loads the tile's Q (128 rows x 128,
+//              a 3-D box of tokens x heads x dims) and the key blocks in
+//              chunks of 8 blocks = 128 keys into a two-stage ring (K and V
+//              of a chunk laid out as 128 swizzled rows per 64-dim half, so
+//              one descriptor spans the whole chunk);
+//   warp 1     allocates 512 tensor-memory columns and, one thread, issues
+//              S = Q K^T (M 128, N 128 keys, K 128 dims) into one of two
+//              S buffers for chunk c+1 while the softmax of chunk c runs, then
+//              O += P V (M 128, N 128 dims, K 128 keys) from P in shared
+//              memory; tcgen05.commit signals each result on an mbarrier;
+//   warps 2-5  one query row per thread (its tensor-memory lane): read S,
+//              apply the scale and the causal mask, online softmax in fp32 with
+//              the running maximum moved only when it grows by more than 2^8
+//              (the exact result either way, fewer rescales of O), write P as
+//              16-bit into shared memory in the operand layout, rescale O in
+//              tensor memory when the maximum moved, and finally write
+//              O / l.
+// Every wait is bounded; a timeout flags PA_DEVERR_TIMEOUT and the CTA
+// drains its copies and tensor-core work before freeing tensor memory.
+
+struct TcCfg {
+  static constexpr int kHalf = 128 * 128;           // 128 rows x 64 16-bit values
+  static constexpr int kQBytes = 2 * kHalf;          // Q tile, head_dim 128
+  static constexpr int kChunkBytes = 2 * kHalf;      // K (or V) of one chunk of 128 keys
+  static constexpr int kPBytes = 2 * kHalf;          // P: 128 rows x 128 keys
+  static constexpr int kChunkBlocks = 8;
+  static constexpr int kKStages = 2;
+  static constexpr int kVStages = 2;
+  static constexpr size_t kOffQ = 0;
+  static constexpr size_t kOffK = kOffQ + kQBytes;
+  static constexpr size_t kOffV = kOffK + static_cast<size_t>(kKStages) * kChunkBytes;
+  static constexpr size_t kOffP = kOffV + static_cast<size_t>(kVStages) * kChunkBytes;
+  static constexpr size_t kOffBar = kOffP + 2 * kPBytes;   // P double-buffered
+  static constexpr size_t kOffX = kOffBar + 512;     // row maxima / sums exchanged by warp pairs
+  static constexpr size_t kBytes = kOffX + 2 * 128 * 4 + 1024;
+  static constexpr int kProducerWarps = 4;           // one per SM sub-partition: TMA issue
+                                                     // from one warp is too slow for a chunk
+  static constexpr int kMmaWarp = kProducerWarps;
+  static constexpr int kSoftmaxWarp0 = kMmaWarp + 1;
+  static constexpr int kSoftmaxWarps = 8;            // two per row: 64 columns each
+  static constexpr int kThreads = 32 * (kSoftmaxWarp0 + kSoftmaxWarps);
+  static constexpr uint32_t kTmemCols = 512;         // S0 | S1 | O (128 columns each)
+};
+static_assert(TcCfg::kBytes <= 232448, "shared memory of one CTA");
+
+// Barrier indices; every ring of two has one barrier per slot, so that a
+// parity wait never meets a phase two uses ahead.
+enum TcBar {
+  kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kSFull = 8, kSFree = 10, kPFull = 12,
+  kODone = 14, kQFull = 16, kQEmpty = 17, kItemFull = 18, kItemEmpty = 20, kDrain = 22,
+  kXFull = 23, kXFree = 27,   // per tensor-memory quarter: the two softmax warps of a row
+  kNumTcBars = 31
+};
+static_assert(kNumTcBars * 8 + 16 <= 512, "barrier region");
+
+template <typename T>
+__global__ void __launch_bounds__(TcCfg::kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const PrefillParams P) {
+  using C = TcCfg;
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sP = smem + C::kOffP;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  volatile int* s_items = reinterpret_cast<volatile int*>(bar + kNumTcBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumTcBars + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + kNumTcBars + 2);
+  int* err = &P.ws->error_bits;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = P.G;
+  if (tid == 0) {
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(&bar[kKFull + i], C::kProducerWarps);
+      mbar_init(&bar[kKEmpty + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar[kVFull + i], C::kProducerWarps);
+      mbar_init(&bar[kVEmpty + i], 1);
+      mbar_init(&bar[kSFull + i], 1);
+      mbar_init(&bar[kSFree + i], C::kSoftmaxWarps);
+      mbar_init(&bar[kPFull + i], C::kSoftmaxWarps);
+      mbar_init(&bar[kODone + i], 1);
+      mbar_init(&bar[kItemFull + i], 1);
+      mbar_init(&bar[kItemEmpty + i], C::kProducerWarps + C::kSoftmaxWarps);   // helpers, MMA, softmax
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bar[kXFull + i], 2);
+      mbar_init(&bar[kXFree + i], 2);
+    }
+    mbar_init(&bar[kQFull], 1);
+    mbar_init(&bar[kQEmpty], 1);
+    mbar_init(&bar[kDrain], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == C::kMmaWarp) tmem_alloc(tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const int n_entries = *reinterpret_cast<volatile int32_t*>(&P.ws->n_entries);
+  const int n_work = n_entries * P.hkv;
+
+  if (warp < C::kProducerWarps) {
+    // ------------------------------------------------------------ producers
+    // Warp 0 takes items from the atomic counter and publishes them; all
+    // four producer warps read block ids 32 at a time (one coalesced load)
+    // and each issues the copies of blocks p and p + 4 of every chunk
+    // (lanes 0..3: block p / p + 4, dims 0-63 / 64-127), arming the stage
+    // barrier for its own 8 KB.
+    const int pw = warp;
+    const int64_t y_oob = P.num_blocks * P.hkv * kBlock;
+    uint32_t it = 0, cc = 0;
+    bool ok = true;
+    auto wait = [&](int idx, uint32_t parity) {
+      if (ok) ok = mbar_wait(&bar[idx], parity, abort_flag, err);
+      ok = __all_sync(0xffffffffu, ok);
+      return ok;
+    };
+    const int my_blk = pw + 4 * (lane & 1), my_hf = (lane >> 1) & 1;
+    while (ok) {
+      const int slot = it & 1;
+      int wi = 0;
+      if (pw == 0) {
+        if (lane == 0) wi = atomicAdd(&P.ws->next_item, 1);
+        wi = __shfl_sync(0xffffffffu, wi, 0);
+        if (*abort_flag) wi = n_work;
+        if (it >= 2 && !wait(kItemEmpty + slot, ((it >> 1) - 1) & 1)) break;
+        if (lane == 0) {
+          s_items[slot] = wi < n_work ? wi : -1;
+          mbar_arrive(&bar[kItemFull + slot]);
+        }
+        if (wi >= n_work) break;
+      } else {
+        if (!wait(kItemFull + slot, (it >> 1) & 1)) break;
+        wi = s_items[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kItemEmpty + slot]);
+        if (wi < 0) break;
+      }
+      const int h = wi / n_entries;
+      const int4 ent = P.entries[wi - h * n_entries];
+      const int b = ent.x, tile = ent.y, nkb = ent.z;
+      if (pw == 0) {
+        const PieceView v = piece_view(P, b, false);
+        if (it >= 1 && !wait(kQEmpty, (it - 1) & 1)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar[kQFull], C::kQBytes);
+          const int z = v.q0 + tile * P.tile_tokens;
+          tma_load_3d(sQ, &tm_q, 0, h * G, z, &bar[kQFull]);
+          tma_load_3d(sQ + C::kHalf, &tm_q, 64, h * G, z, &bar[kQFull]);
+        }
+      }
+      const int32_t* trow = P.tables + static_cast<int64_t>(b) * P.max_blocks;
+      const int nch = (nkb + C::kChunkBlocks - 1) / C::kChunkBlocks;
+      // K runs one chunk ahead of V: S of chunk c needs K(c) one step before
+      // O += P V needs V(c)
+      int32_t ids = 0, yk = 0, yprev = 0;   // lanes 0..3: the row of this lane's block
+      for (int c = 0; c <= nch && ok; ++c) {
+        if (c < nch) {
+          if ((c & 3) == 0) {   // ids of chunks c .. c + 3
+            const int blk = c * C::kChunkBlocks + lane;
+            int32_t id = blk < nkb ? trow[blk] : -1;   // past the tile's keys: zero fill
+            if (blk < nkb && (id < 0 || id >= P.num_blocks)) {
+              if (pw == 0) atomicOr(err, kErrBlockId);
+              id = -1;
+            }
+            ids = id;
+          }
+          const int32_t id = __shfl_sync(0xffffffffu, ids, (c & 3) * C::kChunkBlocks + my_blk);
+          yk = static_cast<int32_t>(id < 0 ? y_oob : (static_cast<int64_t>(id) * P.hkv + h) * kBlock);
+          const uint32_t x = cc + c;
+          const int ks = x % C::kKStages;
+          if (x >= C::kKStages && !wait(kKEmpty + ks, ((x / C::kKStages) - 1) & 1)) break;
+          if (lane == 0) mbar_arrive_expect_tx(&bar[kKFull + ks], C::kChunkBytes / C::kProducerWarps);
+          __syncwarp();
+          if (lane < 4)
+            tma_load_2d(smem + C::kOffK + static_cast<size_t>(ks) * C::kChunkBytes + my_hf * C::kHalf + my_blk * 2048,
+                        &tm_k, my_hf * 64, yk, &bar[kKFull + ks]);
+        }
+        if (c >= 1) {
+          const uint32_t x = cc + c - 1;
+          const int vs = x & 1;
+          if (x >= 2 && !wait(kVEmpty + vs, ((x >> 1) - 1) & 1)) break;
+          if (lane == 0) mbar_arrive_expect_tx(&bar[kVFull + vs], C::kChunkBytes / C::kProducerWarps);
+          __syncwarp();
+          if (lane < 4)
+            tma_load_2d(smem + C::kOffV + static_cast<size_t>(vs) * C::kChunkBytes + my_hf * C::kHalf + my_blk * 2048,
+                        &tm_v, my_hf * 64, yprev, &bar[kVFull + vs]);
+        }
+        yprev = yk;
+      }
+      cc += nch;
+      ++it;
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr int kBf = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+      constexpr uint32_t id_s = umma_idesc_f16(kBf, 0, 128, 128);
+      constexpr uint32_t id_o = umma_idesc_f16(kBf, 1, 128, 128);
+      // descriptors of the operand buffers; an MMA's operand is the base plus
+      // a constant byte offset (>> 4 in the start-address field)
+      const uint64_t dQ = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dP0 = umma_desc_sw128(smem_u32(sP), 16, 1024);
+      const uint64_t dK0 = umma_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+      // V is MN-major (dims contiguous): one N = 128 product spans its two
+      // 64-dim atoms, C::kHalf bytes apart (the leading byte offset); one
+      // 128-wide product runs at the full rate where two 64-wide ones do not
+      const uint64_t dV0 = umma_desc_sw128(smem_u32(smem + C::kOffV), C::kHalf, 1024);
+      uint32_t it = 0, cc = 0;
+      bool ok = true;
+      auto wait = [&](int idx, uint32_t parity) {
+        if (ok) ok = mbar_wait(&bar[idx], parity, abort_flag, err);
+        return ok;
+      };
+      auto issue_s = [&](uint32_t x) {
+        const int kst = x % C::kKStages, sb = x & 1;
+        if (!wait(kKFull + kst, (x / C::kKStages) & 1)) return;
+        if (x >= 2 && !wait(kSFree + sb, ((x >> 1) - 1) & 1)) return;
+        tc_fence_after();
+        const uint64_t dK = dK0 + (static_cast<uint64_t>(kst) * C::kChunkBytes >> 4);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks >> 2) * C::kHalf + (ks & 3) * 32) >> 4;
+          umma_f16_ss(tbase + sb * 128, dQ + off, dK + off, id_s, ks > 0);
+        }
+        umma_commit(&bar[kSFull + sb]);
+        umma_commit(&bar[kKEmpty + kst]);
+      };
+      while (ok) {
+        const int slot = it & 1;
+        if (!wait(kItemFull + slot, (it >> 1) & 1)) break;
+        const int wi = s_items[slot];
+        mbar_arrive(&bar[kItemEmpty + slot]);
+        if (wi < 0) break;
+        const int h = wi / n_entries;
+        const int nkb = P.entries[wi - h * n_entries].z;
+        const int nch = (nkb + C::kChunkBlocks - 1) / C::kChunkBlocks;
+        if (!wait(kQFull, it & 1)) break;
+        tc_fence_after();
+        if (nch == 0) umma_commit(&bar[kQEmpty]);
+        else issue_s(cc);
+        for (int c = 0; c < nch && ok; ++c, ++cc) {
+          if (c + 1 < nch) issue_s(cc + 1);
+          else umma_commit(&bar[kQEmpty]);   // Q is free once this item's S products are done
+          const int vs = cc & 1;
+          if (!wait(kVFull + vs, (cc >> 1) & 1)) break;
+          if (!wait(kPFull + vs, (cc >> 1) & 1)) break;
+          tc_fence_after();
+          const uint64_t dV = dV0 + (static_cast<uint64_t>(vs) * C::kChunkBytes >> 4);
+          const uint64_t dP = dP0 + (static_cast<uint64_t>(vs) * C::kPBytes >> 4);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t aoff = ((ks >> 2) * C::kHalf + (ks & 3) * 32) >> 4;
+            umma_f16_ss(tbase + 256, dP + aoff, dV + ((ks * 2048) >> 4), id_o, c > 0 || ks > 0);
+          }
+          umma_commit(&bar[kODone + vs]);
+          umma_commit(&bar[kVEmpty + vs]);
+        }
+        ++it;
+      }
+      // every product issued has completed before tensor memory is freed
+      umma_commit(&bar[kDrain]);
+      const unsigned long long t0 = global_timer_ns();
+      while (!mbar_try_wait(&bar[kDrain], 0) && global_timer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    // warps 2..9: thread = (row, half of the chunk's 128 columns); the two
+    // threads of a row sit in warps w and w + 4 (same tensor-memory quarter)
+    const int quarter = warp & 3;
+    const int half = (warp - C::kSoftmaxWarp0) >> 2;
+    const int row = 32 * quarter + lane;
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(32 * quarter) << 16);
+    float* xch = reinterpret_cast<float*>(smem + C::kOffX);   // [2 half][128 rows]
+    uint32_t it = 0, cc = 0;
+    bool ok = true;
+    auto wait = [&](int idx, uint32_t parity) {
+      if (ok) ok = mbar_wait(&bar[idx], parity, abort_flag, err);
+      ok = __all_sync(0xffffffffu, ok);
+      return ok;
+    };
+    // the partner's value: both threads of the row publish theirs, wait for
+    // the other (bounded mbarrier waits), read, and release the slot
+    uint32_t xk = 0;   // exchanges so far (the same count in both warps of a pair)
+    auto exchange = [&](float mine) {
+      if (xk >= 1) wait(kXFree + quarter, (xk - 1) & 1);
+      xch[half * 128 + row] = mine;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kXFull + quarter]);
+      wait(kXFull + quarter, xk & 1);
+      const float other = xch[(half ^ 1) * 128 + row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kXFree + quarter]);
+      ++xk;
+      return other;
+    };
+    while (ok) {
+      const int slot = it & 1;
+      if (!wait(kItemFull + slot, (it >> 1) & 1)) break;
+      const int wi = s_items[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kItemEmpty + slot]);
+      if (wi < 0) break;
+      const int h = wi / n_entries;
+      const int4 ent = P.entries[wi - h * n_entries];
+      const int b = ent.x, tile = ent.y, nkb = ent.z;
+      const PieceView v = piece_view(P, b, false);
+      const int nch = (nkb + C::kChunkBlocks - 1) / C::kChunkBlocks;
+      const int tok = tile * P.tile_tokens + row / G;
+      const int pos = v.L - v.n + tok;
+      const bool valid = tok < v.n && pos >= 0;
+      const int lim = valid ? pos : -1;
+      float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
+      for (int c = 0; c < nch; ++c, ++cc) {
+        const int sb = cc & 1;
+        if (!wait(kSFull + sb, (cc >> 1) & 1)) break;
+        tc_fence_after();
+        // this thread's 64 scores of the chunk, and the partner's 64 for the
+        // row maximum (reading them is cheaper than exchanging maxima)
+        const int k0 = c * 128 + 64 * half;
+        const int ko = c * 128 + 64 * (half ^ 1);
+        float t[64];
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // 4 chains for ILP
+        {
+          float u[64];
+          tmem_ld64(lane_addr + sb * 128 + 64 * (half ^ 1), u);
+          if (!__all_sync(0xffffffffu, ko + 63 <= lim)) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) u[i] = ko + i <= lim ? u[i] : -INFINITY;
+          }
+#pragma unroll
+          for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], u[i]);
+        }
+        tmem_ld64(lane_addr + sb * 128 + 64 * half, t);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
+        if (!__all_sync(0xffffffffu, k0 + 63 <= lim)) {   // causal mask / tail: -inf
+#pragma unroll
+          for (int i = 0; i < 64; ++i) t[i] = k0 + i <= lim ? t[i] : -INFINITY;
+        }
+#pragma unroll
+        for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], t[i]);
+        // the scale is positive, so it commutes with the maximum
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
+        const bool need = mx > m_ref + 8.f;
+        const float new_ref = need ? mx : m_ref;
+        const float mu = new_ref == -INFINITY ? 0.f : new_ref;
+        const float alpha = need ? exp2f(m_ref - new_ref) : 1.f;
+        // P buffer sb is free once the PV of two chunks back has completed
+        if (cc >= 2 && !wait(kODone + sb, ((cc >> 1) - 1) & 1)) break;
+        // p = 2^(s * scale - mu) as 16-bit into P (operand layout), row sum in fp32
+        float r4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t prow = smem_u32(sP) + sb * C::kPBytes + half * C::kHalf + row * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {   // 16-byte chunk = keys 8 ch .. 8 ch + 7 of this half
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = fast_exp2(fmaf(t[8 * ch + 2 * e], P.scale_log2, -mu));
+            const float p1 = fast_exp2(fmaf(t[8 * ch + 2 * e + 1], P.scale_log2, -mu));
+            r4[e] += p0 + p1;
+            pk[e] = pack2<T>(p0, p1);
+          }
+          const uint32_t a = prow + ((ch ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]),
+                       "r"(pk[2]), "r"(pk[3])
+                       : "memory");
+        }
+        l = l * alpha + ((r4[0] + r4[1]) + (r4[2] + r4[3]));
+        if (c > 0 && __any_sync(0xffffffffu, need)) {
+          // O must hold the previous chunk's product before it is rescaled
+          if (!wait(kODone + (sb ^ 1), ((cc - 1) >> 1) & 1)) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int cb = 0; cb < 2; ++cb) {
+            float o32[32];
+            tmem_ld32(lane_addr + 256 + 64 * half + cb * 32, o32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o32[i] *= alpha;
+            tmem_st32(lane_addr + 256 + 64 * half + cb * 32, o32);
+          }
+        }
+        // V rows past the sequence end (the last block's tail) may hold
+        // anything, NaN included: zero them so that 0 * NaN never enters O
+        const int kc = c * 128;
+        if (kc + 128 > v.L) {
+          // the chunk's V copies have landed before their rows are overwritten
+          if (!wait(kVFull + sb, (cc >> 1) & 1)) break;
+          const int z0 = max(v.L, kc) - kc, z1 = min(kc + 128, nkb * kBlock) - kc;
+          uint8_t* sV = smem + C::kOffV + static_cast<size_t>(sb) * C::kChunkBytes;
+          for (int i = half * 128 + row; i < (z1 - z0) * 16; i += 256) {   // 16 x 16 bytes per key row
+            const int key = z0 + (i >> 4), part = i & 15;
+            *reinterpret_cast<uint4*>(sV + (part >> 3) * C::kHalf + key * 128 + (part & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kPFull + sb]);
+        m_ref = new_ref;
+      }
+      if (!ok) break;
+      // epilogue: out = O / l, one rounding to T; each thread writes its 64 columns
+      const float lsum = l + exchange(l);
+      if (!ok) break;
+      if (nch > 0 && !wait(kODone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1)) break;
+      tc_fence_after();
+      {
+        const float inv = (valid && lsum > 0.f) ? 1.0f / lsum : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(P.out) +
+                                              ((static_cast<int64_t>(v.q0) + tok) * P.hq + h * G + row % G) * D +
+                                              64 * half);
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+          float o32[32];
+          if (nch > 0) {   // uniform over the warp: every lane takes part in the load
+            tmem_ld32(lane_addr + 256 + 64 * half + cb * 32, o32);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o32[i] = 0.f;
+          }
+          if (tok < v.n) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              dst[cb * 4 + q4] = make_uint4(pack2<T>(o32[8 * q4] * inv, o32[8 * q4 + 1] * inv),
+                                            pack2<T>(o32[8 * q4 + 2] * inv, o32[8 * q4 + 3] * inv),
+                                            pack2<T>(o32[8 * q4 + 4] * inv, o32[8 * q4 + 5] * inv),
+                                            pack2<T>(o32[8 * q4 + 6] * inv, o32[8 * q4 + 7] * inv));
+          }
+        }
+      }
+      tc_fence_before();
+      ++it;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // copies still in flight land before the CTA leaves: a copy takes
+    // microseconds, so every thread waits 200 us of global time
+    const unsigned long long t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+  }
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::kTmemCols);
+  }
+}
+
 namespace {
 
 constexpr int kPrefillWarps = 8;
@@ -415,6 +884,60 @@ bool launch_prefill(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillP
 
 int64_t max_entries(int64_t num_seqs, int64_t num_q_tokens, int64_t tile_tokens) {
   return num_q_tokens / tile_tokens + num_seqs + 1;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// q [Tq][hq][D] as a 3-D tensor (dims, heads, tokens); one box = the G heads
+// of a KV head for 128 / G tokens and 64 dims: 128 rows of 128 bytes in the
+// order (token, head), 128-byte swizzle.
+bool encode_q_map(CUtensorMap* m, const void* q, int64_t Tq, int hq, int G, int D,
+                  std::string* why) {
+  EncodeTiledFn fn = reinterpret_cast<EncodeTiledFn>(tensor_map_encoder(why));
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(hq),
+                        static_cast<cuuint64_t>(Tq)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(hq) * D * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled (q) failed with CUresult " + std::to_string(static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+template <typename T>
+bool launch_prefill_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const PrefillParams& P, int64_t max_work, cudaStream_t s, std::string* why) {
+  auto kern = prefill_tc_kernel<T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(TcCfg::kBytes));
+  if (e != cudaSuccess) {
+    *why = std::string("cudaFuncSetAttribute (prefill tc): ") + cudaGetErrorString(e);
+    return false;
+  }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // one CTA per SM: its shared memory rules out a second one, and each CTA
+  // holds all 512 tensor-memory columns
+  int64_t grid = sms;
+  if (grid > max_work) grid = max_work;
+  if (grid < 1) grid = 1;
+  kern<<<static_cast<unsigned>(grid), TcCfg::kThreads, TcCfg::kBytes, s>>>(tq, tk, tv, P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    *why = std::string("prefill tc launch: ") + cudaGetErrorString(e);
+    return false;
+  }
+  return true;
 }
 
 }  // namespace
@@ -458,12 +981,21 @@ int prefill_launch(const PrefillArgs& a, std::string* why) {
     return 5;
   }
   const int64_t max_work = max_entries(a.num_seqs, a.num_q_tokens, P.tile_tokens) * a.num_kv_heads;
+  // variant 0: tcgen05 at head_dim 128, else mma.sync; 2: mma.sync; 3: tcgen05
+  const bool tc = a.variant == 3 || (a.variant == 0 && a.head_dim == 128);
+  CUtensorMap tq;
+  if (tc && !encode_q_map(&tq, a.q, a.num_q_tokens, a.num_q_heads, P.G, a.head_dim, why)) return 5;
   if (a.ev_before) cudaEventRecord(static_cast<cudaEvent_t>(a.ev_before), s);
-  bool ok = a.dtype == 1
-                ? (a.head_dim == 128 ? launch_prefill<__nv_bfloat16, 128>(tk, tv, P, max_work, s, why)
-                                     : launch_prefill<__nv_bfloat16, 64>(tk, tv, P, max_work, s, why))
-                : (a.head_dim == 128 ? launch_prefill<__half, 128>(tk, tv, P, max_work, s, why)
-                                     : launch_prefill<__half, 64>(tk, tv, P, max_work, s, why));
+  bool ok;
+  if (tc)
+    ok = a.dtype == 1 ? launch_prefill_tc<__nv_bfloat16>(tq, tk, tv, P, max_work, s, why)
+                      : launch_prefill_tc<__half>(tq, tk, tv, P, max_work, s, why);
+  else
+    ok = a.dtype == 1
+             ? (a.head_dim == 128 ? launch_prefill<__nv_bfloat16, 128>(tk, tv, P, max_work, s, why)
+                                  : launch_prefill<__nv_bfloat16, 64>(tk, tv, P, max_work, s, why))
+             : (a.head_dim == 128 ? launch_prefill<__half, 128>(tk, tv, P, max_work, s, why)
+                                  : launch_prefill<__half, 64>(tk, tv, P, max_work, s, why));
   if (!ok) return 5;
   if (a.ev_after) cudaEventRecord(static_cast<cudaEvent_t>(a.ev_after), s);
   return 0;

@@ -21,8 +21,9 @@ def _u16(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def run(pa, pb, rows=None, pools=None, tables=None, write=True):
-    """GPU output (all rows) and the oracle's rows of one multi-query batch."""
+def run(pa, pb, rows=None, pools=None, tables=None, write=True, variant=0):
+    """GPU output (all rows) and the oracle's rows of one multi-query batch
+    (variant: 0 auto, 2 mma.sync, 3 tcgen05)."""
     w = pb.workload
     dt = U.TORCH_DT[w.dtype]
     if pools is None:
@@ -41,7 +42,7 @@ def run(pa, pb, rows=None, pools=None, tables=None, write=True):
                      dtype=torch.uint8, device="cuda")
     out = pa.pa_prefill(U.to_dev(pb.q, w.dtype), kc, vc, torch.from_numpy(tab).cuda(),
                         torch.from_numpy(pb.seq_lens).cuda(), torch.from_numpy(pb.q_offsets).cuda(),
-                        w.scale, workspace=ws)
+                        w.scale, workspace=ws, variant=variant)
     torch.cuda.synchronize()
     assert pa.pa_decode_check(ws) == 0
     got = out.double().cpu().numpy()
@@ -59,11 +60,29 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("name,lens,pieces", SMALL, ids=[s[0] for s in SMALL])
-def test_prefill_small_all_rows(pa, name, lens, pieces):
+CASES = [(n, l, p, v) for n, l, p in SMALL for v in ((2,) if n == "tiny" else (2, 3))]
+
+
+@pytest.mark.parametrize("name,lens,pieces,variant", CASES,
+                         ids=[f"{c[0]}-{'tc' if c[3] == 3 else 'mma'}" for c in CASES])
+def test_prefill_small_all_rows(pa, name, lens, pieces, variant):
     pb = W.make_prefill_batch(name, seed=3, lens=lens, pieces=pieces)
-    got, ref, _ = run(pa, pb)
-    U.assert_close_rounded(got, ref, pb.workload.dtype, f"prefill {name}")
+    got, ref, _ = run(pa, pb, variant=variant)
+    U.assert_close_rounded(got, ref, pb.workload.dtype, f"prefill {name} variant {variant}")
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+def test_prefill_fp16_g4_both_variants(pa, variant):
+    """fp16 operands on the tensor cores (the tcgen05 kind::f16 with fp16 A/B)."""
+    import dataclasses
+    W.WORKLOADS["f16g4"] = dataclasses.replace(W.WORKLOADS["llama8b"], name="f16g4", dtype="f16")
+    W._SEED_SALT["f16g4"] = 78
+    try:
+        pb = W.make_prefill_batch("f16g4", seed=2, lens=[300, 47, 1000], pieces=[150, 47, 3])
+        got, ref, _ = run(pa, pb, variant=variant)
+        U.assert_close_rounded(got, ref, "f16", f"prefill fp16 variant {variant}")
+    finally:
+        del W.WORKLOADS["f16g4"], W._SEED_SALT["f16g4"]
 
 
 def test_prefill_one_query_head_per_kv_head(pa):
@@ -81,8 +100,8 @@ def test_prefill_one_query_head_per_kv_head(pa):
         del W.WORKLOADS["g1"], W._SEED_SALT["g1"]
 
 
-@pytest.mark.parametrize("iteration", [1, 8])
-def test_prefill_chunked_workload_sampled(pa, iteration):
+@pytest.mark.parametrize("iteration,variant", [(1, 3), (8, 3), (8, 2)])
+def test_prefill_chunked_workload_sampled(pa, iteration, variant):
     """The full chunked workload (30000-token prompt, piece k of 8, plus 20
     decode tokens): rows across the piece (first, last, tile edges) and every
     decode token, computed one by one by the oracle."""
@@ -90,8 +109,8 @@ def test_prefill_chunked_workload_sampled(pa, iteration):
     n = int(pb.pieces[0])
     rows = np.unique(np.concatenate([[0, 1, 15, 16, 17, n // 2, n - 17, n - 16, n - 2, n - 1],
                                      np.arange(n, pb.num_q_tokens)])).astype(np.int64)
-    got, ref, _ = run(pa, pb, rows=rows)
-    U.assert_close_rounded(got, ref, "bf16", f"chunked iteration {iteration}")
+    got, ref, _ = run(pa, pb, rows=rows, variant=variant)
+    U.assert_close_rounded(got, ref, "bf16", f"chunked iteration {iteration} variant {variant}")
 
 
 def test_prefill_decode_tokens_match_pa_decode(pa):
@@ -108,19 +127,21 @@ def test_prefill_decode_tokens_match_pa_decode(pa):
     assert (out.double() - dec.double()).abs().max().item() <= 2e-2
 
 
-def test_prefill_deterministic_and_relabel_invariant(pa):
-    """Every row is one warp's sum in block order: repeated calls and a
-    relabelling of the physical blocks give bit-identical outputs."""
+@pytest.mark.parametrize("variant", [2, 3])
+def test_prefill_deterministic_and_relabel_invariant(pa, variant):
+    """Every row is summed in block order by one warp (mma.sync) or one
+    thread and the tensor cores (tcgen05): repeated calls and a relabelling of
+    the physical blocks give bit-identical outputs."""
     pb = W.make_prefill_batch("llama70b", seed=8, lens=[900, 40, 333], pieces=[400, 1, 100])
-    _, _, a = run(pa, pb, rows=np.array([0], np.int64), write=False)
-    _, _, b = run(pa, pb, rows=np.array([0], np.int64), write=False)
+    _, _, a = run(pa, pb, rows=np.array([0], np.int64), write=False, variant=variant)
+    _, _, b = run(pa, pb, rows=np.array([0], np.int64), write=False, variant=variant)
     assert torch.equal(a, b)
     pk, pv = pb.placed_pools()
     perm = np.random.default_rng(2).permutation(pb.num_blocks)
     inv = torch.from_numpy(np.argsort(perm))
     pools = (U.to_dev(pk[inv], "bf16"), U.to_dev(pv[inv], "bf16"))
     _, _, c = run(pa, pb, rows=np.array([0], np.int64), pools=pools,
-                  tables=perm[pb.block_tables].astype(np.int32))
+                  tables=perm[pb.block_tables].astype(np.int32), variant=variant)
     assert torch.equal(a, c)
 
 
