@@ -410,34 +410,37 @@ struct TcCfg {
   static constexpr int kHalf = 128 * 128;           // 128 rows x 64 16-bit values
   static constexpr int kQBytes = 2 * kHalf;          // Q tile, head_dim 128
   static constexpr int kChunkBytes = 2 * kHalf;      // K (or V) of one chunk of 128 keys
-  static constexpr int kPBytes = 2 * kHalf;          // P: 128 rows x 128 keys
   static constexpr int kChunkBlocks = 8;
-  static constexpr int kKStages = 2;
-  static constexpr int kVStages = 2;
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 3;
   static constexpr size_t kOffQ = 0;
   static constexpr size_t kOffK = kOffQ + kQBytes;
   static constexpr size_t kOffV = kOffK + static_cast<size_t>(kKStages) * kChunkBytes;
-  static constexpr size_t kOffP = kOffV + static_cast<size_t>(kVStages) * kChunkBytes;
-  static constexpr size_t kOffBar = kOffP + 2 * kPBytes;   // P double-buffered
+  static constexpr size_t kOffBar = kOffV + static_cast<size_t>(kVStages) * kChunkBytes;
   static constexpr size_t kOffX = kOffBar + 512;     // row maxima / sums exchanged by warp pairs
   static constexpr size_t kBytes = kOffX + 2 * 128 * 4 + 1024;
   static constexpr int kProducerWarps = 4;           // one per SM sub-partition: TMA issue
                                                      // from one warp is too slow for a chunk
   static constexpr int kMmaWarp = kProducerWarps;
   static constexpr int kSoftmaxWarp0 = kMmaWarp + 1;
-  static constexpr int kSoftmaxWarps = 8;            // two per row: 64 columns each
+  static constexpr int kRowSplit = 1;                // softmax threads per row
+  static constexpr int kSoftmaxWarps = 4 * kRowSplit;
+  static constexpr int kCols = 128 / kRowSplit;      // S columns per softmax thread
   static constexpr int kThreads = 32 * (kSoftmaxWarp0 + kSoftmaxWarps);
-  static constexpr uint32_t kTmemCols = 512;         // S0 | S1 | O (128 columns each)
+  // tensor memory: S0 | S1 | O (128 fp32 columns each) | P0 | P1 (128 16-bit
+  // values per row packed into 64 columns each)
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColO = 256, kColP = 384;
 };
 static_assert(TcCfg::kBytes <= 232448, "shared memory of one CTA");
 
 // Barrier indices; every ring of two has one barrier per slot, so that a
 // parity wait never meets a phase two uses ahead.
 enum TcBar {
-  kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kSFull = 8, kSFree = 10, kPFull = 12,
-  kODone = 14, kQFull = 16, kQEmpty = 17, kItemFull = 18, kItemEmpty = 20, kDrain = 22,
-  kXFull = 23, kXFree = 27,   // per tensor-memory quarter: the two softmax warps of a row
-  kNumTcBars = 31
+  kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9, kSFull = 12, kSFree = 14, kPFull = 16,
+  kODone = 18, kQFull = 20, kQEmpty = 21, kItemFull = 22, kItemEmpty = 24, kDrain = 26,
+  kXFull = 27, kXFree = 31,   // per tensor-memory quarter: the two softmax warps of a row
+  kNumTcBars = 35
 };
 static_assert(kNumTcBars * 8 + 16 <= 512, "barrier region");
 
@@ -451,7 +454,6 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + C::kOffQ;
-  uint8_t* sP = smem + C::kOffP;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   volatile int* s_items = reinterpret_cast<volatile int*>(bar + kNumTcBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + kNumTcBars + 1);
@@ -464,9 +466,11 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       mbar_init(&bar[kKFull + i], C::kProducerWarps);
       mbar_init(&bar[kKEmpty + i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kVStages; ++i) {
       mbar_init(&bar[kVFull + i], C::kProducerWarps);
       mbar_init(&bar[kVEmpty + i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bar[kSFull + i], 1);
       mbar_init(&bar[kSFree + i], C::kSoftmaxWarps);
       mbar_init(&bar[kPFull + i], C::kSoftmaxWarps);
@@ -475,8 +479,8 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       mbar_init(&bar[kItemEmpty + i], C::kProducerWarps + C::kSoftmaxWarps);   // helpers, MMA, softmax
     }
     for (int i = 0; i < 4; ++i) {
-      mbar_init(&bar[kXFull + i], 2);
-      mbar_init(&bar[kXFree + i], 2);
+      mbar_init(&bar[kXFull + i], C::kRowSplit);
+      mbar_init(&bar[kXFree + i], C::kRowSplit);
     }
     mbar_init(&bar[kQFull], 1);
     mbar_init(&bar[kQEmpty], 1);
@@ -576,8 +580,8 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         }
         if (c >= 1) {
           const uint32_t x = cc + c - 1;
-          const int vs = x & 1;
-          if (x >= 2 && !wait(kVEmpty + vs, ((x >> 1) - 1) & 1)) break;
+          const int vs = x % C::kVStages;
+          if (x >= C::kVStages && !wait(kVEmpty + vs, ((x / C::kVStages) - 1) & 1)) break;
           if (lane == 0) mbar_arrive_expect_tx(&bar[kVFull + vs], C::kChunkBytes / C::kProducerWarps);
           __syncwarp();
           if (lane < 4)
@@ -598,7 +602,6 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       // descriptors of the operand buffers; an MMA's operand is the base plus
       // a constant byte offset (>> 4 in the start-address field)
       const uint64_t dQ = umma_desc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dP0 = umma_desc_sw128(smem_u32(sP), 16, 1024);
       const uint64_t dK0 = umma_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
       // V is MN-major (dims contiguous): one N = 128 product spans its two
       // 64-dim atoms, C::kHalf bytes apart (the leading byte offset); one
@@ -640,18 +643,17 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         for (int c = 0; c < nch && ok; ++c, ++cc) {
           if (c + 1 < nch) issue_s(cc + 1);
           else umma_commit(&bar[kQEmpty]);   // Q is free once this item's S products are done
-          const int vs = cc & 1;
-          if (!wait(kVFull + vs, (cc >> 1) & 1)) break;
-          if (!wait(kPFull + vs, (cc >> 1) & 1)) break;
+          const int vs = cc % C::kVStages, pb = cc & 1;
+          if (!wait(kVFull + vs, (cc / C::kVStages) & 1)) break;
+          if (!wait(kPFull + pb, (cc >> 1) & 1)) break;
           tc_fence_after();
           const uint64_t dV = dV0 + (static_cast<uint64_t>(vs) * C::kChunkBytes >> 4);
-          const uint64_t dP = dP0 + (static_cast<uint64_t>(vs) * C::kPBytes >> 4);
+          // A = P from tensor memory: 16 keys = 8 packed columns per step
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t aoff = ((ks >> 2) * C::kHalf + (ks & 3) * 32) >> 4;
-            umma_f16_ss(tbase + 256, dP + aoff, dV + ((ks * 2048) >> 4), id_o, c > 0 || ks > 0);
-          }
-          umma_commit(&bar[kODone + vs]);
+          for (int ks = 0; ks < 8; ++ks)
+            umma_f16_ts(tbase + C::kColO, tbase + C::kColP + 64 * pb + 8 * ks, dV + ((ks * 2048) >> 4), id_o,
+                        c > 0 || ks > 0);
+          umma_commit(&bar[kODone + pb]);
           umma_commit(&bar[kVEmpty + vs]);
         }
         ++it;
@@ -714,57 +716,49 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         const int sb = cc & 1;
         if (!wait(kSFull + sb, (cc >> 1) & 1)) break;
         tc_fence_after();
-        // this thread's 64 scores of the chunk, and the partner's 64 for the
-        // row maximum (reading them is cheaper than exchanging maxima)
-        const int k0 = c * 128 + 64 * half;
-        const int ko = c * 128 + 64 * (half ^ 1);
-        float t[64];
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // 4 chains for ILP
-        {
-          float u[64];
-          tmem_ld64(lane_addr + sb * 128 + 64 * (half ^ 1), u);
-          if (!__all_sync(0xffffffffu, ko + 63 <= lim)) {
+        // this thread's scores of the chunk; with two threads per row the
+        // row maximum combines the halves through the pair's exchange slot
+        const int k0 = c * 128 + C::kCols * half;
+        float t[C::kCols];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) u[i] = ko + i <= lim ? u[i] : -INFINITY;
-          }
-#pragma unroll
-          for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], u[i]);
-        }
-        tmem_ld64(lane_addr + sb * 128 + 64 * half, t);
+        for (int q = 0; q < C::kCols / 64; ++q) tmem_ld64(lane_addr + sb * 128 + C::kCols * half + 64 * q, t + 64 * q);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
-        if (!__all_sync(0xffffffffu, k0 + 63 <= lim)) {   // causal mask / tail: -inf
+        if (!__all_sync(0xffffffffu, k0 + C::kCols - 1 <= lim)) {   // causal mask / tail: -inf
 #pragma unroll
-          for (int i = 0; i < 64; ++i) t[i] = k0 + i <= lim ? t[i] : -INFINITY;
+          for (int i = 0; i < C::kCols; ++i) t[i] = k0 + i <= lim ? t[i] : -INFINITY;
         }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // 4 chains for ILP
 #pragma unroll
-        for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], t[i]);
+        for (int i = 0; i < C::kCols; ++i) m4[i & 3] = fmaxf(m4[i & 3], t[i]);
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        if (C::kRowSplit > 1) {
+          mx = fmaxf(mx, exchange(mx));
+          if (!ok) break;
+        }
         // the scale is positive, so it commutes with the maximum
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
+        mx *= P.scale_log2;
         const bool need = mx > m_ref + 8.f;
         const float new_ref = need ? mx : m_ref;
         const float mu = new_ref == -INFINITY ? 0.f : new_ref;
         const float alpha = need ? exp2f(m_ref - new_ref) : 1.f;
         // P buffer sb is free once the PV of two chunks back has completed
         if (cc >= 2 && !wait(kODone + sb, ((cc >> 1) - 1) & 1)) break;
-        // p = 2^(s * scale - mu) as 16-bit into P (operand layout), row sum in fp32
+        // p = 2^(s * scale - mu) as 16-bit, two per column, into this half's
+        // 32 columns of P buffer sb in tensor memory; row sum in fp32
         float r4[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t prow = smem_u32(sP) + sb * C::kPBytes + half * C::kHalf + row * 128;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {   // 16-byte chunk = keys 8 ch .. 8 ch + 7 of this half
-          uint32_t pk[4];
+        for (int q = 0; q < C::kCols / 64; ++q) {
+          uint32_t pk[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = fast_exp2(fmaf(t[8 * ch + 2 * e], P.scale_log2, -mu));
-            const float p1 = fast_exp2(fmaf(t[8 * ch + 2 * e + 1], P.scale_log2, -mu));
-            r4[e] += p0 + p1;
-            pk[e] = pack2<T>(p0, p1);
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = fast_exp2(fmaf(t[64 * q + 2 * i], P.scale_log2, -mu));
+            const float p1 = fast_exp2(fmaf(t[64 * q + 2 * i + 1], P.scale_log2, -mu));
+            r4[i & 3] += p0 + p1;
+            pk[i] = pack2<T>(p0, p1);
           }
-          const uint32_t a = prow + ((ch ^ (row & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(pk[0]), "r"(pk[1]),
-                       "r"(pk[2]), "r"(pk[3])
-                       : "memory");
+          tmem_st32u(lane_addr + C::kColP + 64 * sb + C::kCols / 2 * half + 32 * q, pk);
         }
         l = l * alpha + ((r4[0] + r4[1]) + (r4[2] + r4[3]));
         if (c > 0 && __any_sync(0xffffffffu, need)) {
@@ -772,12 +766,12 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
           if (!wait(kODone + (sb ^ 1), ((cc - 1) >> 1) & 1)) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int cb = 0; cb < 2; ++cb) {
+          for (int cb = 0; cb < C::kCols / 32; ++cb) {
             float o32[32];
-            tmem_ld32(lane_addr + 256 + 64 * half + cb * 32, o32);
+            tmem_ld32(lane_addr + C::kColO + C::kCols * half + cb * 32, o32);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o32[i] *= alpha;
-            tmem_st32(lane_addr + 256 + 64 * half + cb * 32, o32);
+            tmem_st32(lane_addr + C::kColO + C::kCols * half + cb * 32, o32);
           }
         }
         // V rows past the sequence end (the last block's tail) may hold
@@ -785,16 +779,17 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         const int kc = c * 128;
         if (kc + 128 > v.L) {
           // the chunk's V copies have landed before their rows are overwritten
-          if (!wait(kVFull + sb, (cc >> 1) & 1)) break;
+          const int vs = cc % C::kVStages;
+          if (!wait(kVFull + vs, (cc / C::kVStages) & 1)) break;
           const int z0 = max(v.L, kc) - kc, z1 = min(kc + 128, nkb * kBlock) - kc;
-          uint8_t* sV = smem + C::kOffV + static_cast<size_t>(sb) * C::kChunkBytes;
-          for (int i = half * 128 + row; i < (z1 - z0) * 16; i += 256) {   // 16 x 16 bytes per key row
+          uint8_t* sV = smem + C::kOffV + static_cast<size_t>(vs) * C::kChunkBytes;
+          for (int i = half * 128 + row; i < (z1 - z0) * 16; i += 128 * C::kRowSplit) {   // 16 x 16 B per key row
             const int key = z0 + (i >> 4), part = i & 15;
             *reinterpret_cast<uint4*>(sV + (part >> 3) * C::kHalf + key * 128 + (part & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();   // the zeros before the tensor cores read V
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kPFull + sb]);
@@ -802,20 +797,23 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       }
       if (!ok) break;
       // epilogue: out = O / l, one rounding to T; each thread writes its 64 columns
-      const float lsum = l + exchange(l);
-      if (!ok) break;
+      float lsum = l;
+      if (C::kRowSplit > 1) {
+        lsum += exchange(l);
+        if (!ok) break;
+      }
       if (nch > 0 && !wait(kODone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1)) break;
       tc_fence_after();
       {
         const float inv = (valid && lsum > 0.f) ? 1.0f / lsum : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(P.out) +
                                               ((static_cast<int64_t>(v.q0) + tok) * P.hq + h * G + row % G) * D +
-                                              64 * half);
+                                              C::kCols * half);
 #pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
+        for (int cb = 0; cb < C::kCols / 32; ++cb) {
           float o32[32];
           if (nch > 0) {   // uniform over the warp: every lane takes part in the load
-            tmem_ld32(lane_addr + 256 + 64 * half + cb * 32, o32);
+            tmem_ld32(lane_addr + C::kColO + C::kCols * half + cb * 32, o32);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o32[i] = 0.f;
