@@ -546,18 +546,20 @@ def run_pa(args, rank, world, local_rank):
     def step(evs=None):
         for li, (q, kc, vc, nk, nv) in enumerate(layers):
             ev = evs[li] if evs else None
+            rp = li > 0   # the later layers of a step reuse the first layer's plan
             if args.fp8:
                 pa.pa_cache_write_fp8(nk, nv, slots, k_sc, v_sc, kc, vc)
                 pa.pa_decode_fp8(q, kc, vc, k_sc, v_sc, tab, lens, w.scale, max_seq_len=msl,
-                                 out=out, workspace=ws, events=ev)
+                                 out=out, workspace=ws, events=ev, reuse_plan=rp)
                 continue
             pa.pa_cache_write(nk, nv, slots, kc, vc)
             if grouped:
                 pa.pa_decode_grouped(q, kc, vc, tab, lens, w.scale, goff, gpre, max_seq_len=msl,
-                                     out=out, workspace=ws, variant=variant, events=ev)
+                                     out=out, workspace=ws, variant=variant, events=ev,
+                                     reuse_plan=rp)
             else:
                 pa.pa_decode(q, kc, vc, tab, lens, w.scale, max_seq_len=msl, out=out, workspace=ws,
-                             variant=variant, events=ev)
+                             variant=variant, events=ev, reuse_plan=rp)
 
     for _ in range(args.warmup):
         step()
@@ -602,6 +604,11 @@ def run_pa(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     achieved = alg / (kern_avg * 1e-3) / 1e9
 
+    # ---- the same step replayed from a CUDA graph (launch gaps removed) ---------
+    graph = None
+    if args.graph:
+        graph = time_graph(step, args.steps, args.warmup, stream, barrier, dist, dev, kvb, world)
+
     # ---- end to end through the public API, host buffers -------------------------
     e2e = run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped,
                   (k_sc, v_sc) if args.fp8 else None) \
@@ -631,7 +638,8 @@ def run_pa(args, rank, world, local_rank):
                    "unique_kv_bytes_per_step": b.unique_kv_bytes() * nl * kv_elem // 2,
                    "l2": f"inputs larger than L2: {kvb / 1e9:.2f} GB of KV per step vs 129 MB L2; "
                          "no flush",
-                   "step": f"{nl} x (pa_cache_write of one new token per sequence + pa_decode)",
+                   "step": f"{nl} x (pa_cache_write of one new token per sequence + pa_decode)"
+                           + (" (layers after the first reuse its partition plan)" if nl > 1 else ""),
                    "variant": args.variant, "partition_tokens": part_tokens,
                    "shared_prefix": "pa_decode_grouped (prefix read once per group and KV head)"
                                     if grouped else "none (pa_decode)",
@@ -643,13 +651,43 @@ def run_pa(args, rank, world, local_rank):
                      "kernel": "attend_kernel", "kernel_ms": kern_avg,
                      "algorithmic_bytes": alg, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": e2e,
-        "gpu_launches": 4 * nl * args.steps,
+        "graph": graph,
+        # per layer: cache write, attention, merge (+ prefix kernel when grouped);
+        # one prep per step (the later layers reuse its plan)
+        "gpu_launches": ((3 + int(grouped)) * nl + 1) * args.steps,
         "clocks": clocks,
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
+
+
+def time_graph(step, steps, warmup, stream, barrier, dist, dev, units, world):
+    """Capture one step in a CUDA graph and time `steps` replays (the library
+    calls neither synchronise nor allocate, so the whole step is capturable).
+    Returns the step time and the throughput of `units` bytes per step."""
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(max(warmup, 3)):
+        g.replay()
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    a.record(stream)
+    for _ in range(steps):
+        g.replay()
+    z.record(stream)
+    barrier()
+    ms = reduce_max(a.elapsed_time(z) / steps, dist, dev)
+    return {"ms_per_step": ms, "value": job_throughput(units, world, ms * 1e-3) / 1e9,
+            "unit": "GB/s", "how": "one step captured in a CUDA graph, replayed back to back"}
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one attention launch, from
@@ -783,19 +821,20 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped=F
             k_d[li].copy_(k_h[li], non_blocking=True)
             v_d[li].copy_(v_h[li], non_blocking=True)
             kc, vc = caches[li]
+            rp = li > 0   # the later layers of a step reuse the first layer's plan
             if args.fp8:
                 pa.pa_cache_write_fp8(k_d[li], v_d[li], slots_d, k_sc, v_sc, kc, vc)
                 pa.pa_decode_fp8(q_d[li], kc, vc, k_sc, v_sc, table_d, lens_d, w.scale,
-                                 max_seq_len=msl, out=out_d[li], workspace=ws)
+                                 max_seq_len=msl, out=out_d[li], workspace=ws, reuse_plan=rp)
             else:
                 pa.pa_cache_write(k_d[li], v_d[li], slots_d, kc, vc)
                 if grouped:
                     pa.pa_decode_grouped(q_d[li], kc, vc, table_d, lens_d, w.scale, *groups_d,
                                          max_seq_len=msl, out=out_d[li], workspace=ws,
-                                         variant=variant)
+                                         variant=variant, reuse_plan=rp)
                 else:
                     pa.pa_decode(q_d[li], kc, vc, table_d, lens_d, w.scale, max_seq_len=msl,
-                                 out=out_d[li], workspace=ws, variant=variant)
+                                 out=out_d[li], workspace=ws, variant=variant, reuse_plan=rp)
             out_h[li].copy_(out_d[li], non_blocking=True)
         torch.cuda.current_stream().synchronize()
         kv_bytes.append(int(lens_np.astype(np.int64).sum()) * Hkv * D * 2 * (1 if args.fp8 else 2)
@@ -864,6 +903,8 @@ def main():
                     help="E4M3 KV caches: pa_cache_write_fp8 + pa_decode_fp8")
     ap.add_argument("--grouped", action="store_true",
                     help="decode shared-prefix groups with pa_decode_grouped (fullstep)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="skip timing the step replayed from a CUDA graph")
     args = ap.parse_args()
     if args.fp8 and args.grouped:
         ap.error("--fp8 and --grouped do not combine (the shared-prefix kernel reads 16-bit caches)")

@@ -213,11 +213,22 @@ int pa_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int
               void* stream);
 
 /* Options for pa_decode_ex.  Zero-initialised = the pa_decode behaviour. */
+enum {
+    /* Reuse the plan the previous decode on this workspace computed (its
+     * partition list and merge records): the prep kernel is skipped.  The
+     * caller guarantees that seq_lens, block_tables, num_seqs, max_seq_len,
+     * the head counts, head_dim and (for pa_decode_grouped) the groups are
+     * those of that call, and that it completed on this stream or one
+     * ordered after it; q, the caches and out may differ -- e.g. the layers
+     * of one decode step.  Not for pa_prefill. */
+    PA_DECODE_REUSE_PLAN = 1
+};
+
 typedef struct {
     int32_t variant;         /* 0 auto, 1 CUDA-core FMA + warp shuffles, 2 tensor-core
                                 mma.sync, 3 tcgen05 with tensor-memory accumulators
                                 (pa_prefill at head_dim 128 only) */
-    int32_t reserved0;
+    int32_t flags;           /* PA_DECODE_* bits (decode calls only) */
     void* event_before_main; /* optional cudaEvent_t recorded just before the attention */
     void* event_after_main;  /* kernel and just after it, on the same stream */
     int64_t reserved[4];

@@ -35,7 +35,7 @@ class PaStats(ctypes.Structure):
 
 
 class PaDecodeOpts(ctypes.Structure):
-    _fields_ = [("variant", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+    _fields_ = [("variant", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("event_before_main", ctypes.c_void_p), ("event_after_main", ctypes.c_void_p),
                 ("reserved", ctypes.c_int64 * 4)]
 
@@ -43,12 +43,16 @@ class PaDecodeOpts(ctypes.Structure):
 _lib = None
 
 
-def _opts(variant, events, stream):
+PA_DECODE_REUSE_PLAN = 1
+
+
+def _opts(variant, events, stream, flags=0):
     """pa_decode_opts for a call, or None for the defaults."""
-    if not (variant or events):
+    if not (variant or events or flags):
         return None
     o = PaDecodeOpts()
     o.variant = variant
+    o.flags = flags
     if events:
         for e in events:       # torch creates the CUDA event lazily, on first record
             if not e.cuda_event:
@@ -164,14 +168,16 @@ def pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len):
 
 
 def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0, out=None,
-              workspace=None, dtype=None, variant=0, events=None, stream=None):
+              workspace=None, dtype=None, variant=0, events=None, stream=None, reuse_plan=False):
     """out[b, i] = softmax(scale q[b,i] K_b^T) V_b over each sequence's paged K/V.
 
     q [B, Hq, D]; caches [NB, Hkv, 16, D]; block_tables [B, max_blocks] int32;
     seq_lens [B] int32 (device).  Returns out [B, Hq, D].  ``workspace`` is a
     uint8 CUDA tensor of at least pa_decode_workspace_bytes() bytes (one is
     allocated when None).  ``events`` = (before, after) torch.cuda.Event pair
-    recorded around the attention kernel.
+    recorded around the attention kernel.  ``reuse_plan``: skip the prep
+    kernel and reuse the plan of the previous call on this workspace (same
+    lengths, tables and shapes; e.g. the later layers of one step).
     """
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens)
     assert block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
@@ -184,7 +190,9 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0,
     need = pa_decode_workspace_bytes(B, Hq, D, msl)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    opts = _opts(variant, events, stream)
+    if reuse_plan and workspace is None:
+        raise ValueError("reuse_plan needs the workspace of the planning call")
+    opts = _opts(variant, events, stream, PA_DECODE_REUSE_PLAN if reuse_plan else 0)
     rc = lib().pa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), mb,
                             _ptr(seq_lens), B, msl, Hq, Hkv, D, float(scale), _dtype_code(q, dtype),
                             _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream), opts)
@@ -224,9 +232,10 @@ def pa_cache_write_fp8(k, v, slot_mapping, k_scale, v_scale, k_cache8, v_cache8,
 
 
 def pa_decode_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_lens, scale,
-                  max_seq_len=0, out=None, workspace=None, dtype=None, stream=None, events=None):
+                  max_seq_len=0, out=None, workspace=None, dtype=None, stream=None, events=None,
+                  reuse_plan=False):
     """pa_decode over E4M3 caches (see pa_cache_write_fp8 for the layout);
-    ``events`` as for pa_decode."""
+    ``events`` and ``reuse_plan`` as for pa_decode."""
     _need_cuda(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_lens)
     B, Hq, D = q.shape
     NB, Hkv = k_cache8.shape[0], k_cache8.shape[1]
@@ -240,7 +249,8 @@ def pa_decode_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_len
     rc = lib().pa_decode_fp8(_ptr(q), _ptr(k_cache8), _ptr(v_cache8), _ptr(k_scale), _ptr(v_scale), NB,
                              _ptr(block_tables), mb, _ptr(seq_lens), B, msl, Hq, Hkv, D, float(scale),
                              _dtype_code(q, dtype), _ptr(out), _ptr(workspace), workspace.numel(),
-                             _stream(stream), _opts(0, events, stream))
+                             _stream(stream),
+                             _opts(0, events, stream, PA_DECODE_REUSE_PLAN if reuse_plan else 0))
     _check(rc, "pa_decode_fp8")
     return out
 
@@ -251,7 +261,7 @@ def pa_decode_grouped_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_l
 
 def pa_decode_grouped(q, k_cache, v_cache, block_tables, seq_lens, scale, group_offsets,
                       group_prefix_tokens, max_seq_len=0, out=None, workspace=None, dtype=None,
-                      stream=None, variant=0, events=None):
+                      stream=None, variant=0, events=None, reuse_plan=False):
     """pa_decode where contiguous groups of sequences share a prefix:
     group_offsets [G+1] and group_prefix_tokens [G] are int32 CUDA tensors.
     ``events`` bracket the attention kernel over the members' own tokens."""
@@ -271,7 +281,8 @@ def pa_decode_grouped(q, k_cache, v_cache, block_tables, seq_lens, scale, group_
                                  _dtype_code(q, dtype), _ptr(group_offsets),
                                  _ptr(group_prefix_tokens), group_prefix_tokens.numel(), _ptr(out),
                                  _ptr(workspace), workspace.numel(), _stream(stream),
-                                 _opts(variant, events, stream))
+                                 _opts(variant, events, stream,
+                                       PA_DECODE_REUSE_PLAN if reuse_plan else 0))
     _check(rc, "pa_decode_grouped")
     return out
 

@@ -146,6 +146,8 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_decode: scale is not finite");
   if (opts && (opts->variant < 0 || opts->variant > 2))
     return fail(PA_ERR_INVALID, "pa_decode: opts->variant must be 0, 1 or 2");
+  if (opts && (opts->flags & ~PA_DECODE_REUSE_PLAN))
+    return fail(PA_ERR_INVALID, "pa_decode: unknown opts->flags bits");
   if (num_seqs == 0) return PA_OK;
   const int64_t per_seq_parts = (max_seq_len + pa::kPartTokens - 1) / pa::kPartTokens;
   if (static_cast<int64_t>(num_seqs) * per_seq_parts * num_kv_heads > INT32_MAX)
@@ -188,6 +190,7 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
   a.variant = opts ? opts->variant : 0;
   a.ev_before = opts ? opts->event_before_main : nullptr;
   a.ev_after = opts ? opts->event_after_main : nullptr;
+  a.reuse_plan = opts && (opts->flags & PA_DECODE_REUSE_PLAN);
   a.group_off = d_group_offsets;
   a.group_prefix = d_group_prefix_tokens;
   a.num_groups = num_groups;
@@ -297,6 +300,8 @@ int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, in
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_prefill: scale is not finite");
   if (opts && opts->variant != 0 && opts->variant != 2 && opts->variant != 3)
     return fail(PA_ERR_UNSUPPORTED, "pa_prefill: variant must be 0 (auto), 2 (mma.sync) or 3 (tcgen05)");
+  if (opts && opts->flags != 0)
+    return fail(PA_ERR_INVALID, "pa_prefill: opts->flags must be 0");
   if (opts && opts->variant == 3 && head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "pa_prefill: the tcgen05 variant needs head_dim 128");
   if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;

@@ -271,10 +271,6 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
       if (nparts > 1 || sp.z > 0)
         P.split[atomicAdd(&s_nsplit, 1)] =
             MergeInfo{b, first, tail_idx, nfull, nfull + (r != 0), sp.x, sp.y, sp.z};
-      if (L == 0) {  // empty softmax: the output is defined as 0
-        uint4* o = reinterpret_cast<uint4*>(P.out) + static_cast<int64_t>(b) * row_uint4;
-        for (int i = 0; i < row_uint4; ++i) o[i] = make_uint4(0, 0, 0, 0);
-      }
     }
     carry_full += tot_f;
   }
@@ -991,6 +987,17 @@ __global__ void __launch_bounds__(kMergeThreads, 1024 / kMergeThreads) merge_ker
   const int n4 = G * D / 4;
   const int t = threadIdx.x;
   const float4* acc4 = reinterpret_cast<const float4*>(P.acc);
+  // the attention kernel has finished: its work counter is reset here, so
+  // that a later call may reuse this workspace's plan without the prep kernel
+  if (blockIdx.x == 0 && t == 0) P.ws->next_item = 0;
+  // the empty softmax of a zero-length sequence: its output is defined as 0
+  for (int b = blockIdx.x * kMergeThreads + t; b < P.num_seqs; b += gridDim.x * kMergeThreads) {
+    int L = P.seq_lens[b];
+    if (L <= 0) {
+      uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(P.out) + static_cast<int64_t>(b) * P.hq * D);
+      for (int i = 0; i < P.hq * D * 2 / 16; ++i) o[i] = make_uint4(0, 0, 0, 0);
+    }
+  }
   for (int wi = blockIdx.x; wi < n_work; wi += gridDim.x) {
     const MergeInfo mi = P.split[wi / P.hkv];
     const int h = wi - (wi / P.hkv) * P.hkv;
@@ -1479,11 +1486,15 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   cudaGetDevice(&dev0);
   cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev0);
   // 8 full-partition items per attention CTA (two CTAs per SM)
-  prep_kernel<<<1, 1024, 0, s>>>(P, row_uint4, 16 * n_sm);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) {
-    *why = std::string("prep launch: ") + cudaGetErrorString(e);
-    return 5;
+  // the plan (partition list, merge records, counters) depends only on the
+  // lengths, tables and shapes: a caller may reuse the workspace's plan
+  if (!a.reuse_plan) {
+    prep_kernel<<<1, 1024, 0, s>>>(P, row_uint4, 16 * n_sm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      *why = std::string("prep launch: ") + cudaGetErrorString(e);
+      return 5;
+    }
   }
   if (grouped) {
     // The prefix kernel moves little data and is mostly latency: it runs on a
@@ -1548,7 +1559,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
       merge_kernel<__half, 64, 128><<<mg, 128, 0, s>>>(P);
     }
   }
-  e = cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("merge launch: ") + cudaGetErrorString(e);
     return 5;

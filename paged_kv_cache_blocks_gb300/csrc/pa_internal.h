@@ -38,6 +38,7 @@ struct DecodeArgs {
   bool fp8 = false;                       // E4M3 caches (K token-major, V dim-major)
   const float* k_scale = nullptr;         // [num_kv_heads] (device), FP8 only
   const float* v_scale = nullptr;
+  bool reuse_plan = false;                // skip the prep kernel: the workspace holds the plan
 };
 
 // Both return 0 on success or a pa_status code, with *why set on failure.

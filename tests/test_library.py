@@ -114,3 +114,13 @@ def test_prefill_empty_is_a_noop_and_workspace_sizes(L):
     assert b > a > 0
     assert b - a >= (100000 - 1000) // 16 * 16 - 256
     assert L.pa_prefill_workspace_bytes(4, 100, 6, 4) == 0
+
+
+def test_decode_rejects_unknown_flags(L):
+    from paged_kv_cache_blocks_gb300 import binding as b
+    o = b.PaDecodeOpts()
+    o.flags = 2
+    assert L.pa_decode_ex(*_decode_args(), ctypes.byref(o)) == 1
+    assert b"flags" in L.pa_last_error_string()
+    o.flags = 1
+    assert L.pa_prefill(*_prefill_args(opts=ctypes.byref(o))) == 1
