@@ -770,10 +770,12 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped=F
                 append(i, ids[i], lens0[i])
     ids_c = ids.ctypes.data_as(ctypes.c_void_p)
     g = torch.Generator().manual_seed(99)
+    # step inputs in pinned host memory (q/k/v per layer; metadata rewritten by
+    # the allocator every step) and the step's outputs, read back every step
     q_h = [torch.randn((B, Hq, D), generator=g).to(dt).pin_memory() for _ in range(nl)]
     k_h = [torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory() for _ in range(nl)]
     v_h = [torch.randn((B, Hkv, D), generator=g).to(dt).pin_memory() for _ in range(nl)]
-    out_h = [torch.empty((B, Hq, D), dtype=dt).pin_memory() for _ in range(nl)]
+    out_h = [[torch.empty((B, Hq, D), dtype=dt).pin_memory() for _ in range(nl)] for _ in range(2)]
     slots_h = torch.empty(B, dtype=torch.int64).pin_memory()
     if args.fp8:   # K token-major, V dimension-major bytes
         caches = [(torch.zeros((nb, Hkv, 16, D), dtype=torch.uint8, device=dev),
@@ -782,19 +784,28 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped=F
     else:
         caches = [(torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev),
                    torch.zeros((nb, Hkv, 16, D), dtype=dt, device=dev)) for _ in range(nl)]
-    q_d = [torch.empty((B, Hq, D), dtype=dt, device=dev) for _ in range(nl)]
-    k_d = [torch.empty((B, Hkv, D), dtype=dt, device=dev) for _ in range(nl)]
-    v_d = [torch.empty((B, Hkv, D), dtype=dt, device=dev) for _ in range(nl)]
-    out_d = [torch.empty((B, Hq, D), dtype=dt, device=dev) for _ in range(nl)]
-    slots_d = torch.empty(B, dtype=torch.int64, device=dev)
-    table_d = torch.empty((B, mb), dtype=torch.int32, device=dev)
-    lens_d = torch.empty(B, dtype=torch.int32, device=dev)
-    msl = mb * 16
     meta_h = [slots_h, table_h, lens_h]
     if grouped:
-        groups_h = [torch.from_numpy(x).pin_memory() for x in b.group_arrays()]
-        groups_d = [torch.empty_like(x, device=dev) for x in groups_h]
-        meta_h += groups_h
+        meta_h += [torch.from_numpy(x).pin_memory() for x in b.group_arrays()]
+    msl = mb * 16
+
+    # two device slots: step i uses slot i % 2, so that the copies of step i
+    # overlap the compute of step i - 1
+    class Slot:
+        pass
+    slots = []
+    for _ in range(2):
+        sl = Slot()
+        sl.q = [torch.empty((B, Hq, D), dtype=dt, device=dev) for _ in range(nl)]
+        sl.k = [torch.empty((B, Hkv, D), dtype=dt, device=dev) for _ in range(nl)]
+        sl.v = [torch.empty((B, Hkv, D), dtype=dt, device=dev) for _ in range(nl)]
+        sl.out = [torch.empty((B, Hq, D), dtype=dt, device=dev) for _ in range(nl)]
+        sl.meta = [torch.empty_like(x, device=dev) for x in meta_h]
+        sl.meta_copied = torch.cuda.Event()
+        sl.inputs_ready = torch.cuda.Event()
+        sl.comp_done = torch.cuda.Event()
+        slots.append(sl)
+    if grouped:
         ws = torch.empty(pa.pa_decode_grouped_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8,
                          device=dev)
     else:
@@ -802,62 +813,80 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped=F
     slots_np, table_np, lens_np = slots_h.numpy(), table_h.numpy(), lens_h.numpy()
     nbytes = lambda t: t.numel() * t.element_size()
     h2d = sum(nbytes(t) for t in q_h + k_h + v_h) + sum(nbytes(t) for t in meta_h)
-    d2h = sum(nbytes(t) for t in out_h)
+    d2h = sum(nbytes(t) for t in out_h[0])
     kv_bytes = []
+    compute = torch.cuda.current_stream()
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    state = {"i": 0}
 
     def one_step():
+        i = state["i"]
+        sl = slots[i & 1]
+        if i >= 1:   # the pinned metadata is free once the previous step's copy ran
+            slots[(i - 1) & 1].meta_copied.synchronize()
         rc = pa.lib().pa_seq_append_slots(alloc._h, ids_c, B, 1, slots_np.ctypes.data, None, None,
                                           0, None, table_np.ctypes.data, mb, lens_np.ctypes.data)
         if rc != 0:
             raise RuntimeError(pa.lib().pa_last_error_string().decode())
-        slots_d.copy_(slots_h, non_blocking=True)
-        table_d.copy_(table_h, non_blocking=True)
-        lens_d.copy_(lens_h, non_blocking=True)
-        if grouped:
-            for hx, dx in zip(groups_h, groups_d):
+        with torch.cuda.stream(h2d_stream):
+            if i >= 2:   # this slot's buffers are free once step i - 2 computed
+                h2d_stream.wait_event(sl.comp_done)
+            for hx, dx in zip(meta_h, sl.meta):
                 dx.copy_(hx, non_blocking=True)
+            sl.meta_copied.record(h2d_stream)
+            for li in range(nl):
+                sl.q[li].copy_(q_h[li], non_blocking=True)
+                sl.k[li].copy_(k_h[li], non_blocking=True)
+                sl.v[li].copy_(v_h[li], non_blocking=True)
+            sl.inputs_ready.record(h2d_stream)
+        compute.wait_event(sl.inputs_ready)
+        slots_d, table_d, lens_d = sl.meta[0], sl.meta[1], sl.meta[2]
         for li in range(nl):
-            q_d[li].copy_(q_h[li], non_blocking=True)
-            k_d[li].copy_(k_h[li], non_blocking=True)
-            v_d[li].copy_(v_h[li], non_blocking=True)
             kc, vc = caches[li]
             rp = li > 0   # the later layers of a step reuse the first layer's plan
             if args.fp8:
-                pa.pa_cache_write_fp8(k_d[li], v_d[li], slots_d, k_sc, v_sc, kc, vc)
-                pa.pa_decode_fp8(q_d[li], kc, vc, k_sc, v_sc, table_d, lens_d, w.scale,
-                                 max_seq_len=msl, out=out_d[li], workspace=ws, reuse_plan=rp)
+                pa.pa_cache_write_fp8(sl.k[li], sl.v[li], slots_d, k_sc, v_sc, kc, vc)
+                pa.pa_decode_fp8(sl.q[li], kc, vc, k_sc, v_sc, table_d, lens_d, w.scale,
+                                 max_seq_len=msl, out=sl.out[li], workspace=ws, reuse_plan=rp)
             else:
-                pa.pa_cache_write(k_d[li], v_d[li], slots_d, kc, vc)
+                pa.pa_cache_write(sl.k[li], sl.v[li], slots_d, kc, vc)
                 if grouped:
-                    pa.pa_decode_grouped(q_d[li], kc, vc, table_d, lens_d, w.scale, *groups_d,
-                                         max_seq_len=msl, out=out_d[li], workspace=ws,
+                    pa.pa_decode_grouped(sl.q[li], kc, vc, table_d, lens_d, w.scale, *sl.meta[3:5],
+                                         max_seq_len=msl, out=sl.out[li], workspace=ws,
                                          variant=variant, reuse_plan=rp)
                 else:
-                    pa.pa_decode(q_d[li], kc, vc, table_d, lens_d, w.scale, max_seq_len=msl,
-                                 out=out_d[li], workspace=ws, variant=variant, reuse_plan=rp)
-            out_h[li].copy_(out_d[li], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+                    pa.pa_decode(sl.q[li], kc, vc, table_d, lens_d, w.scale, max_seq_len=msl,
+                                 out=sl.out[li], workspace=ws, variant=variant, reuse_plan=rp)
+        sl.comp_done.record(compute)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(sl.comp_done)
+            for li in range(nl):
+                out_h[i & 1][li].copy_(sl.out[li], non_blocking=True)
         kv_bytes.append(int(lens_np.astype(np.int64).sum()) * Hkv * D * 2 * (1 if args.fp8 else 2)
                         * nl)
+        state["i"] = i + 1
 
     for _ in range(args.warmup):
         one_step()
+    torch.cuda.synchronize()
     kv_bytes.clear()
     barrier()
     t0 = time.perf_counter()
     for _ in range(steps):
         one_step()
+    torch.cuda.synchronize()
     barrier()
     sec = reduce_max((time.perf_counter() - t0) / steps, dist, dev)
     alloc.close()
     return {"value": job_throughput(statistics.fmean(kv_bytes), world, sec) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": sec * 1e3,
-            "path": "host allocator append_slots -> H2D (pinned) slots,table,lens"
+            "path": "per step: host allocator append_slots -> H2D (pinned, copy stream) slots,table,lens"
                     + (",group offsets/prefixes" if grouped else "") + " and per layer q,k,v -> "
                     + ("pa_cache_write_fp8 -> pa_decode_fp8" if args.fp8 else
                        "pa_cache_write -> " + ("pa_decode_grouped" if grouped else "pa_decode"))
-                    + " -> D2H out, then sync"}
+                    + " -> D2H out (second copy stream); two device slots let step i's copies "
+                      "overlap step i-1's compute; synchronised after the last step"}
 
 
 def run_reference_prefill(args, rank, world):
