@@ -357,6 +357,16 @@ int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, in
 int pa_decode_check(const void* d_workspace, void* stream, int32_t* error_bits);
 
 /* ------------------------------------------------------------------------
+ * Diagnostic with no counterpart on the pages: the bounded wait that every
+ * kernel of this library uses on its mbarriers, shown to end.  One CTA waits
+ * on a barrier nothing arrives at; after limit_ns (0 < limit_ns <= 1e9) the
+ * wait gives up and the kernel returns normally, writing to d_status[0..3]
+ * (int32, device): whether the wait succeeded (0 expected), the error bits
+ * (PA_DEVERR_TIMEOUT expected), the CTA's abort flag (1 expected) and the
+ * microseconds waited.  Asynchronous on `stream`. */
+int pa_selftest_bounded_wait(int64_t limit_ns, int32_t* d_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * Decode without any allocation.  The pages have no counterpart: this is a
  * convenience for callers that cannot allocate device memory or pass a
  * workspace (a fixed, pre-planned memory budget, a plugin or callback that

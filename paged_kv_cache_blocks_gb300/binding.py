@@ -89,6 +89,7 @@ _SIGS = {
                            P, SZ, P, P], ctypes.c_int),
     "pa_decode_noalloc": ([P, P, P, I64, P, I32, P, I32, I32, I32, I32, I32, F32, I32, P, P],
                           ctypes.c_int),
+    "pa_selftest_bounded_wait": ([I64, P, P], ctypes.c_int),
     "pa_prefill_workspace_bytes": ([I32, I32, I32, I32], SZ),
     "pa_prefill": ([P, P, P, I64, P, I32, P, P, I32, I32, I32, I32, I32, I32, F32, I32, P, P, SZ, P,
                     P], ctypes.c_int),
@@ -323,6 +324,16 @@ def pa_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_offsets, scale, ma
                           _stream(stream), _opts(variant, events, stream))
     _check(rc, "pa_prefill")
     return out
+
+
+def pa_selftest_bounded_wait(limit_ns, stream=None):
+    """Run the bounded-wait diagnostic; returns (wait succeeded, error bits,
+    abort flag, microseconds waited) once it has finished."""
+    status = torch.full((4,), -1, dtype=torch.int32, device="cuda")
+    _check(lib().pa_selftest_bounded_wait(int(limit_ns), _ptr(status), _stream(stream)),
+           "pa_selftest_bounded_wait")
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    return tuple(int(x) for x in status.cpu().tolist())
 
 
 def pa_decode_check(workspace, stream=None):

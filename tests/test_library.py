@@ -124,3 +124,10 @@ def test_decode_rejects_unknown_flags(L):
     assert b"flags" in L.pa_last_error_string()
     o.flags = 1
     assert L.pa_prefill(*_prefill_args(opts=ctypes.byref(o))) == 1
+
+
+def test_selftest_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    assert L.pa_selftest_bounded_wait(0, P(1 << 20), None) == 1
+    assert L.pa_selftest_bounded_wait(2_000_000_000, P(1 << 20), None) == 1
+    assert L.pa_selftest_bounded_wait(1000, P(0), None) == 1
