@@ -229,8 +229,14 @@ def cpu_baseline(workload, budget_s=12.0):
         rows = oracle_sample_rows(lens_all, n_long)
         t1, lens, _ = time_oracle(workload, rows, threads)
     kvb = logical_kv_bytes(lens, w.num_kv_heads, w.head_dim)
+    # one thread, on the first long and the first short sequence of the sample
+    rows1 = oracle_sample_rows(lens_all, 1)[:2]
+    t_one, lens_one, _ = time_oracle(workload, rows1, 1)
+    one = logical_kv_bytes(lens_one, w.num_kv_heads, w.head_dim) / t_one / 1e9
     return {"value": kvb / t1 / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "seconds": t1, "seqs_steps_per_s": len(lens) / t1,
+            "single_thread_value": one,
+            "single_thread_sample": f"{len(lens_one)} sequences ({int(np.sum(lens_one))} tokens), 1 thread",
             "sample": f"{len(lens)} of the {len(lens_all)} sequences of the same workload "
                       f"({int((np.asarray(lens) > 10 * np.median(lens_all)).sum())} long, same "
                       f"length draw), {int(np.sum(lens))} tokens, one decode step, fp64, "
@@ -601,6 +607,7 @@ def run_pa(args, rank, world, local_rank):
     alg = algorithmic_bytes(b.seq_lens, Hq, Hkv, D, part_tokens=part_tokens, kv_elem=kv_elem,
                             starts=starts)
     kern_avg = statistics.fmean(kern_ms)
+    kq = np.percentile(np.asarray(kern_ms), [10, 50, 90]) if kern_ms else [float("nan")] * 3
     peak, peak_kind = measured_peaks()
     achieved = alg / (kern_avg * 1e-3) / 1e9
 
@@ -649,6 +656,7 @@ def run_pa(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "attend_kernel", "kernel_ms": kern_avg,
+                     "kernel_ms_p10_p50_p90": [float(x) for x in kq],
                      "algorithmic_bytes": alg, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": e2e,
         "graph": graph,
