@@ -16,7 +16,8 @@
 //                            token x one of the G heads of a KV head) and
 //                            lists them in the workspace by descending number
 //                            of key blocks (longest first);
-//   2. prefill (persistent, one CTA per SM)
+//   2. prefill_tc (head_dim 128, tcgen05; described below) or prefill
+//      (mma.sync; persistent, one CTA per SM)
 //                            one work item = (KV head, tile), taken from an
 //                            atomic counter, KV-head-major so that the CTAs
 //                            running together share their K/V in L2.  Warp NW
@@ -384,25 +385,29 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
 
 // ---------------------------------------------------------------------------
 // tcgen05 version (head_dim 128).  One work item = (KV head, tile of 128 query
-// rows) as above.  Per CTA (one per SM, 6 warps):
-//   warp 0     takes items from the atomic counter and publishes them in a
-//              two-slot item ring; TMA-loads the tile's Q (128 rows x 128,
-//              a 3-D box of tokens x heads x dims) and the key blocks in
-//              chunks of 8 blocks = 128 keys into a two-stage ring (K and V
-//              of a chunk laid out as 128 swizzled rows per 64-dim half, so
-//              one descriptor spans the whole chunk);
-//   warp 1     allocates 512 tensor-memory columns and, one thread, issues
-//              S = Q K^T (M 128, N 128 keys, K 128 dims) into one of two
-//              S buffers for chunk c+1 while the softmax of chunk c runs, then
-//              O += P V (M 128, N 128 dims, K 128 keys) from P in shared
-//              memory; tcgen05.commit signals each result on an mbarrier;
-//   warps 2-5  one query row per thread (its tensor-memory lane): read S,
-//              apply the scale and the causal mask, online softmax in fp32 with
-//              the running maximum moved only when it grows by more than 2^8
-//              (the exact result either way, fewer rescales of O), write P as
-//              16-bit into shared memory in the operand layout, rescale O in
-//              tensor memory when the maximum moved, and finally write
-//              O / l.
+// rows) as above.  Per CTA (one per SM, 9 warps):
+//   warps 0-3  producers: warp 0 takes items from the atomic counter,
+//              publishes them in a two-slot item ring and TMA-loads the
+//              tile's Q (128 rows x 128 dims, one 3-D box of tokens x heads x
+//              dims); all four load the key blocks in chunks of 8 blocks =
+//              128 keys (K one chunk ahead of V) into three-stage K and V
+//              rings, each warp issuing the copies of two blocks (K and V of
+//              a chunk are 128 swizzled rows per 64-dim half, so one
+//              descriptor spans the chunk).  TMA issue from one warp is too
+//              slow for a chunk;
+//   warp 4     allocates the 512 tensor-memory columns (S0 | S1 | O | P0 |
+//              P1) and, one thread, issues S = Q K^T (M 128, N 128 keys, K
+//              128 dims) into one of two S buffers for chunk c+1 while the
+//              softmax of chunk c runs, then O += P V (M 128, N 128 dims, K
+//              128 keys) with P read from tensor memory; tcgen05.commit
+//              signals each result on an mbarrier;
+//   warps 5-8  one query row per thread (its tensor-memory lane): read S,
+//              apply the scale and the causal mask, online softmax in fp32
+//              with the running maximum moved only when it grows by more
+//              than 2^8 (the exact result either way, fewer rescales of O),
+//              write P as 16-bit values, two per column, into one of two P
+//              buffers in tensor memory, rescale O when the maximum moved,
+//              and finally write O / l.
 // Every wait is bounded; a timeout flags PA_DEVERR_TIMEOUT and the CTA
 // drains its copies and tensor-core work before freeing tensor memory.
 
