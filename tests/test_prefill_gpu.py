@@ -172,3 +172,20 @@ def test_prefill_flags_bad_input_without_faulting(pa):
                          pb.q_offsets, w.scale, w.dtype)
     U.assert_close_rounded(out[10:].double().cpu().numpy(), ref[10:], "bf16",
                            "rows after a bad block id")
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+@pytest.mark.parametrize("hq", [8, 16])
+def test_prefill_head_dim_128_small_groups(pa, hq, variant):
+    """G = 1 (Q box of 128 tokens x 1 head) and G = 2 (64 tokens x 2 heads) at
+    head_dim 128, where the tcgen05 kernel applies."""
+    import dataclasses
+    name = f"g{hq // 8}d128"
+    W.WORKLOADS[name] = dataclasses.replace(W.WORKLOADS["llama8b"], name=name, num_q_heads=hq)
+    W._SEED_SALT[name] = 80 + hq
+    try:
+        pb = W.make_prefill_batch(name, seed=4, lens=[400, 129, 1000, 7], pieces=[300, 129, 2, 7])
+        got, ref, _ = run(pa, pb, variant=variant)
+        U.assert_close_rounded(got, ref, "bf16", f"prefill G={hq // 8} d128 variant {variant}")
+    finally:
+        del W.WORKLOADS[name], W._SEED_SALT[name]
