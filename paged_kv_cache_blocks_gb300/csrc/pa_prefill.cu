@@ -385,29 +385,36 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
 
 // ---------------------------------------------------------------------------
 // tcgen05 version (head_dim 128).  One work item = (KV head, tile of 128 query
-// rows) as above.  Per CTA (one per SM, 9 warps):
-//   warps 0-3  producers: warp 0 takes items from the atomic counter,
+// rows) as above.  Per CTA (one per SM, 10 warps):
+//   warps 4-7  producers: warp 4 takes items from the atomic counter,
 //              publishes them in a two-slot item ring and TMA-loads the
 //              tile's Q (128 rows x 128 dims, one 3-D box of tokens x heads x
-//              dims); all four load the key blocks in chunks of 8 blocks =
-//              128 keys (K one chunk ahead of V) into three-stage K and V
-//              rings, each warp issuing the copies of two blocks (K and V of
-//              a chunk are 128 swizzled rows per 64-dim half, so one
-//              descriptor spans the chunk).  TMA issue from one warp is too
-//              slow for a chunk;
-//   warp 4     allocates the 512 tensor-memory columns (S0 | S1 | O | P0 |
-//              P1) and, one thread, issues S = Q K^T (M 128, N 128 keys, K
-//              128 dims) into one of two S buffers for chunk c+1 while the
-//              softmax of chunk c runs, then O += P V (M 128, N 128 dims, K
-//              128 keys) with P read from tensor memory; tcgen05.commit
-//              signals each result on an mbarrier;
-//   warps 5-8  one query row per thread (its tensor-memory lane): read S,
-//              apply the scale and the causal mask, online softmax in fp32
-//              with the running maximum moved only when it grows by more
-//              than 2^8 (the exact result either way, fewer rescales of O),
-//              write P as 16-bit values, two per column, into one of two P
-//              buffers in tensor memory, rescale O when the maximum moved,
-//              and finally write O / l.
+//              dims) into shared memory; all four load the key blocks in
+//              chunks of 8 blocks = 128 keys (K one chunk ahead of V) into
+//              three-stage K and V rings, each warp issuing the copies of two
+//              blocks (K and V of a chunk are 128 swizzled rows per 64-dim
+//              half, so one descriptor spans the chunk).  TMA issue from one
+//              warp is too slow for a chunk;
+//   warp 8     allocates the tensor memory (S | P0 | P1 | O | Q); one
+//              thread issues S = Q K^T (M 128, N 128 keys, K 128 dims) for
+//              chunk c+1 as soon as the softmax of chunk c has read S;
+//   warp 9     one thread issues O += P V (M 128, N 128 dims, K 128 keys)
+//              once the softmax has written P.  Issuing a product blocks the
+//              thread about as long as the product runs, hence two issuers.
+//              Both products take their A
+//              operand (Q, P) from tensor memory, which runs them at the full
+//              rate where an A operand in shared memory halves it;
+//              tcgen05.commit signals each result on an mbarrier;
+//   warps 0-3  one query row per thread (its tensor-memory lane): at the
+//              start of an item, move the row of Q from shared to tensor
+//              memory; per chunk read S, apply the scale and the causal mask,
+//              online softmax in fp32 with the running maximum moved only
+//              when it grows by more than 2^8 (the exact result either way,
+//              fewer rescales of O), write P as 16-bit values, two per
+//              column, into one of two P buffers, rescale O when the maximum
+//              moved, and finally write O / l.
+// The softmax warpgroup holds 128 scores per thread: it takes registers the
+// producer warpgroup gives back (setmaxnreg), so that nothing spills.
 // Every wait is bounded; a timeout flags PA_DEVERR_TIMEOUT and the CTA
 // drains its copies and tensor-core work before freeing tensor memory.
 
@@ -422,30 +429,36 @@ struct TcCfg {
   static constexpr size_t kOffK = kOffQ + kQBytes;
   static constexpr size_t kOffV = kOffK + static_cast<size_t>(kKStages) * kChunkBytes;
   static constexpr size_t kOffBar = kOffV + static_cast<size_t>(kVStages) * kChunkBytes;
-  static constexpr size_t kOffX = kOffBar + 512;     // row maxima / sums exchanged by warp pairs
-  static constexpr size_t kBytes = kOffX + 2 * 128 * 4 + 1024;
+  static constexpr size_t kBytes = kOffBar + 512 + 1024;
+  static constexpr int kSoftmaxWarps = 4;            // warpgroup 0
+  static constexpr int kProducerWarp0 = 4;           // warpgroup 1
   static constexpr int kProducerWarps = 4;           // one per SM sub-partition: TMA issue
                                                      // from one warp is too slow for a chunk
-  static constexpr int kMmaWarp = kProducerWarps;
-  static constexpr int kSoftmaxWarp0 = kMmaWarp + 1;
-  static constexpr int kRowSplit = 1;                // softmax threads per row
-  static constexpr int kSoftmaxWarps = 4 * kRowSplit;
-  static constexpr int kCols = 128 / kRowSplit;      // S columns per softmax thread
-  static constexpr int kThreads = 32 * (kSoftmaxWarp0 + kSoftmaxWarps);
-  // tensor memory: S0 | S1 | O (128 fp32 columns each) | P0 | P1 (128 16-bit
-  // values per row packed into 64 columns each)
+  static constexpr int kMmaWarp = 8;                 // warps 8 (S) and 9 (PV)
+  static constexpr int kMmaWarps = 2;
+  static constexpr int kThreads = 32 * (kMmaWarp + kMmaWarps);
+  // registers per thread: 168 at launch (three warps on one sub-partition);
+  // the producers drop to 80 and the softmax threads rise to 240:
+  // 128 x 240 + 128 x 80 + 64 x 168 = 51712 <= 320 x 168 = 53760
+  static constexpr int kRegsLaunch = 168, kRegsProducer = 80, kRegsSoftmax = 240;
+  // tensor memory: S (128 fp32 columns) | P0 | P1 (128 16-bit values per row
+  // packed into 64 columns each) | O (128 fp32 columns) | Q (128 16-bit
+  // values per row in 64 columns); 448 of the 512 allocated columns
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256, kColP = 384;
+  static constexpr uint32_t kColS = 0, kColP = 128, kColO = 256, kColQ = 384;
 };
 static_assert(TcCfg::kBytes <= 232448, "shared memory of one CTA");
+static_assert(TcCfg::kColQ + 64 <= TcCfg::kTmemCols, "tensor-memory columns");
+static_assert(32 * (TcCfg::kSoftmaxWarps * TcCfg::kRegsSoftmax + TcCfg::kProducerWarps * TcCfg::kRegsProducer +
+                    TcCfg::kMmaWarps * TcCfg::kRegsLaunch) <= TcCfg::kThreads * TcCfg::kRegsLaunch,
+              "register split within the registers the CTA is launched with");
 
-// Barrier indices; every ring of two has one barrier per slot, so that a
-// parity wait never meets a phase two uses ahead.
+// Barrier indices; every ring of n slots has one barrier per slot, so that a
+// parity wait never meets a phase n uses ahead.
 enum TcBar {
-  kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9, kSFull = 12, kSFree = 14, kPFull = 16,
-  kODone = 18, kQFull = 20, kQEmpty = 21, kItemFull = 22, kItemEmpty = 24, kDrain = 26,
-  kXFull = 27, kXFree = 31,   // per tensor-memory quarter: the two softmax warps of a row
-  kNumTcBars = 35
+  kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9, kSFull = 12, kSFree = 13, kPFull = 14,
+  kODone = 16, kQFull = 18, kQTmem = 19, kItemFull = 20, kItemEmpty = 22, kDrain = 24,
+  kNumTcBars = 25
 };
 static_assert(kNumTcBars * 8 + 16 <= 512, "barrier region");
 
@@ -475,25 +488,22 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       mbar_init(&bar[kVFull + i], C::kProducerWarps);
       mbar_init(&bar[kVEmpty + i], 1);
     }
+    mbar_init(&bar[kSFull], 1);
+    mbar_init(&bar[kSFree], C::kSoftmaxWarps);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[kSFull + i], 1);
-      mbar_init(&bar[kSFree + i], C::kSoftmaxWarps);
       mbar_init(&bar[kPFull + i], C::kSoftmaxWarps);
       mbar_init(&bar[kODone + i], 1);
       mbar_init(&bar[kItemFull + i], 1);
-      mbar_init(&bar[kItemEmpty + i], C::kProducerWarps + C::kSoftmaxWarps);   // helpers, MMA, softmax
-    }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&bar[kXFull + i], C::kRowSplit);
-      mbar_init(&bar[kXFree + i], C::kRowSplit);
+      // helpers (3), MMA issuers (2), softmax (4)
+      mbar_init(&bar[kItemEmpty + i], C::kProducerWarps - 1 + C::kMmaWarps + C::kSoftmaxWarps);
     }
     mbar_init(&bar[kQFull], 1);
-    mbar_init(&bar[kQEmpty], 1);
-    mbar_init(&bar[kDrain], 1);
+    mbar_init(&bar[kQTmem], C::kSoftmaxWarps);
+    mbar_init(&bar[kDrain], C::kMmaWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == C::kProducerWarp0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -506,14 +516,15 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
   const int n_entries = *reinterpret_cast<volatile int32_t*>(&P.ws->n_entries);
   const int n_work = n_entries * P.hkv;
 
-  if (warp < C::kProducerWarps) {
+  if (warp >= C::kProducerWarp0 && warp < C::kMmaWarp) {
     // ------------------------------------------------------------ producers
-    // Warp 0 takes items from the atomic counter and publishes them; all
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kRegsProducer));
+    // Warp 4 takes items from the atomic counter and publishes them; all
     // four producer warps read block ids 32 at a time (one coalesced load)
     // and each issues the copies of blocks p and p + 4 of every chunk
     // (lanes 0..3: block p / p + 4, dims 0-63 / 64-127), arming the stage
     // barrier for its own 8 KB.
-    const int pw = warp;
+    const int pw = warp - C::kProducerWarp0;
     const int64_t y_oob = P.num_blocks * P.hkv * kBlock;
     uint32_t it = 0, cc = 0;
     bool ok = true;
@@ -547,8 +558,9 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       const int4 ent = P.entries[wi - h * n_entries];
       const int b = ent.x, tile = ent.y, nkb = ent.z;
       if (pw == 0) {
+        // the softmax warps moved the previous item's Q into tensor memory
         const PieceView v = piece_view(P, b, false);
-        if (it >= 1 && !wait(kQEmpty, (it - 1) & 1)) break;
+        if (it >= 1 && !wait(kQTmem, (it - 1) & 1)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&bar[kQFull], C::kQBytes);
           const int z = v.q0 + tile * P.tile_tokens;
@@ -598,15 +610,19 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       cc += nch;
       ++it;
     }
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // lane 0 of warp 8 issues the S products, lane 0 of warp 9 the PV
+    // products: issuing blocks a thread about as long as the product runs,
+    // so with one issuer its waits and commits sat between the products;
+    // with two, each one's bookkeeping overlaps the other's products
     if (lane == 0) {
+      const bool pv_role = warp == C::kMmaWarp + 1;
       constexpr int kBf = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
       constexpr uint32_t id_s = umma_idesc_f16(kBf, 0, 128, 128);
       constexpr uint32_t id_o = umma_idesc_f16(kBf, 1, 128, 128);
-      // descriptors of the operand buffers; an MMA's operand is the base plus
-      // a constant byte offset (>> 4 in the start-address field)
-      const uint64_t dQ = umma_desc_sw128(smem_u32(sQ), 16, 1024);
+      // shared-memory descriptors of the K and V rings; an MMA's operand is
+      // the base plus a constant byte offset (>> 4 in the start-address field)
       const uint64_t dK0 = umma_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
       // V is MN-major (dims contiguous): one N = 128 product spans its two
       // 64-dim atoms, C::kHalf bytes apart (the leading byte offset); one
@@ -618,20 +634,6 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         if (ok) ok = mbar_wait(&bar[idx], parity, abort_flag, err);
         return ok;
       };
-      auto issue_s = [&](uint32_t x) {
-        const int kst = x % C::kKStages, sb = x & 1;
-        if (!wait(kKFull + kst, (x / C::kKStages) & 1)) return;
-        if (x >= 2 && !wait(kSFree + sb, ((x >> 1) - 1) & 1)) return;
-        tc_fence_after();
-        const uint64_t dK = dK0 + (static_cast<uint64_t>(kst) * C::kChunkBytes >> 4);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = ((ks >> 2) * C::kHalf + (ks & 3) * 32) >> 4;
-          umma_f16_ss(tbase + sb * 128, dQ + off, dK + off, id_s, ks > 0);
-        }
-        umma_commit(&bar[kSFull + sb]);
-        umma_commit(&bar[kKEmpty + kst]);
-      };
       while (ok) {
         const int slot = it & 1;
         if (!wait(kItemFull + slot, (it >> 1) & 1)) break;
@@ -641,25 +643,41 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         const int h = wi / n_entries;
         const int nkb = P.entries[wi - h * n_entries].z;
         const int nch = (nkb + C::kChunkBlocks - 1) / C::kChunkBlocks;
-        if (!wait(kQFull, it & 1)) break;
-        tc_fence_after();
-        if (nch == 0) umma_commit(&bar[kQEmpty]);
-        else issue_s(cc);
-        for (int c = 0; c < nch && ok; ++c, ++cc) {
-          if (c + 1 < nch) issue_s(cc + 1);
-          else umma_commit(&bar[kQEmpty]);   // Q is free once this item's S products are done
-          const int vs = cc % C::kVStages, pb = cc & 1;
-          if (!wait(kVFull + vs, (cc / C::kVStages) & 1)) break;
-          if (!wait(kPFull + pb, (cc >> 1) & 1)) break;
-          tc_fence_after();
-          const uint64_t dV = dV0 + (static_cast<uint64_t>(vs) * C::kChunkBytes >> 4);
-          // A = P from tensor memory: 16 keys = 8 packed columns per step
+        if (!pv_role) {
+          // S of chunk x into the single S buffer once the softmax has read
+          // S of chunk x - 1: A = Q from tensor memory (16 dims = 8 packed
+          // columns per step), B = K (K-major, 32 bytes per step inside a
+          // 128-byte row)
+          if (!wait(kQTmem, it & 1)) break;   // this item's Q is in tensor memory
+          for (int c = 0; c < nch && ok; ++c, ++cc) {
+            const int kst = cc % C::kKStages;
+            if (!wait(kKFull + kst, (cc / C::kKStages) & 1)) break;
+            if (cc >= 1 && !wait(kSFree, (cc - 1) & 1)) break;
+            tc_fence_after();
+            const uint64_t dK = dK0 + (static_cast<uint64_t>(kst) * C::kChunkBytes >> 4);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_f16_ts(tbase + C::kColO, tbase + C::kColP + 64 * pb + 8 * ks, dV + ((ks * 2048) >> 4), id_o,
-                        c > 0 || ks > 0);
-          umma_commit(&bar[kODone + pb]);
-          umma_commit(&bar[kVEmpty + vs]);
+            for (int ks = 0; ks < D / 16; ++ks)
+              umma_f16_ts(tbase + C::kColS, tbase + C::kColQ + 8 * ks,
+                          dK + (((ks >> 2) * C::kHalf + (ks & 3) * 32) >> 4), id_s, ks > 0);
+            umma_commit(&bar[kSFull]);
+            umma_commit(&bar[kKEmpty + kst]);
+          }
+        } else {
+          // O += P V of chunk x: A = P from tensor memory (16 keys = 8
+          // packed columns per step), B = V (MN-major)
+          for (int c = 0; c < nch && ok; ++c, ++cc) {
+            const int vs = cc % C::kVStages, pb = cc & 1;
+            if (!wait(kPFull + pb, (cc >> 1) & 1)) break;
+            if (!wait(kVFull + vs, (cc / C::kVStages) & 1)) break;
+            tc_fence_after();
+            const uint64_t dV = dV0 + (static_cast<uint64_t>(vs) * C::kChunkBytes >> 4);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              umma_f16_ts(tbase + C::kColO, tbase + C::kColP + 64 * pb + 8 * ks, dV + ((ks * 2048) >> 4), id_o,
+                          c > 0 || ks > 0);
+            umma_commit(&bar[kODone + pb]);
+            umma_commit(&bar[kVEmpty + vs]);
+          }
         }
         ++it;
       }
@@ -671,34 +689,16 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // warps 2..9: thread = (row, half of the chunk's 128 columns); the two
-    // threads of a row sit in warps w and w + 4 (same tensor-memory quarter)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
     const int quarter = warp & 3;
-    const int half = (warp - C::kSoftmaxWarp0) >> 2;
     const int row = 32 * quarter + lane;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(32 * quarter) << 16);
-    float* xch = reinterpret_cast<float*>(smem + C::kOffX);   // [2 half][128 rows]
     uint32_t it = 0, cc = 0;
     bool ok = true;
     auto wait = [&](int idx, uint32_t parity) {
       if (ok) ok = mbar_wait(&bar[idx], parity, abort_flag, err);
       ok = __all_sync(0xffffffffu, ok);
       return ok;
-    };
-    // the partner's value: both threads of the row publish theirs, wait for
-    // the other (bounded mbarrier waits), read, and release the slot
-    uint32_t xk = 0;   // exchanges so far (the same count in both warps of a pair)
-    auto exchange = [&](float mine) {
-      if (xk >= 1) wait(kXFree + quarter, (xk - 1) & 1);
-      xch[half * 128 + row] = mine;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[kXFull + quarter]);
-      wait(kXFull + quarter, xk & 1);
-      const float other = xch[(half ^ 1) * 128 + row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[kXFree + quarter]);
-      ++xk;
-      return other;
     };
     while (ok) {
       const int slot = it & 1;
@@ -716,45 +716,61 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       const int pos = v.L - v.n + tok;
       const bool valid = tok < v.n && pos >= 0;
       const int lim = valid ? pos : -1;
-      float m_ref = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
-      for (int c = 0; c < nch; ++c, ++cc) {
-        const int sb = cc & 1;
-        if (!wait(kSFull + sb, (cc >> 1) & 1)) break;
-        tc_fence_after();
-        // this thread's scores of the chunk; with two threads per row the
-        // row maximum combines the halves through the pair's exchange slot
-        const int k0 = c * 128 + C::kCols * half;
-        float t[C::kCols];
+      // Q row -> tensor memory (the previous item's products, which read the
+      // old Q, completed before its epilogue).  The TMA box put row `row`
+      // at row * 128 bytes of each 64-dim half, its 16-byte pieces permuted
+      // by the 128-byte swizzle (piece j at j ^ (row & 7)).
+      if (!wait(kQFull, it & 1)) break;
+      {
+        uint32_t qw[32];
 #pragma unroll
-        for (int q = 0; q < C::kCols / 64; ++q) tmem_ld64(lane_addr + sb * 128 + C::kCols * half + 64 * q, t + 64 * q);
+        for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 u = *reinterpret_cast<const uint4*>(sQ + hf * C::kHalf + row * 128 + ((j ^ (row & 7)) << 4));
+            qw[4 * j] = u.x;
+            qw[4 * j + 1] = u.y;
+            qw[4 * j + 2] = u.z;
+            qw[4 * j + 3] = u.w;
+          }
+          tmem_st32u(lane_addr + C::kColQ + 32 * hf, qw);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kQTmem]);
+      float m_ref = -INFINITY, l = 0.f;
+      for (int c = 0; c < nch; ++c, ++cc) {
+        if (!wait(kSFull, cc & 1)) break;
+        tc_fence_after();
+        const int k0 = c * 128;
+        float t[128];
+        tmem_ld64(lane_addr + C::kColS, t);
+        tmem_ld64(lane_addr + C::kColS + 64, t + 64);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
-        if (!__all_sync(0xffffffffu, k0 + C::kCols - 1 <= lim)) {   // causal mask / tail: -inf
+        if (lane == 0) mbar_arrive(&bar[kSFree]);
+        if (!__all_sync(0xffffffffu, k0 + 127 <= lim)) {   // causal mask / tail: -inf
 #pragma unroll
-          for (int i = 0; i < C::kCols; ++i) t[i] = k0 + i <= lim ? t[i] : -INFINITY;
+          for (int i = 0; i < 128; ++i) t[i] = k0 + i <= lim ? t[i] : -INFINITY;
         }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // 4 chains for ILP
 #pragma unroll
-        for (int i = 0; i < C::kCols; ++i) m4[i & 3] = fmaxf(m4[i & 3], t[i]);
-        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        if (C::kRowSplit > 1) {
-          mx = fmaxf(mx, exchange(mx));
-          if (!ok) break;
-        }
+        for (int i = 0; i < 128; ++i) m4[i & 3] = fmaxf(m4[i & 3], t[i]);
         // the scale is positive, so it commutes with the maximum
-        mx *= P.scale_log2;
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
         const bool need = mx > m_ref + 8.f;
         const float new_ref = need ? mx : m_ref;
         const float mu = new_ref == -INFINITY ? 0.f : new_ref;
         const float alpha = need ? exp2f(m_ref - new_ref) : 1.f;
-        // P buffer sb is free once the PV of two chunks back has completed
-        if (cc >= 2 && !wait(kODone + sb, ((cc >> 1) - 1) & 1)) break;
-        // p = 2^(s * scale - mu) as 16-bit, two per column, into this half's
-        // 32 columns of P buffer sb in tensor memory; row sum in fp32
+        // P buffer pb is free once the PV of two chunks back has completed
+        const int pb = cc & 1;
+        if (cc >= 2 && !wait(kODone + pb, ((cc >> 1) - 1) & 1)) break;
+        // p = 2^(s * scale - mu) as 16-bit, two per column, into P buffer pb;
+        // row sum in fp32
         float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int q = 0; q < C::kCols / 64; ++q) {
+        for (int q = 0; q < 2; ++q) {
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -763,32 +779,31 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
             r4[i & 3] += p0 + p1;
             pk[i] = pack2<T>(p0, p1);
           }
-          tmem_st32u(lane_addr + C::kColP + 64 * sb + C::kCols / 2 * half + 32 * q, pk);
+          tmem_st32u(lane_addr + C::kColP + 64 * pb + 32 * q, pk);
         }
         l = l * alpha + ((r4[0] + r4[1]) + (r4[2] + r4[3]));
         if (c > 0 && __any_sync(0xffffffffu, need)) {
           // O must hold the previous chunk's product before it is rescaled
-          if (!wait(kODone + (sb ^ 1), ((cc - 1) >> 1) & 1)) break;
+          if (!wait(kODone + (pb ^ 1), ((cc - 1) >> 1) & 1)) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int cb = 0; cb < C::kCols / 32; ++cb) {
+          for (int cb = 0; cb < 4; ++cb) {
             float o32[32];
-            tmem_ld32(lane_addr + C::kColO + C::kCols * half + cb * 32, o32);
+            tmem_ld32(lane_addr + C::kColO + cb * 32, o32);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o32[i] *= alpha;
-            tmem_st32(lane_addr + C::kColO + C::kCols * half + cb * 32, o32);
+            tmem_st32(lane_addr + C::kColO + cb * 32, o32);
           }
         }
         // V rows past the sequence end (the last block's tail) may hold
         // anything, NaN included: zero them so that 0 * NaN never enters O
-        const int kc = c * 128;
-        if (kc + 128 > v.L) {
+        if (k0 + 128 > v.L) {
           // the chunk's V copies have landed before their rows are overwritten
           const int vs = cc % C::kVStages;
           if (!wait(kVFull + vs, (cc / C::kVStages) & 1)) break;
-          const int z0 = max(v.L, kc) - kc, z1 = min(kc + 128, nkb * kBlock) - kc;
+          const int z0 = max(v.L, k0) - k0, z1 = min(k0 + 128, nkb * kBlock) - k0;
           uint8_t* sV = smem + C::kOffV + static_cast<size_t>(vs) * C::kChunkBytes;
-          for (int i = half * 128 + row; i < (z1 - z0) * 16; i += 128 * C::kRowSplit) {   // 16 x 16 B per key row
+          for (int i = row; i < (z1 - z0) * 16; i += 128) {   // 16 x 16 B per key row
             const int key = z0 + (i >> 4), part = i & 15;
             *reinterpret_cast<uint4*>(sV + (part >> 3) * C::kHalf + key * 128 + (part & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -797,28 +812,22 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kPFull + sb]);
+        if (lane == 0) mbar_arrive(&bar[kPFull + pb]);
         m_ref = new_ref;
       }
       if (!ok) break;
-      // epilogue: out = O / l, one rounding to T; each thread writes its 64 columns
-      float lsum = l;
-      if (C::kRowSplit > 1) {
-        lsum += exchange(l);
-        if (!ok) break;
-      }
+      // epilogue: out = O / l, one rounding to T
       if (nch > 0 && !wait(kODone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1)) break;
       tc_fence_after();
       {
-        const float inv = (valid && lsum > 0.f) ? 1.0f / lsum : 0.f;
+        const float inv = (valid && l > 0.f) ? 1.0f / l : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(P.out) +
-                                              ((static_cast<int64_t>(v.q0) + tok) * P.hq + h * G + row % G) * D +
-                                              C::kCols * half);
+                                              ((static_cast<int64_t>(v.q0) + tok) * P.hq + h * G + row % G) * D);
 #pragma unroll
-        for (int cb = 0; cb < C::kCols / 32; ++cb) {
+        for (int cb = 0; cb < 4; ++cb) {
           float o32[32];
           if (nch > 0) {   // uniform over the warp: every lane takes part in the load
-            tmem_ld32(lane_addr + C::kColO + C::kCols * half + cb * 32, o32);
+            tmem_ld32(lane_addr + C::kColO + cb * 32, o32);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) o32[i] = 0.f;
