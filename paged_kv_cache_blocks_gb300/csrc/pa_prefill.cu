@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       uint32_t it = 0, cc = 0;
       bool ok = true;
       auto wait = [&](int idx, uint32_t parity) {
-        if (ok) ok = mbar_wait(&bar[idx], parity, abort_flag, err);
+        if (ok) ok = mbar_wait_sleep(&bar[idx], parity, abort_flag, err);
         return ok;
       };
       while (ok) {
@@ -768,20 +768,23 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         if (cc >= 2 && !wait(kODone + pb, ((cc >> 1) - 1) & 1)) break;
         // p = 2^(s * scale - mu) as 16-bit, two per column, into P buffer pb;
         // row sum in fp32
-        float r4[4] = {0.f, 0.f, 0.f, 0.f};
+        // (pairs of columns on the packed two-lane fp32 FMA / add)
+        const float2 sc2 = make_float2(P.scale_log2, P.scale_log2), nm2 = make_float2(-mu, -mu);
+        float2 r2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(fmaf(t[64 * q + 2 * i], P.scale_log2, -mu));
-            const float p1 = fast_exp2(fmaf(t[64 * q + 2 * i + 1], P.scale_log2, -mu));
-            r4[i & 3] += p0 + p1;
-            pk[i] = pack2<T>(p0, p1);
+            const float2 x = fma2(make_float2(t[64 * q + 2 * i], t[64 * q + 2 * i + 1]), sc2, nm2);
+            const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            r2[i & 3] = add2(r2[i & 3], p);
+            pk[i] = pack2<T>(p.x, p.y);
           }
           tmem_st32u(lane_addr + C::kColP + 64 * pb + 32 * q, pk);
         }
-        l = l * alpha + ((r4[0] + r4[1]) + (r4[2] + r4[3]));
+        r2[0] = add2(add2(r2[0], r2[1]), add2(r2[2], r2[3]));
+        l = l * alpha + (r2[0].x + r2[0].y);
         if (c > 0 && __any_sync(0xffffffffu, need)) {
           // O must hold the previous chunk's product before it is rescaled
           if (!wait(kODone + (pb ^ 1), ((cc - 1) >> 1) & 1)) break;
