@@ -392,7 +392,9 @@ def run_prefill(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}"},
         "query_tokens_per_s": job_throughput(q_tokens, world, ms_step * 1e-3),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": load_traffic("chunked", args.variant),
+                     "traffic_per": "step (the 8 prefill launches)",
                      "kernel": "prefill_kernel (mma.sync)" if args.variant == "mma"
                      else "prefill_tc_kernel (tcgen05)",
                      "kernel_ms": kern_ms, "algorithmic_flops": flops, "peak_source": peak_src},
@@ -711,20 +713,26 @@ TRAFFIC = {
 }
 
 
-def kernel_src_hash():
+DECODE_SRC = ("pa_decode.cu", "pa_device.cuh")
+PREFILL_SRC = ("pa_prefill.cu", "pa_device.cuh")
+
+
+def kernel_src_hash(files=DECODE_SRC):
     import hashlib
     h = hashlib.sha256()
-    for f in ("pa_decode.cu", "pa_device.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_cache_blocks_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def load_traffic(workload, variant):
-    """DRAM bytes per attention launch from the ncu capture of this kernel
-    build, or None when there is none (or the kernel changed since)."""
+    """DRAM bytes per attention launch (per step of 8 launches for the
+    chunked prefill) from the ncu capture of this kernel build, or None when
+    there is none (or the kernel changed since)."""
     ent = TRAFFIC.get((workload, variant))
-    if not ent or ent["kernel_src"] != kernel_src_hash():
+    files = PREFILL_SRC if workload == "chunked" else DECODE_SRC
+    if not ent or ent["kernel_src"] != kernel_src_hash(files):
         return None
     return ent["bytes"]
 
