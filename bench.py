@@ -704,12 +704,15 @@ def time_graph(step, steps, warmup, stream, barrier, dist, dev, units, world):
 # the ncu captures summarised in profiles/ (file named below), keyed by the
 # hash of the kernel sources they were taken on: a changed kernel reports null.
 TRAFFIC = {
-    ("llama70b", "auto"): {"bytes": 3774.52e6 + 16.49e6, "kernel_src": "5a0c47d1456b6a42",
+    ("llama70b", "auto"): {"bytes": 3774.53e6 + 16.45e6, "kernel_src": "6c247c8e74f6a49b",
                            "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "mma"): {"bytes": 3774.52e6 + 16.49e6, "kernel_src": "5a0c47d1456b6a42",
+    ("llama70b", "mma"): {"bytes": 3774.53e6 + 16.45e6, "kernel_src": "6c247c8e74f6a49b",
                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "fp8"): {"bytes": 1892.64e6 + 17.38e6, "kernel_src": "5a0c47d1456b6a42",
+    ("llama70b", "fp8"): {"bytes": 1892.61e6 + 17.35e6, "kernel_src": "6c247c8e74f6a49b",
                           "profile": "profiles/decode_step_llama70b_fp8_launches.md"},
+    # the 8 prefill launches of one step (iterations 1..8), summed
+    ("chunked", "auto"): {"bytes": 1285.36e6 + 286.86e6, "kernel_src": "6ab8715fdaf9d592",
+                          "profile": "profiles/prefill_tc_kernel_chunked.md"},
 }
 
 
