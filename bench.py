@@ -727,14 +727,14 @@ def time_graph(step, steps, warmup, stream, barrier, dist, dev, units, world):
 # the ncu captures summarised in profiles/ (file named below), keyed by the
 # hash of the kernel sources they were taken on: a changed kernel reports null.
 TRAFFIC = {
-    ("llama70b", "auto"): {"bytes": 3774.53e6 + 16.45e6, "kernel_src": "6c247c8e74f6a49b",
+    ("llama70b", "auto"): {"bytes": 3774.53e6 + 16.45e6, "kernel_src": "cfe2825b97ee6d57",
                            "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "mma"): {"bytes": 3774.53e6 + 16.45e6, "kernel_src": "6c247c8e74f6a49b",
+    ("llama70b", "mma"): {"bytes": 3774.53e6 + 16.45e6, "kernel_src": "cfe2825b97ee6d57",
                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "fp8"): {"bytes": 1892.61e6 + 17.35e6, "kernel_src": "6c247c8e74f6a49b",
+    ("llama70b", "fp8"): {"bytes": 1892.61e6 + 17.35e6, "kernel_src": "cfe2825b97ee6d57",
                           "profile": "profiles/decode_step_llama70b_fp8_launches.md"},
     # the 8 prefill launches of one step (iterations 1..8), summed
-    ("chunked", "auto"): {"bytes": 1285.36e6 + 286.86e6, "kernel_src": "6ab8715fdaf9d592",
+    ("chunked", "auto"): {"bytes": 1285.36e6 + 286.86e6, "kernel_src": "6f58af1f530c2d60",
                           "profile": "profiles/prefill_tc_kernel_chunked.md"},
 }
 
@@ -744,11 +744,17 @@ PREFILL_SRC = ("pa_prefill.cu", "pa_device.cuh")
 
 
 def kernel_src_hash(files=DECODE_SRC):
+    """First 16 hex of the sha256 of the kernel sources with comments and
+    whitespace removed, so that only a change of code invalidates counters."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "paged_kv_cache_blocks_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_blocks_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

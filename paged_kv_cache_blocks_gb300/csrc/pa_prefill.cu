@@ -401,18 +401,19 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
 //   warp 9     one thread issues O += P V (M 128, N 128 dims, K 128 keys)
 //              once the softmax has written P.  Issuing a product blocks the
 //              thread about as long as the product runs, hence two issuers.
-//              Both products take their A
-//              operand (Q, P) from tensor memory, which runs them at the full
-//              rate where an A operand in shared memory halves it;
-//              tcgen05.commit signals each result on an mbarrier;
+//              Both products take their A operand (Q, P) from tensor memory,
+//              which runs them at the full rate where an A operand in shared
+//              memory halves it; tcgen05.commit signals each result on an
+//              mbarrier;
 //   warps 0-3  one query row per thread (its tensor-memory lane): at the
 //              start of an item, move the row of Q from shared to tensor
 //              memory; per chunk read S, apply the scale and the causal mask,
 //              online softmax in fp32 with the running maximum moved only
 //              when it grows by more than 2^8 (the exact result either way,
-//              fewer rescales of O), write P as 16-bit values, two per
-//              column, into one of two P buffers, rescale O when the maximum
-//              moved, and finally write O / l.
+//              fewer rescales of O), scale-and-subtract and row sums on the
+//              packed two-lane fp32 FMA / add, write P as 16-bit values, two
+//              per column, into one of two P buffers, rescale O when the
+//              maximum moved, and finally write O / l.
 // The softmax warpgroup holds 128 scores per thread: it takes registers the
 // producer warpgroup gives back (setmaxnreg), so that nothing spills.
 // Every wait is bounded; a timeout flags PA_DEVERR_TIMEOUT and the CTA
