@@ -438,8 +438,8 @@ def make_prefill_batch(name, seed=0, iteration=CHUNK_PIECES, poison=True, keep_c
         lens, pieces = chunked_iteration_shape(iteration, seed)
     lens = np.asarray(lens, np.int64)
     pieces = np.asarray(pieces, np.int64)
-    if lens.shape != pieces.shape or (pieces < 1).any() or (pieces > lens).any():
-        raise ValueError("every piece must hold 1..len tokens")
+    if lens.shape != pieces.shape or (pieces < 0).any() or (pieces > lens).any():
+        raise ValueError("every piece must hold 0..len tokens")
     gseed = int(seed) * 1000 + _SEED_SALT[name] + 500 + int(iteration)
     g = torch.Generator(device="cpu")
     g.manual_seed(gseed)

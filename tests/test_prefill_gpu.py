@@ -189,3 +189,27 @@ def test_prefill_head_dim_128_small_groups(pa, hq, variant):
         U.assert_close_rounded(got, ref, "bf16", f"prefill G={hq // 8} d128 variant {variant}")
     finally:
         del W.WORKLOADS[name], W._SEED_SALT[name]
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+def test_prefill_empty_pieces_and_empty_sequences(pa, variant):
+    """Sequences with no query token this iteration (empty pieces) or with no
+    tokens at all, beside pieces of one token, of a few and of several tiles."""
+    pb = W.make_prefill_batch("llama70b", seed=11, lens=[0, 5, 300, 17, 129, 16, 0],
+                              pieces=[0, 0, 130, 17, 1, 16, 0])
+    got, ref, _ = run(pa, pb, variant=variant)
+    assert got.shape[0] == 164
+    U.assert_close_rounded(got, ref, "bf16", f"empty pieces variant {variant}")
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+def test_prefill_without_query_tokens_is_a_noop(pa, variant):
+    """Every piece empty: the call returns at once with an empty output."""
+    pb = W.make_prefill_batch("llama8b", seed=12, lens=[40, 0, 17], pieces=[0, 0, 0])
+    w = pb.workload
+    kc, vc = pb.placed_pools()
+    out = pa.pa_prefill(U.to_dev(pb.q, w.dtype), U.to_dev(kc, w.dtype), U.to_dev(vc, w.dtype),
+                        torch.from_numpy(pb.block_tables).cuda(), torch.from_numpy(pb.seq_lens).cuda(),
+                        torch.from_numpy(pb.q_offsets).cuda(), w.scale, variant=variant)
+    torch.cuda.synchronize()
+    assert tuple(out.shape) == (0, w.num_q_heads, w.head_dim)
