@@ -55,6 +55,11 @@ DESCR["chunked"] = ("chunked prefill, Llama-3-70B-shaped layer (64 q / 8 kv head
                     "iteration with the decode tokens of 20 chats of 300+U{1..100} tokens; one step "
                     "= the 8 iterations (pa_cache_write of the pieces + pa_prefill)")
 PREFILL_METRIC = "paged chunked-prefill attention TFLOP/s (causal, dense-equivalent 4*q*k*d per head)"
+COW_PAIRS, COW_POOL = 4096, 32768
+DESCR["cow"] = (f"copy-on-write block copies: {COW_PAIRS} (source, destination) pairs of "
+                "Llama-3-70B-shaped blocks (8 kv heads x 16 tokens x 128 dims, bf16, K and V: "
+                f"64 KB per pair) in a {COW_POOL}-block pool; one step = one pa_copy_blocks call")
+COW_METRIC = "paged KV copy-on-write block copy GB/s (bytes read + written)"
 VARIANTS = {"auto": 0, "fma": 1, "mma": 2, "tc": 3}
 
 
@@ -472,6 +477,178 @@ def run_prefill_e2e(args, pa, its, w, dev, barrier, dist, world, flops):
                     "iteration i+1's inputs go up while i computes; synchronised after the last step"}
 
 
+def cow_pairs(seed):
+    """Distinct source and destination blocks of the copy workload (seeded)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(4000 + int(seed))
+    perm = torch.randperm(COW_POOL, generator=g).to(torch.int32)
+    return perm[:COW_PAIRS].clone(), perm[COW_PAIRS:2 * COW_PAIRS].clone()
+
+
+def cow_cpu_baseline(pairs=COW_PAIRS):
+    """The oracle's block copy (single-threaded C, plus the copies of the
+    caches its Python wrapper returns) on a sample: `pairs` pairs in a pool of
+    2 x pairs blocks of the same shape."""
+    import oracle
+    oracle.build()
+    g = np.random.default_rng(7)
+    nb = 2 * pairs
+    kc = g.integers(0, 1 << 16, (nb, 8, 16, 128), dtype=np.uint16)
+    vc = g.integers(0, 1 << 16, (nb, 8, 16, 128), dtype=np.uint16)
+    perm = g.permutation(nb).astype(np.int32)
+    src, dst = perm[:pairs], perm[pairs:]
+    oracle.copy_blocks(kc[:4], vc[:4], src[:0], dst[:0])   # load the library
+    t0 = time.perf_counter()
+    oracle.copy_blocks(kc, vc, src, dst)
+    sec = time.perf_counter() - t0
+    moved = 2 * pairs * 2 * 8 * 16 * 128 * 2
+    return moved / sec / 1e9, sec, (f"{pairs} pairs in a pool of {nb} blocks of the same shape "
+                                    "(oracle_copy_blocks, one thread, with the wrapper's copies "
+                                    "of both caches)")
+
+
+def run_cow(args, rank, world, local_rank):
+    """Copy-on-write block copies (the f2 row): one step = one pa_copy_blocks
+    call over COW_PAIRS pairs; bytes read + written per second against the
+    measured HBM copy bandwidth."""
+    from paged_kv_cache_blocks_gb300 import build as pb_build
+    pb_build.build()
+    from paged_kv_cache_blocks_gb300 import binding as pa
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    Hkv, D, dt = 8, 128, torch.bfloat16
+    g = torch.Generator(device=dev)
+    g.manual_seed(5000 + rank)
+    kc = torch.randn((COW_POOL, Hkv, 16, D), generator=g, device=dev).to(dt)
+    vc = torch.randn((COW_POOL, Hkv, 16, D), generator=g, device=dev).to(dt)
+    src, dst = cow_pairs(rank)
+    src_d, dst_d = src.to(dev), dst.to(dev)
+    per_pair = 2 * Hkv * 16 * D * 2                 # K and V of one block, bytes
+    moved = 2 * per_pair * COW_PAIRS                # read + written per step
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        pa.pa_copy_blocks(kc, vc, src_d, dst_d)
+    torch.cuda.synchronize()
+    # the copy is idempotent once done: check it against the sources
+    if not (torch.equal(kc[dst.long()], kc[src.long()]) and torch.equal(vc[dst.long()], vc[src.long()])):
+        raise RuntimeError("pa_copy_blocks: destinations differ from sources after warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_identity(local_rank)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_host0 = time.time()
+    start.record(stream)
+    for a, z in ev:
+        a.record(stream)
+        pa.pa_copy_blocks(kc, vc, src_d, dst_d)
+        z.record(stream)
+    stop.record(stream)
+    barrier()
+    t_host1 = time.time()
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+    ms_step = reduce_max(start.elapsed_time(stop) / args.steps, dist, dev)
+    times = sorted(a.elapsed_time(z) for a, z in ev)
+    kern_ms = statistics.fmean(times)
+    peak_gbs, peak_src = measured_peaks()
+    e2e = None
+    if not args.no_e2e:
+        # through the public API: pair lists up from pinned host memory, the
+        # copy, one destination block of K read back as the step's result
+        src_h, dst_h = src.pin_memory(), dst.pin_memory()
+        res_h = torch.empty((Hkv, 16, D), dtype=dt).pin_memory()
+        probe = int(dst[0])
+        steps = max(1, min(args.steps, args.e2e_steps))
+        for _ in range(3):
+            src_d.copy_(src_h, non_blocking=True)
+            dst_d.copy_(dst_h, non_blocking=True)
+            pa.pa_copy_blocks(kc, vc, src_d, dst_d)
+            res_h.copy_(kc[probe], non_blocking=True)
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            src_d.copy_(src_h, non_blocking=True)
+            dst_d.copy_(dst_h, non_blocking=True)
+            pa.pa_copy_blocks(kc, vc, src_d, dst_d)
+            res_h.copy_(kc[probe], non_blocking=True)
+        torch.cuda.synchronize()
+        barrier()
+        sec = reduce_max((time.perf_counter() - t0) / steps, dist, dev)
+        e2e = {"value": job_throughput(moved, world, sec) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": 2 * 4 * COW_PAIRS, "d2h_bytes_per_step": Hkv * 16 * D * 2,
+               "steps": steps, "ms_per_step": sec * 1e3,
+               "path": "per step: H2D (pinned) source and destination ids -> pa_copy_blocks -> "
+                       "D2H of one copied K block; synchronised after the last step"}
+    if rank != 0:
+        return 0
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, sec, sample = cow_cpu_baseline()
+        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "seconds": sec,
+               "sample": sample}
+    line = {
+        "metric": COW_METRIC, "value": job_throughput(moved, world, ms_step * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCR["cow"], "pairs": COW_PAIRS, "pool_blocks": COW_POOL,
+                   "bytes_per_step": moved,
+                   "l2": f"{moved / 2**20:.0f} MB read + written per step vs 129 MB L2; no flush",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": moved / (kern_ms * 1e-3) / 1e9,
+                     "peak": peak_gbs, "unit": "GB/s",
+                     "frac": moved / (kern_ms * 1e-3) / 1e9 / peak_gbs,
+                     "traffic": load_traffic("cow", "auto"), "kernel": "copy_blocks_kernel",
+                     "kernel_ms": kern_ms,
+                     "kernel_ms_p10_p50_p90": [times[len(times) // 10], times[len(times) // 2],
+                                               times[(9 * len(times)) // 10]],
+                     "algorithmic_bytes": moved,
+                     "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(t_host0, t_host1) if sampler else None,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_cow(args, rank, world):
+    """The oracle's block copy as the reference arm of the copy workload."""
+    if rank != 0:
+        return 0
+    vals = []
+    for _ in range(args.warmup + args.steps):
+        v, sec, sample = cow_cpu_baseline()
+        vals.append((v, sec))
+    v = statistics.fmean(x for x, _ in vals[args.warmup:])
+    sec = statistics.fmean(s for _, s in vals[args.warmup:])
+    line = {"impl": "reference", "metric": COW_METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": DESCR["cow"], "parallelism": "oracle, one thread"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -733,6 +910,8 @@ TRAFFIC = {
                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
     ("llama70b", "fp8"): {"bytes": 1892.61e6 + 17.35e6, "kernel_src": "cfe2825b97ee6d57",
                           "profile": "profiles/decode_step_llama70b_fp8_launches.md"},
+    ("cow", "auto"): {"bytes": 268.52e6 + 216.53e6, "kernel_src": "ba3a77c251cf3178",
+                      "profile": "profiles/copy_blocks_kernel_cow.md"},
     # the 8 prefill launches of one step (iterations 1..8), summed
     ("chunked", "auto"): {"bytes": 1285.36e6 + 286.86e6, "kernel_src": "6f58af1f530c2d60",
                           "profile": "profiles/prefill_tc_kernel_chunked.md"},
@@ -741,6 +920,7 @@ TRAFFIC = {
 
 DECODE_SRC = ("pa_decode.cu", "pa_device.cuh")
 PREFILL_SRC = ("pa_prefill.cu", "pa_device.cuh")
+COPY_SRC = ("pa_cache_write.cu", "pa_device.cuh")
 
 
 def kernel_src_hash(files=DECODE_SRC):
@@ -763,7 +943,7 @@ def load_traffic(workload, variant):
     chunked prefill) from the ncu capture of this kernel build, or None when
     there is none (or the kernel changed since)."""
     ent = TRAFFIC.get((workload, variant))
-    files = PREFILL_SRC if workload == "chunked" else DECODE_SRC
+    files = {"chunked": PREFILL_SRC, "cow": COPY_SRC}.get(workload, DECODE_SRC)
     if not ent or ent["kernel_src"] != kernel_src_hash(files):
         return None
     return ent["bytes"]
@@ -993,9 +1173,13 @@ def main():
     if args.impl == "reference":
         if args.workload == "chunked":
             return run_reference_prefill(args, rank, world)
+        if args.workload == "cow":
+            return run_reference_cow(args, rank, world)
         return run_reference(args, rank, world)
     if args.workload == "chunked":
         return run_prefill(args, rank, world, local_rank)
+    if args.workload == "cow":
+        return run_cow(args, rank, world, local_rank)
     return run_pa(args, rank, world, local_rank)
 
 

@@ -136,18 +136,32 @@ int cache_write_fp8_launch(const void* k, const void* v, const int64_t* slot_map
 // section 03: a shared block is copied when one holder writes into it).
 // One CTA per (pair, K or V): the whole block -- every KV head's 16 rows -- is
 // contiguous in the [num_blocks][num_kv_heads][16][head_dim] layout, so each
-// CTA streams it with 16-byte loads and stores.
+// CTA streams it with 16-byte loads and stores, eight loads in flight per
+// thread before their stores (source and destination are different blocks).
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                        const int32_t* __restrict__ src, const int32_t* __restrict__ dst,
                        int64_t num_blocks, int chunks_per_block) {
+  constexpr int kBatch = 8;
   const int i = blockIdx.x;
   const int32_t s = src[i], d = dst[i];
   if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks || s == d) return;
   uint4* cache = blockIdx.y == 0 ? k_cache : v_cache;
   const uint4* from = cache + static_cast<int64_t>(s) * chunks_per_block;
   uint4* to = cache + static_cast<int64_t>(d) * chunks_per_block;
-  for (int c = threadIdx.x; c < chunks_per_block; c += blockDim.x) to[c] = from[c];
+  for (int base = threadIdx.x; base < chunks_per_block; base += kBatch * blockDim.x) {
+    uint4 r[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int c = base + j * blockDim.x;
+      if (c < chunks_per_block) r[j] = from[c];
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int c = base + j * blockDim.x;
+      if (c < chunks_per_block) to[c] = r[j];
+    }
+  }
 }
 
 int copy_blocks_launch(void* k_cache, void* v_cache, int64_t num_blocks, int32_t num_kv_heads,
