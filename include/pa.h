@@ -47,7 +47,7 @@ typedef enum {
     PA_OK = 0,
     PA_ERR_INVALID = 1,      /* bad argument, shape, id or size */
     PA_ERR_OOM = 2,          /* the allocator's free queue cannot cover the request */
-    PA_ERR_UNSUPPORTED = 3,  /* dtype / head_dim / group size this build has no kernel for */
+    PA_ERR_UNSUPPORTED = 3,  /* dtype / head_dim / group size with no compiled kernel */
     PA_ERR_SHARED_WRITE = 4, /* reserved: write into a block held by several sequences */
     PA_ERR_CUDA = 5,         /* a CUDA call failed (launch, tensor map, copy) */
     PA_ERR_DEVICE = 6        /* a kernel flagged bad data (see pa_decode_check) */
