@@ -142,12 +142,18 @@ def _need_cuda(*ts):
             raise ValueError("libpa device arguments must be contiguous CUDA tensors")
 
 
+def _need(cond, what):
+    """Argument check that stays on under ``python -O`` (unlike assert)."""
+    if not cond:
+        raise TypeError(what)
+
+
 # --------------------------------------------------------------------------- device calls
 
 def pa_cache_write(k, v, slot_mapping, k_cache, v_cache, dtype=None, stream=None):
     """Scatter k/v [T, Hkv, D] into the caches [NB, Hkv, 16, D] at slot_mapping (int64)."""
     _need_cuda(k, v, slot_mapping, k_cache, v_cache)
-    assert slot_mapping.dtype == torch.int64
+    _need(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
     T, H, D = k.shape
     rc = lib().pa_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), T, H, D, _ptr(k_cache),
                               _ptr(v_cache), k_cache.shape[0], _dtype_code(k, dtype), _stream(stream))
@@ -157,7 +163,8 @@ def pa_cache_write(k, v, slot_mapping, k_cache, v_cache, dtype=None, stream=None
 def pa_copy_blocks(k_cache, v_cache, src, dst, stream=None):
     """Copy-on-write: block dst[i] of both caches becomes a copy of block src[i]."""
     _need_cuda(k_cache, v_cache, src, dst)
-    assert src.dtype == torch.int32 and dst.dtype == torch.int32 and src.shape == dst.shape
+    _need(src.dtype == torch.int32 and dst.dtype == torch.int32 and src.shape == dst.shape,
+          "src and dst must be int32 tensors of one shape")
     NB, Hkv, _, D = k_cache.shape
     rc = lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), NB, Hkv, D, _ptr(src), _ptr(dst),
                               src.numel(), _stream(stream))
@@ -181,7 +188,8 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0,
     lengths, tables and shapes; e.g. the later layers of one step).
     """
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens)
-    assert block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_tables and seq_lens must be int32")
     B, Hq, D = q.shape
     NB, Hkv = k_cache.shape[0], k_cache.shape[1]
     mb = block_tables.shape[1]
@@ -223,8 +231,10 @@ def pa_cache_write_fp8(k, v, slot_mapping, k_scale, v_scale, k_cache8, v_cache8,
     """Quantise k/v [T, Hkv, 128] (16-bit) to E4M3 into k_cache8 [NB, Hkv, 16, 128]
     and the dimension-major v_cache8 [NB, Hkv, 128, 16] (uint8 tensors)."""
     _need_cuda(k, v, slot_mapping, k_scale, v_scale, k_cache8, v_cache8)
-    assert k_cache8.dtype == torch.uint8 and v_cache8.dtype == torch.uint8
-    assert k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32
+    _need(k_cache8.dtype == torch.uint8 and v_cache8.dtype == torch.uint8,
+          "FP8 caches must be uint8 tensors of E4M3 codes")
+    _need(k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32,
+          "k_scale and v_scale must be float32")
     T, H, D = k.shape
     rc = lib().pa_cache_write_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), T, H, D, _ptr(k_scale),
                                   _ptr(v_scale), _ptr(k_cache8), _ptr(v_cache8), k_cache8.shape[0],
@@ -267,7 +277,8 @@ def pa_decode_grouped(q, k_cache, v_cache, block_tables, seq_lens, scale, group_
     group_offsets [G+1] and group_prefix_tokens [G] are int32 CUDA tensors.
     ``events`` bracket the attention kernel over the members' own tokens."""
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens, group_offsets, group_prefix_tokens)
-    assert group_offsets.dtype == torch.int32 and group_prefix_tokens.dtype == torch.int32
+    _need(group_offsets.dtype == torch.int32 and group_prefix_tokens.dtype == torch.int32,
+          "group_offsets and group_prefix_tokens must be int32")
     B, Hq, D = q.shape
     NB, Hkv = k_cache.shape[0], k_cache.shape[1]
     mb = block_tables.shape[1]
@@ -306,8 +317,9 @@ def pa_prefill(q, k_cache, v_cache, block_tables, seq_lens, q_offsets, scale, ma
     head_dim 128), 2 mma.sync, 3 tcgen05.  Returns out [Tq, Hq, D].
     """
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens, q_offsets)
-    assert block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
-    assert q_offsets.dtype == torch.int32
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_tables and seq_lens must be int32")
+    _need(q_offsets.dtype == torch.int32, "q_offsets must be int32")
     Tq, Hq, D = q.shape
     NB, Hkv = k_cache.shape[0], k_cache.shape[1]
     B = seq_lens.shape[0]
