@@ -179,6 +179,25 @@ def job_throughput(units_per_rank, world, seconds_max):
     return units_per_rank * world / seconds_max
 
 
+def cpu_model():
+    """Host CPU model (lscpu's "Model name", else /proc/cpuinfo), for the
+    record of where the oracle baseline ran."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
 def gpu_identity(local_rank):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -408,6 +427,7 @@ def run_prefill(args, rank, world, local_rank):
         "clocks": sampler.summary(t_host0, t_host1) if sampler else None,
     }
     if cpu is not None:
+        cpu["cpu_model"] = cpu_model()
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
@@ -612,7 +632,10 @@ def run_cow(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": moved / (kern_ms * 1e-3) / 1e9,
                      "peak": peak_gbs, "unit": "GB/s",
                      "frac": moved / (kern_ms * 1e-3) / 1e9 / peak_gbs,
-                     "traffic": load_traffic("cow", "auto"), "kernel": "copy_blocks_kernel",
+                     "traffic": load_traffic("cow", "auto"),
+                     "traffic_gbs": (load_traffic("cow", "auto") / (kern_ms * 1e-3) / 1e9
+                                     if load_traffic("cow", "auto") else None),
+                     "kernel": "copy_blocks_kernel",
                      "kernel_ms": kern_ms,
                      "kernel_ms_p10_p50_p90": [times[len(times) // 10], times[len(times) // 2],
                                                times[(9 * len(times)) // 10]],
@@ -623,6 +646,7 @@ def run_cow(args, rank, world, local_rank):
         "clocks": sampler.summary(t_host0, t_host1) if sampler else None,
     }
     if cpu is not None:
+        cpu["cpu_model"] = cpu_model()
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
@@ -642,7 +666,8 @@ def run_reference_cow(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": {"workload": DESCR["cow"], "parallelism": "oracle, one thread"},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -687,6 +712,7 @@ def run_reference(args, rank, world):
                                             "sample": sample},
             "seqs_steps_per_s": len(b.seq_lens) / dt,
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": sample},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -857,6 +883,8 @@ def run_pa(args, rank, world, local_rank):
         "hbm_frac_step": (kvb / (ms_step * 1e-3) / 1e9) / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "traffic_gbs": traffic / (kern_avg * 1e-3) / 1e9 if traffic else None,
+                     "traffic_frac": traffic / (kern_avg * 1e-3) / 1e9 / peak if traffic else None,
                      "kernel": "attend_kernel", "kernel_ms": kern_avg,
                      "kernel_ms_p10_p50_p90": [float(x) for x in kq],
                      "algorithmic_bytes": alg, "peak_source": f"{peak_kind} hbm_gbs"},
@@ -868,6 +896,7 @@ def run_pa(args, rank, world, local_rank):
         "clocks": clocks,
     }
     if cpu is not None:
+        cpu["cpu_model"] = cpu_model()
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
@@ -1137,6 +1166,7 @@ def run_reference_prefill(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": DESCR["chunked"], "sample": sample},
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": sample},
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
