@@ -213,3 +213,28 @@ def test_prefill_without_query_tokens_is_a_noop(pa, variant):
                         torch.from_numpy(pb.q_offsets).cuda(), w.scale, variant=variant)
     torch.cuda.synchronize()
     assert tuple(out.shape) == (0, w.num_q_heads, w.head_dim)
+
+
+def _random_shape(seed):
+    """A seeded random batch shape: 1..10 sequences of 1..2000 tokens, pieces
+    of 0..300 tokens (some of one token, some empty)."""
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 11))
+    lens = rng.integers(1, 2001, B)
+    pieces = np.minimum(lens, rng.integers(1, 301, B))
+    kind = rng.integers(0, 4, B)
+    pieces = np.where(kind == 0, 1, pieces)                 # decode tokens
+    pieces = np.where((kind == 1) & (B > 1), 0, pieces)     # sequences idle this iteration
+    return lens.tolist(), pieces.tolist()
+
+
+@pytest.mark.parametrize("variant", [2, 3])
+@pytest.mark.parametrize("seed", range(4))
+def test_prefill_random_batches(pa, seed, variant):
+    """Seeded random batches on the Llama-3-70B and -8B head layouts: every
+    output row against the oracle."""
+    name = "llama70b" if seed % 2 == 0 else "llama8b"
+    lens, pieces = _random_shape(seed)
+    pb = W.make_prefill_batch(name, seed=20 + seed, lens=lens, pieces=pieces)
+    got, ref, _ = run(pa, pb, variant=variant)
+    U.assert_close_rounded(got, ref, pb.workload.dtype, f"random batch {seed} variant {variant}")
