@@ -144,3 +144,20 @@ def test_variants_agree_closely(pa):
     b = U.batch("llama8b")
     a, c = run(pa, b, variant=1), run(pa, b, variant=2)
     assert np.max(np.abs(a - c)) <= 1e-2
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("seed", range(3))
+def test_random_batches(pa, seed, variant):
+    """Seeded random batches mixing one-token, short and long sequences
+    (1..12000 tokens) on the Llama-3-70B and -8B head layouts: every output
+    row against the oracle."""
+    rng = np.random.default_rng(2000 + seed)
+    B = int(rng.integers(1, 97))
+    kind = rng.integers(0, 10, B)
+    lens = np.where(kind == 0, rng.integers(1, 17, B),
+                    np.where(kind < 8, rng.integers(17, 2049, B), rng.integers(2049, 12001, B)))
+    name = "llama70b" if seed % 2 == 0 else "llama8b"
+    b = U.batch(name, seed=30 + seed, lens=tuple(int(x) for x in lens))
+    got = run(pa, b, variant=variant)
+    U.assert_close(got, U.oracle_out(b), f"random decode batch {seed} v{variant}")
