@@ -872,11 +872,9 @@ __global__ void __launch_bounds__(32 * (NC + 2))
           tma_load_2d(dst, &tm_k, 0, y, &full[st]);
           tma_load_2d(dst + Cfg::kKBytes, &tm_v, 0, y, &full[st]);
         } else {
-#pragma unroll
-          for (int hf = 0; hf < Tile<D>::kHalves; ++hf) {
-            tma_load_2d(dst + hf * Tile<D>::kHalfBytes, &tm_k, hf * 64, y, &full[st]);
-            tma_load_2d(dst + Tile<D>::kKVBytes + hf * Tile<D>::kHalfBytes, &tm_v, hf * 64, y, &full[st]);
-          }
+          // one 3-D box per K (V) tile: both 64-dim halves
+          tma_load_3d(dst, &tm_k, 0, y, 0, &full[st]);
+          tma_load_3d(dst + Tile<D>::kKVBytes, &tm_v, 0, y, 0, &full[st]);
         }
       }
       if (ok) mbar_arrive(&item_empty[slot]);
@@ -1129,11 +1127,8 @@ __global__ void __launch_bounds__(kPrefixWarps * 32)
         }
         const int32_t y = static_cast<int32_t>(id < 0 ? y_oob : (static_cast<int64_t>(id) * P.hkv + h) * kBlock);
         uint8_t* dst = smem + static_cast<size_t>(j) * Cfg::kStageBytes;
-#pragma unroll
-        for (int hf = 0; hf < Tile<D>::kHalves; ++hf) {
-          tma_load_2d(dst + hf * Tile<D>::kHalfBytes, &tm_k, hf * 64, y, bar);
-          tma_load_2d(dst + Tile<D>::kKVBytes + hf * Tile<D>::kHalfBytes, &tm_v, hf * 64, y, bar);
-        }
+        tma_load_3d(dst, &tm_k, 0, y, 0, bar);
+        tma_load_3d(dst + Tile<D>::kKVBytes, &tm_v, 0, y, 0, bar);
       }
     }
     // this warp's 16 query rows: row r -> member r / G, head r % G
@@ -1322,6 +1317,29 @@ bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int 
   return true;
 }
 
+// The 16-bit caches as a 3-D tensor for the decode kernels: (64 dims of one
+// half, token rows, halves), so that one box of 64 x 16 x D/64 moves a whole
+// (block, KV head) tile, its halves 2048 bytes apart as two 2-D boxes would
+// put them (the 128-byte swizzle phase is the token row either way).
+bool encode_cache_map3(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D,
+                       std::string* why) {
+  EncodeTiledFn fn = get_encode_fn(why);
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(num_blocks) * hkv * kBlock,
+                        static_cast<cuuint64_t>(D / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, 128};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlock), static_cast<cuuint32_t>(D / 64)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (why) *why = "cuTensorMapEncodeTiled (3-D) failed with CUresult " + std::to_string(static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
 namespace {
 
 struct LaunchShape {
@@ -1474,8 +1492,8 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   if (a.fp8) {
     if (!encode_fp8_maps(&tk, &tv, a.k_cache, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why))
       return 5;
-  } else if (!encode_cache_map(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why) ||
-             !encode_cache_map(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why)) {
+  } else if (!encode_cache_map3(&tk, a.k_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why) ||
+             !encode_cache_map3(&tv, a.v_cache, a.num_blocks, a.num_kv_heads, a.head_dim, why)) {
     return 5;
   }
 
