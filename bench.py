@@ -933,11 +933,11 @@ def time_graph(step, steps, warmup, stream, barrier, dist, dev, units, world):
 # the ncu captures summarised in profiles/ (file named below), keyed by the
 # hash of the kernel sources they were taken on: a changed kernel reports null.
 TRAFFIC = {
-    ("llama70b", "auto"): {"bytes": 3774.53e6 + 16.45e6, "kernel_src": "cfe2825b97ee6d57",
+    ("llama70b", "auto"): {"bytes": 3774.52e6 + 16.44e6, "kernel_src": "717825758c1db16c",
                            "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "mma"): {"bytes": 3774.53e6 + 16.45e6, "kernel_src": "cfe2825b97ee6d57",
+    ("llama70b", "mma"): {"bytes": 3774.52e6 + 16.44e6, "kernel_src": "717825758c1db16c",
                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "fp8"): {"bytes": 1892.61e6 + 17.35e6, "kernel_src": "cfe2825b97ee6d57",
+    ("llama70b", "fp8"): {"bytes": 1892.59e6 + 17.28e6, "kernel_src": "717825758c1db16c",
                           "profile": "profiles/decode_step_llama70b_fp8_launches.md"},
     ("cow", "auto"): {"bytes": 268.52e6 + 216.53e6, "kernel_src": "ba3a77c251cf3178",
                       "profile": "profiles/copy_blocks_kernel_cow.md"},
