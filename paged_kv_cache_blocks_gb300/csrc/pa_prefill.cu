@@ -385,39 +385,62 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
 
 // ---------------------------------------------------------------------------
 // tcgen05 version (head_dim 128).  One work item = (KV head, tile of 128 query
-// rows) as above.  Per CTA (one per SM, 10 warps):
-//   warps 4-7  producers: warp 4 takes items from the atomic counter,
-//              publishes them in a two-slot item ring and TMA-loads the
-//              tile's Q (128 rows x 128 dims, one 3-D box of tokens x heads x
-//              dims) into shared memory; all four load the key blocks in
-//              chunks of 8 blocks = 128 keys (K one chunk ahead of V) into
-//              three-stage K and V rings, each warp issuing the copies of two
-//              blocks (K and V of a chunk are 128 swizzled rows per 64-dim
-//              half, so one descriptor spans the chunk).  TMA issue from one
-//              warp is too slow for a chunk;
-//   warp 8     allocates the tensor memory (S | P0 | P1 | O | Q); one
-//              thread issues S = Q K^T (M 128, N 128 keys, K 128 dims) for
-//              chunk c+1 as soon as the softmax of chunk c has read S;
-//   warp 9     one thread issues O += P V (M 128, N 128 dims, K 128 keys)
-//              once the softmax has written P.  Issuing a product blocks the
-//              thread about as long as the product runs, hence two issuers.
-//              Both products take their A operand (Q, P) from tensor memory,
-//              which runs them at the full rate where an A operand in shared
-//              memory halves it; tcgen05.commit signals each result on an
-//              mbarrier;
-//   warps 0-3  one query row per thread (its tensor-memory lane): at the
-//              start of an item, move the row of Q from shared to tensor
-//              memory; per chunk read S, apply the scale and the causal mask,
-//              online softmax in fp32 with the running maximum moved only
-//              when it grows by more than 2^8 (the exact result either way,
-//              fewer rescales of O), scale-and-subtract and row sums on the
-//              packed two-lane fp32 FMA / add, write P as 16-bit values, two
-//              per column, into one of two P buffers, rescale O when the
-//              maximum moved, and finally write O / l.
-// The softmax warpgroup holds 128 scores per thread: it takes registers the
-// producer warpgroup gives back (setmaxnreg), so that nothing spills.
+// rows) as above.  Per CTA (one per SM, 14 warps):
+//   warps 8-11  producers: warp 8 takes items from the atomic counter,
+//               publishes them in a two-slot item ring and TMA-loads the
+//               tile's Q (128 rows x 128 dims, one 3-D box of tokens x heads
+//               x dims) into shared memory; all four load the key blocks in
+//               chunks of 8 blocks = 128 keys (K one chunk ahead of V) into
+//               three-stage K and V rings, each warp issuing the copies of
+//               two blocks (K and V of a chunk are 128 swizzled rows per
+//               64-dim half, so one descriptor spans the chunk).  TMA issue
+//               from one warp is too slow for a chunk;
+//   warp 12     allocates the tensor memory (S | P | O0 | O1 | Q); one thread
+//               issues S = Q K^T (M 128, N 128 keys, K 128 dims) for chunk
+//               c+1 as soon as the softmax of chunk c has read S;
+//   warp 13     one thread issues, per key half hk, O_hk += P[:, 64 hk ..]
+//               V[64 hk .., :] (M 128, N 128 dims, K 64 keys) once that
+//               half's softmax warps have written P.  Issuing a product
+//               blocks the thread about as long as the product runs, hence
+//               two issuers.  Both products take their A operand (Q, P) from
+//               tensor memory, which runs them at the full rate where an A
+//               operand in shared memory halves it; tcgen05.commit signals
+//               each result on an mbarrier;
+//   warps 0-7   two threads per query row (its tensor-memory lane): warp w
+//               takes keys 0-63 of every chunk, warp w + 4 keys 64-127.  At
+//               the start of an item each moves its 64 dims of the Q row from
+//               shared to tensor memory; per chunk it reads its 64 scores,
+//               applies the scale and the causal mask, runs an online softmax
+//               in fp32 with its own running maximum (moved only when it
+//               grows by more than 2^8: the exact result either way, fewer
+//               rescales of its O), scale-and-subtract and row sums on the
+//               packed two-lane fp32 FMA / add, and writes its P as 16-bit
+//               values, two per column.  The halves never wait for each other
+//               inside an item; at its end they exchange (maximum, sum) and
+//               each writes 64 dims of (O0 2^(m0-m) + O1 2^(m1-m)) / l.
+// The softmax warpgroups take registers the producer warpgroup gives back
+// (setmaxnreg), so that nothing spills.
 // Every wait is bounded; a timeout flags PA_DEVERR_TIMEOUT and the CTA
 // drains its copies and tensor-core work before freeing tensor memory.
+
+// One 32-bit tensor-memory column of this thread's lane, stored / loaded
+// and waited for in the same statement.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr), "r"(__float_as_uint(v))
+      : "memory");
+}
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return __uint_as_float(r);
+}
 
 struct TcCfg {
   static constexpr int kHalf = 128 * 128;           // 128 rows x 64 16-bit values
@@ -431,25 +454,27 @@ struct TcCfg {
   static constexpr size_t kOffV = kOffK + static_cast<size_t>(kKStages) * kChunkBytes;
   static constexpr size_t kOffBar = kOffV + static_cast<size_t>(kVStages) * kChunkBytes;
   static constexpr size_t kBytes = kOffBar + 512 + 1024;
-  static constexpr int kSoftmaxWarps = 4;            // warpgroup 0
-  static constexpr int kProducerWarp0 = 4;           // warpgroup 1
+  static constexpr int kSoftmaxWarps = 8;            // warpgroups 0 and 1: key halves 0 and 1
+  static constexpr int kProducerWarp0 = 8;           // warpgroup 2
   static constexpr int kProducerWarps = 4;           // one per SM sub-partition: TMA issue
                                                      // from one warp is too slow for a chunk
-  static constexpr int kMmaWarp = 8;                 // warps 8 (S) and 9 (PV)
+  static constexpr int kMmaWarp = 12;                // warps 12 (S) and 13 (PV)
   static constexpr int kMmaWarps = 2;
   static constexpr int kThreads = 32 * (kMmaWarp + kMmaWarps);
-  // registers per thread: 168 at launch (three warps on one sub-partition);
-  // the producers drop to 80 and the softmax threads rise to 240:
-  // 128 x 240 + 128 x 80 + 64 x 168 = 51712 <= 320 x 168 = 53760
-  static constexpr int kRegsLaunch = 168, kRegsProducer = 80, kRegsSoftmax = 240;
-  // tensor memory: S (128 fp32 columns) | P0 | P1 (128 16-bit values per row
-  // packed into 64 columns each) | O (128 fp32 columns) | Q (128 16-bit
-  // values per row in 64 columns); 448 of the 512 allocated columns
+  // registers per thread: 128 at launch (four warps on one sub-partition);
+  // the producers drop to 64 and the softmax threads rise to 160:
+  // 256 x 160 + 128 x 64 + 64 x 128 = 57344 <= 448 x 128 = 57344
+  static constexpr int kRegsLaunch = 128, kRegsProducer = 64, kRegsSoftmax = 160;
+  // tensor memory: S (128 fp32 columns) | P (128 16-bit values per row in 64
+  // columns, keys 0-63 then 64-127) | O0 | O1 (128 fp32 columns each: the
+  // products over keys 0-63 and 64-127 of every chunk, each half with its own
+  // running maximum) | Q (128 16-bit values per row in 64 columns)
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColP = 128, kColO = 256, kColQ = 384;
+  static constexpr uint32_t kColS = 0, kColP = 128, kColO = 192, kColQ = 448;
 };
 static_assert(TcCfg::kBytes <= 232448, "shared memory of one CTA");
 static_assert(TcCfg::kColQ + 64 <= TcCfg::kTmemCols, "tensor-memory columns");
+static_assert(TcCfg::kColO + 256 <= TcCfg::kColQ, "tensor-memory columns of O0 and O1");
 static_assert(32 * (TcCfg::kSoftmaxWarps * TcCfg::kRegsSoftmax + TcCfg::kProducerWarps * TcCfg::kRegsProducer +
                     TcCfg::kMmaWarps * TcCfg::kRegsLaunch) <= TcCfg::kThreads * TcCfg::kRegsLaunch,
               "register split within the registers the CTA is launched with");
@@ -459,7 +484,8 @@ static_assert(32 * (TcCfg::kSoftmaxWarps * TcCfg::kRegsSoftmax + TcCfg::kProduce
 enum TcBar {
   kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9, kSFull = 12, kSFree = 13, kPFull = 14,
   kODone = 16, kQFull = 18, kQTmem = 19, kItemFull = 20, kItemEmpty = 22, kDrain = 24,
-  kNumTcBars = 25
+  kXFull = 25,   // [quarter][slot]: the two threads of a row published a value (epilogue)
+  kNumTcBars = 33
 };
 static_assert(kNumTcBars * 8 + 16 <= 512, "barrier region");
 
@@ -492,7 +518,7 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
     mbar_init(&bar[kSFull], 1);
     mbar_init(&bar[kSFree], C::kSoftmaxWarps);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bar[kPFull + i], C::kSoftmaxWarps);
+      mbar_init(&bar[kPFull + i], C::kSoftmaxWarps / 2);   // per key half
       mbar_init(&bar[kODone + i], 1);
       mbar_init(&bar[kItemFull + i], 1);
       // helpers (3), MMA issuers (2), softmax (4)
@@ -501,6 +527,7 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
     mbar_init(&bar[kQFull], 1);
     mbar_init(&bar[kQTmem], C::kSoftmaxWarps);
     mbar_init(&bar[kDrain], C::kMmaWarps);
+    for (int i = 0; i < 8; ++i) mbar_init(&bar[kXFull + i], 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -667,16 +694,22 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
           // O += P V of chunk x: A = P from tensor memory (16 keys = 8
           // packed columns per step), B = V (MN-major)
           for (int c = 0; c < nch && ok; ++c, ++cc) {
-            const int vs = cc % C::kVStages, pb = cc & 1;
-            if (!wait(kPFull + pb, (cc >> 1) & 1)) break;
+            const int vs = cc % C::kVStages;
             if (!wait(kVFull + vs, (cc / C::kVStages) & 1)) break;
-            tc_fence_after();
             const uint64_t dV = dV0 + (static_cast<uint64_t>(vs) * C::kChunkBytes >> 4);
+            // key half hk: O_hk += P[:, 64 hk ..] V[64 hk .., :] once that half's
+            // softmax warps wrote their P
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              umma_f16_ts(tbase + C::kColO, tbase + C::kColP + 64 * pb + 8 * ks, dV + ((ks * 2048) >> 4), id_o,
-                          c > 0 || ks > 0);
-            umma_commit(&bar[kODone + pb]);
+            for (int hk = 0; hk < 2; ++hk) {
+              if (!wait(kPFull + hk, cc & 1)) break;
+              tc_fence_after();
+#pragma unroll
+              for (int ks = 4 * hk; ks < 4 * hk + 4; ++ks)
+                umma_f16_ts(tbase + C::kColO + 128 * hk, tbase + C::kColP + 8 * ks, dV + ((ks * 2048) >> 4),
+                            id_o, c > 0 || ks > 4 * hk);
+              umma_commit(&bar[kODone + hk]);
+            }
+            if (!ok) break;
             umma_commit(&bar[kVEmpty + vs]);
           }
         }
@@ -690,16 +723,40 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
+    // two threads per query row: warp w (w < 4) takes keys 0-63 of every
+    // chunk, warp w + 4 keys 64-127, in the same tensor-memory lane quarter.
+    // Each keeps its own running maximum and sum and its own O (O0, O1), so
+    // the two never wait for each other inside an item; at its end they
+    // exchange (maximum, sum) once and each writes 64 of the 128 output
+    // dims of the combined result.
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kRegsSoftmax));
-    const int quarter = warp & 3;
+    const int quarter = warp & 3, half = warp >> 2;
     const int row = 32 * quarter + lane;
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(32 * quarter) << 16);
-    uint32_t it = 0, cc = 0;
+    const uint32_t o_mine = lane_addr + C::kColO + 128 * half;
+    uint32_t it = 0, cc = 0, xk = 0;
     bool ok = true;
     auto wait = [&](int idx, uint32_t parity) {
       if (ok) ok = mbar_wait(&bar[idx], parity, abort_flag, err);
       ok = __all_sync(0xffffffffu, ok);
       return ok;
+    };
+    // one value with the row's other thread, through two tensor-memory
+    // columns of the S buffer (free at an epilogue: the next item's first S
+    // waits for its Q, which these warps write after the epilogue); a slot
+    // is rewritten two exchanges later, after the partner passed the
+    // exchange between
+    auto exchange = [&](float mine) -> float {
+      const uint32_t xs = xk & 1;
+      tmem_st1(lane_addr + C::kColS + 2 * xs + half, mine);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kXFull + 2 * quarter + xs]);
+      wait(kXFull + 2 * quarter + xs, (xk >> 1) & 1);
+      tc_fence_after();
+      const float other = tmem_ld1(lane_addr + C::kColS + 2 * xs + (half ^ 1));
+      ++xk;
+      return other;
     };
     while (ok) {
       const int slot = it & 1;
@@ -717,95 +774,89 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
       const int pos = v.L - v.n + tok;
       const bool valid = tok < v.n && pos >= 0;
       const int lim = valid ? pos : -1;
-      // Q row -> tensor memory (the previous item's products, which read the
-      // old Q, completed before its epilogue).  The TMA box put row `row`
-      // at row * 128 bytes of each 64-dim half, its 16-byte pieces permuted
-      // by the 128-byte swizzle (piece j at j ^ (row & 7)).
+      // this thread's 64 dims of the Q row -> tensor memory (the previous
+      // item's products, which read the old Q, completed before its
+      // epilogue).  The TMA box put row `row` at row * 128 bytes of each
+      // 64-dim half, its 16-byte pieces permuted by the 128-byte swizzle
+      // (piece j at j ^ (row & 7)).
       if (!wait(kQFull, it & 1)) break;
       {
         uint32_t qw[32];
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 u = *reinterpret_cast<const uint4*>(sQ + hf * C::kHalf + row * 128 + ((j ^ (row & 7)) << 4));
-            qw[4 * j] = u.x;
-            qw[4 * j + 1] = u.y;
-            qw[4 * j + 2] = u.z;
-            qw[4 * j + 3] = u.w;
-          }
-          tmem_st32u(lane_addr + C::kColQ + 32 * hf, qw);
+        for (int j = 0; j < 8; ++j) {
+          const uint4 u = *reinterpret_cast<const uint4*>(sQ + half * C::kHalf + row * 128 + ((j ^ (row & 7)) << 4));
+          qw[4 * j] = u.x;
+          qw[4 * j + 1] = u.y;
+          qw[4 * j + 2] = u.z;
+          qw[4 * j + 3] = u.w;
         }
+        tmem_st32u(lane_addr + C::kColQ + 32 * half, qw);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kQTmem]);
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;   // this key half's reference maximum and sum
       for (int c = 0; c < nch; ++c, ++cc) {
         if (!wait(kSFull, cc & 1)) break;
         tc_fence_after();
-        const int k0 = c * 128;
-        float t[128];
-        tmem_ld64(lane_addr + C::kColS, t);
-        tmem_ld64(lane_addr + C::kColS + 64, t + 64);
+        const int kc = c * 128, k0 = kc + 64 * half;
+        float t[64];
+        tmem_ld64(lane_addr + C::kColS + 64 * half, t);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kSFree]);
-        if (!__all_sync(0xffffffffu, k0 + 127 <= lim)) {   // causal mask / tail: -inf
+        if (!__all_sync(0xffffffffu, k0 + 63 <= lim)) {   // causal mask / tail: -inf
 #pragma unroll
-          for (int i = 0; i < 128; ++i) t[i] = k0 + i <= lim ? t[i] : -INFINITY;
+          for (int i = 0; i < 64; ++i) t[i] = k0 + i <= lim ? t[i] : -INFINITY;
         }
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // 4 chains for ILP
 #pragma unroll
-        for (int i = 0; i < 128; ++i) m4[i & 3] = fmaxf(m4[i & 3], t[i]);
+        for (int i = 0; i < 64; ++i) m4[i & 3] = fmaxf(m4[i & 3], t[i]);
         // the scale is positive, so it commutes with the maximum
         const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * P.scale_log2;
         const bool need = mx > m_ref + 8.f;
         const float new_ref = need ? mx : m_ref;
         const float mu = new_ref == -INFINITY ? 0.f : new_ref;
         const float alpha = need ? exp2f(m_ref - new_ref) : 1.f;
-        // P buffer pb is free once the PV of two chunks back has completed
-        const int pb = cc & 1;
-        if (cc >= 2 && !wait(kODone + pb, ((cc >> 1) - 1) & 1)) break;
-        // p = 2^(s * scale - mu) as 16-bit, two per column, into P buffer pb;
-        // row sum in fp32
-        // (pairs of columns on the packed two-lane fp32 FMA / add)
+        // p = 2^(s * scale - mu) as 16-bit, two per column, into this half's
+        // 32 columns of P, once the previous chunk's product over this half
+        // has read them; row sum in fp32 (pairs on the packed two-lane FMA/add)
         const float2 sc2 = make_float2(P.scale_log2, P.scale_log2), nm2 = make_float2(-mu, -mu);
         float2 r2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        uint32_t pk[32];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float2 x = fma2(make_float2(t[64 * q + 2 * i], t[64 * q + 2 * i + 1]), sc2, nm2);
-            const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-            r2[i & 3] = add2(r2[i & 3], p);
-            pk[i] = pack2<T>(p.x, p.y);
-          }
-          tmem_st32u(lane_addr + C::kColP + 64 * pb + 32 * q, pk);
+        for (int i = 0; i < 32; ++i) {
+          const float2 x = fma2(make_float2(t[2 * i], t[2 * i + 1]), sc2, nm2);
+          const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          r2[i & 3] = add2(r2[i & 3], p);
+          pk[i] = pack2<T>(p.x, p.y);
         }
+        if (cc >= 1 && !wait(kODone + half, (cc - 1) & 1)) break;
+        tc_fence_after();
+        tmem_st32u(lane_addr + C::kColP + 32 * half, pk);
         r2[0] = add2(add2(r2[0], r2[1]), add2(r2[2], r2[3]));
         l = l * alpha + (r2[0].x + r2[0].y);
         if (c > 0 && __any_sync(0xffffffffu, need)) {
-          // O must hold the previous chunk's product before it is rescaled
-          if (!wait(kODone + (pb ^ 1), ((cc - 1) >> 1) & 1)) break;
-          tc_fence_after();
+          // this half's O holds the previous chunk's product (waited above)
 #pragma unroll 1
           for (int cb = 0; cb < 4; ++cb) {
             float o32[32];
-            tmem_ld32(lane_addr + C::kColO + cb * 32, o32);
+            tmem_ld32(o_mine + cb * 32, o32);
 #pragma unroll
             for (int i = 0; i < 32; ++i) o32[i] *= alpha;
-            tmem_st32(lane_addr + C::kColO + cb * 32, o32);
+            tmem_st32(o_mine + cb * 32, o32);
           }
         }
         // V rows past the sequence end (the last block's tail) may hold
         // anything, NaN included: zero them so that 0 * NaN never enters O
-        if (k0 + 128 > v.L) {
+        if (kc + 128 > v.L) {
           // the chunk's V copies have landed before their rows are overwritten
           const int vs = cc % C::kVStages;
           if (!wait(kVFull + vs, (cc / C::kVStages) & 1)) break;
-          const int z0 = max(v.L, k0) - k0, z1 = min(k0 + 128, nkb * kBlock) - k0;
+          // this half's product reads only keys 64 half .. 64 half + 63 of the
+          // chunk, and waits only for this half's warps: they zero those rows
+          const int z0 = max(max(v.L, kc) - kc, 64 * half);
+          const int z1 = min(min(kc + 128, nkb * kBlock) - kc, 64 * half + 64);
           uint8_t* sV = smem + C::kOffV + static_cast<size_t>(vs) * C::kChunkBytes;
           for (int i = row; i < (z1 - z0) * 16; i += 128) {   // 16 x 16 B per key row
             const int key = z0 + (i >> 4), part = i & 15;
@@ -816,33 +867,52 @@ __global__ void __launch_bounds__(TcCfg::kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kPFull + pb]);
+        if (lane == 0) mbar_arrive(&bar[kPFull + half]);
         m_ref = new_ref;
       }
       if (!ok) break;
-      // epilogue: out = O / l, one rounding to T
-      if (nch > 0 && !wait(kODone + ((cc - 1) & 1), ((cc - 1) >> 1) & 1)) break;
+      // epilogue: combine the halves, out = (O0 2^(m0 - m) + O1 2^(m1 - m)) /
+      // (l0 2^(m0 - m) + l1 2^(m1 - m)) with m the larger maximum; each thread
+      // writes 64 of the 128 dims, one rounding to T
+      const float m_other = exchange(m_ref);
+      const float l_other = exchange(l);
+      if (!ok) break;
+      if (nch > 0) {
+        if (!wait(kODone + 0, (cc - 1) & 1)) break;
+        if (!wait(kODone + 1, (cc - 1) & 1)) break;
+      }
       tc_fence_after();
       {
-        const float inv = (valid && l > 0.f) ? 1.0f / l : 0.f;
+        const float m0 = half == 0 ? m_ref : m_other, m1 = half == 0 ? m_other : m_ref;
+        const float l0 = half == 0 ? l : l_other, l1 = half == 0 ? l_other : l;
+        const float mm = fmaxf(m0, m1);
+        const float w0 = mm == -INFINITY ? 0.f : exp2f(m0 - mm);
+        const float w1 = mm == -INFINITY ? 0.f : exp2f(m1 - mm);
+        const float lsum = l0 * w0 + l1 * w1;
+        const float inv = (valid && lsum > 0.f) ? 1.0f / lsum : 0.f;
+        const float a0 = w0 * inv, a1 = w1 * inv;
         uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(P.out) +
-                                              ((static_cast<int64_t>(v.q0) + tok) * P.hq + h * G + row % G) * D);
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          float o32[32];
-          if (nch > 0) {   // uniform over the warp: every lane takes part in the load
-            tmem_ld32(lane_addr + C::kColO + cb * 32, o32);
+                                              ((static_cast<int64_t>(v.q0) + tok) * P.hq + h * G + row % G) * D +
+                                              64 * half);
+#pragma unroll 1
+        for (int cb = 0; cb < 2; ++cb) {
+          float x32[32], y32[32];
+          if (nch > 0) {   // uniform over the warp: every lane takes part in the loads
+            tmem_ld32(lane_addr + C::kColO + 64 * half + cb * 32, x32);
+            tmem_ld32(lane_addr + C::kColO + 128 + 64 * half + cb * 32, y32);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o32[i] = 0.f;
+            for (int i = 0; i < 32; ++i) x32[i] = y32[i] = 0.f;
           }
           if (tok < v.n) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              dst[cb * 4 + q4] = make_uint4(pack2<T>(o32[8 * q4] * inv, o32[8 * q4 + 1] * inv),
-                                            pack2<T>(o32[8 * q4 + 2] * inv, o32[8 * q4 + 3] * inv),
-                                            pack2<T>(o32[8 * q4 + 4] * inv, o32[8 * q4 + 5] * inv),
-                                            pack2<T>(o32[8 * q4 + 6] * inv, o32[8 * q4 + 7] * inv));
+            for (int q4 = 0; q4 < 4; ++q4) {
+              float o8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o8[e] = fmaf(x32[8 * q4 + e], a0, y32[8 * q4 + e] * a1);
+              dst[cb * 4 + q4] = make_uint4(pack2<T>(o8[0], o8[1]), pack2<T>(o8[2], o8[3]),
+                                            pack2<T>(o8[4], o8[5]), pack2<T>(o8[6], o8[7]));
+            }
           }
         }
       }
