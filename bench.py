@@ -942,7 +942,7 @@ TRAFFIC = {
     ("cow", "auto"): {"bytes": 268.52e6 + 216.53e6, "kernel_src": "ba3a77c251cf3178",
                       "profile": "profiles/copy_blocks_kernel_cow.md"},
     # the 8 prefill launches of one step (iterations 1..8), summed
-    ("chunked", "auto"): {"bytes": 1285.36e6 + 286.86e6, "kernel_src": "6f58af1f530c2d60",
+    ("chunked", "auto"): {"bytes": 1285.77e6 + 286.73e6, "kernel_src": "0be3bea094e22414",
                           "profile": "profiles/prefill_tc_kernel_chunked.md"},
 }
 
