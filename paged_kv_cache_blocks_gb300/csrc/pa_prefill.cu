@@ -479,13 +479,25 @@ static_assert(32 * (TcCfg::kSoftmaxWarps * TcCfg::kRegsSoftmax + TcCfg::kProduce
                     TcCfg::kMmaWarps * TcCfg::kRegsLaunch) <= TcCfg::kThreads * TcCfg::kRegsLaunch,
               "register split within the registers the CTA is launched with");
 
-// Barrier indices; every ring of n slots has one barrier per slot, so that a
-// parity wait never meets a phase n uses ahead.
-enum TcBar {
-  kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9, kSFull = 12, kSFree = 13, kPFull = 14,
-  kODone = 16, kQFull = 18, kQTmem = 19, kItemFull = 20, kItemEmpty = 22, kDrain = 24,
-  kXFull = 25,   // [quarter][slot]: the two threads of a row published a value (epilogue)
-  kNumTcBars = 33
+// Barrier indices, laid out from the ring sizes; every ring of n slots has
+// one barrier per slot, so that a parity wait never meets a phase n uses
+// ahead.
+enum TcBar : int {
+  kKFull = 0,
+  kKEmpty = kKFull + TcCfg::kKStages,
+  kVFull = kKEmpty + TcCfg::kKStages,
+  kVEmpty = kVFull + TcCfg::kVStages,
+  kSFull = kVEmpty + TcCfg::kVStages,
+  kSFree = kSFull + 1,
+  kPFull = kSFree + 1,        // [key half]
+  kODone = kPFull + 2,        // [key half]
+  kQFull = kODone + 2,
+  kQTmem = kQFull + 1,
+  kItemFull = kQTmem + 1,     // [item slot]
+  kItemEmpty = kItemFull + 2,
+  kDrain = kItemEmpty + 2,
+  kXFull = kDrain + 1,        // [quarter][slot]: the two threads of a row published a value (epilogue)
+  kNumTcBars = kXFull + 8
 };
 static_assert(kNumTcBars * 8 + 16 <= 512, "barrier region");
 
