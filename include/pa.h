@@ -340,7 +340,13 @@ int pa_decode_fp8(const void* d_q, const void* d_k_cache8, const void* d_v_cache
  * length outside [0, max_seq_len], a piece longer than its sequence or
  * offsets out of order are flagged (PA_DEVERR_SEQ_LEN) and clamped, block
  * ids outside the pool read as zeros (PA_DEVERR_BLOCK_ID); the error bits
- * are read with pa_decode_check on this workspace. */
+ * are read with pa_decode_check on this workspace.
+ *
+ * Resources: the tcgen05 kernel runs one CTA per SM with ~226 KB of shared
+ * memory and allocates all 512 tensor-memory columns of its SM for the
+ * CTA's lifetime (the allocation waits while another kernel on the SM
+ * holds tensor memory); num_blocks * num_kv_heads * 16 must stay below
+ * 2^31 (tensor-map row coordinates). */
 size_t pa_prefill_workspace_bytes(int32_t num_seqs, int32_t num_q_tokens, int32_t num_q_heads,
                                   int32_t num_kv_heads);
 
