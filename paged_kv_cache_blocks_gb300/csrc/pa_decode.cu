@@ -292,9 +292,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
 
 template <int D>
 struct Tile {
-  static constexpr int kHalfBytes = 16 * 64 * 2;             // one 16 x 64 box
-  static constexpr int kHalves = D / 64;                     // boxes per K (or V) tile
-  static constexpr int kKVBytes = kHalves * kHalfBytes;      // one K (or V) tile
+  static constexpr int kHalfBytes = 16 * 64 * 2;             // 16 rows x 64 dims, 2048 B apart
+  static constexpr int kHalves = D / 64;                     // 64-dim halves per K (or V) tile
+  static constexpr int kKVBytes = kHalves * kHalfBytes;      // one K (or V) tile: one 3-D box
   static constexpr int kStageBytes = 2 * kKVBytes;           // K then V
 };
 
@@ -1298,6 +1298,9 @@ bool encode_fp8_maps(CUtensorMap* mk, CUtensorMap* mv, const void* kbase, const 
 
 void* tensor_map_encoder(std::string* why) { return reinterpret_cast<void*>(get_encode_fn(why)); }
 
+// The 16-bit caches as a 2-D tensor of token rows (one 16 x 64 box per
+// block and 64-dim half): the prefill kernel's chunk layout puts a block's
+// halves 16 KB apart, so it copies them separately.
 bool encode_cache_map(CUtensorMap* m, const void* base, int64_t num_blocks, int hkv, int D,
                       std::string* why) {
   EncodeTiledFn fn = get_encode_fn(why);
