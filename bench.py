@@ -942,7 +942,7 @@ TRAFFIC = {
     ("cow", "auto"): {"bytes": 268.52e6 + 216.53e6, "kernel_src": "ba3a77c251cf3178",
                       "profile": "profiles/copy_blocks_kernel_cow.md"},
     # the 8 prefill launches of one step (iterations 1..8), summed
-    ("chunked", "auto"): {"bytes": 1286.04e6 + 286.43e6, "kernel_src": "f96d34b762058bd4",
+    ("chunked", "auto"): {"bytes": 1285.08e6 + 286.55e6, "kernel_src": "771ab884a675a98c",
                           "profile": "profiles/prefill_tc_kernel_chunked.md"},
 }
 

@@ -93,21 +93,94 @@ __device__ __forceinline__ int tile_key_blocks(const PieceView& v, int tile, int
   return maxpos < 0 ? 0 : (maxpos + kBlock) / kBlock;
 }
 
+constexpr int kPrepSeqs = 4096;   // sequences whose tile offsets the prep keeps in shared memory
+
 __global__ void __launch_bounds__(1024) prefill_prep_kernel(PrefillParams P) {
   __shared__ int sw[32];
   __shared__ int s_hist[kPrefillBins];
+  __shared__ int s_first[kPrepSeqs + 1];   // first global tile index of each sequence
   __shared__ int s_shift;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, nthr = blockDim.x;
   if (tid == 0) {
     P.ws->error_bits = 0;
     int sh = 0;
     while ((P.max_blocks >> sh) >= kPrefillBins) ++sh;
     s_shift = sh;
   }
-  for (int i = tid; i < kPrefillBins; i += blockDim.x) s_hist[i] = 0;
+  for (int i = tid; i < kPrefillBins; i += nthr) s_hist[i] = 0;
   __syncthreads();
   const int shift = s_shift;
-  for (int b = tid; b < P.num_seqs; b += blockDim.x) {
+  if (P.num_seqs <= kPrepSeqs) {
+    // one thread per (sequence, tile): the tile counts' prefix sum in shared
+    // memory maps a global tile index back to its sequence (binary search),
+    // so a long piece's tiles spread over all threads
+    const int per = (P.num_seqs + nthr - 1) / nthr;   // <= 4 sequences per thread
+    const int b0 = tid * per;
+    int cnt = 0;
+    for (int k = 0; k < per; ++k) {
+      const int b = b0 + k;
+      if (b < P.num_seqs) {
+        const PieceView v = piece_view(P, b, true);   // flags bad input once per sequence
+        const int nt = (v.n + P.tile_tokens - 1) / P.tile_tokens;
+        s_first[b] = nt;                                // count for now
+        cnt += nt;
+      }
+    }
+    __syncthreads();
+    int total_tiles = 0;
+    int run = block_exclusive_scan(cnt, sw, &total_tiles);
+    for (int k = 0; k < per; ++k) {
+      const int b = b0 + k;
+      if (b < P.num_seqs) {
+        const int nt = s_first[b];
+        s_first[b] = run;
+        run += nt;
+      }
+    }
+    if (tid == 0) s_first[P.num_seqs] = total_tiles;
+    __syncthreads();
+    auto locate = [&](int g, int* tile) -> int {   // sequence of global tile g
+      int lo = 0, hi = P.num_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_first[mid] <= g) lo = mid;
+        else hi = mid - 1;
+      }
+      *tile = g - s_first[lo];
+      return lo;
+    };
+    for (int g = tid; g < total_tiles; g += nthr) {
+      int t;
+      const int b = locate(g, &t);
+      const PieceView v = piece_view(P, b, false);
+      atomicAdd(&s_hist[min(tile_key_blocks(v, t, P.tile_tokens) >> shift, kPrefillBins - 1)], 1);
+    }
+    __syncthreads();
+    // start offsets in descending bin order: a scan over the reversed bins
+    int total = 0;
+    const int c = tid < kPrefillBins ? s_hist[kPrefillBins - 1 - tid] : 0;
+    const int off = block_exclusive_scan(c, sw, &total);
+    if (tid < kPrefillBins) s_hist[kPrefillBins - 1 - tid] = off;
+    __syncthreads();
+    for (int g = tid; g < total_tiles; g += nthr) {
+      int t;
+      const int b = locate(g, &t);
+      const PieceView v = piece_view(P, b, false);
+      const int kb = tile_key_blocks(v, t, P.tile_tokens);
+      const int slot = atomicAdd(&s_hist[min(kb >> shift, kPrefillBins - 1)], 1);
+      // overlapping pieces (offsets out of order, already flagged) cannot
+      // overflow the list: records past its capacity are dropped
+      if (slot < P.max_entries) P.entries[slot] = make_int4(b, t, kb, 0);
+    }
+    if (tid == 0) {
+      if (total > P.max_entries) atomicOr(&P.ws->error_bits, kErrSeqLen);
+      P.ws->n_entries = min(total, P.max_entries);
+      P.ws->next_item = 0;
+    }
+    return;
+  }
+  // many sequences: one thread per sequence walks its tiles
+  for (int b = tid; b < P.num_seqs; b += nthr) {
     const PieceView v = piece_view(P, b, true);
     const int nt = (v.n + P.tile_tokens - 1) / P.tile_tokens;
     for (int t = 0; t < nt; ++t)
@@ -120,14 +193,12 @@ __global__ void __launch_bounds__(1024) prefill_prep_kernel(PrefillParams P) {
   const int off = block_exclusive_scan(c, sw, &total);
   if (tid < kPrefillBins) s_hist[kPrefillBins - 1 - tid] = off;
   __syncthreads();
-  for (int b = tid; b < P.num_seqs; b += blockDim.x) {
+  for (int b = tid; b < P.num_seqs; b += nthr) {
     const PieceView v = piece_view(P, b, false);
     const int nt = (v.n + P.tile_tokens - 1) / P.tile_tokens;
     for (int t = 0; t < nt; ++t) {
       const int kb = tile_key_blocks(v, t, P.tile_tokens);
       const int slot = atomicAdd(&s_hist[min(kb >> shift, kPrefillBins - 1)], 1);
-      // overlapping pieces (offsets out of order, already flagged) cannot
-      // overflow the list: records past its capacity are dropped
       if (slot < P.max_entries) P.entries[slot] = make_int4(b, t, kb, 0);
     }
   }

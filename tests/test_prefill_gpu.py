@@ -238,3 +238,17 @@ def test_prefill_random_batches(pa, seed, variant):
     pb = W.make_prefill_batch(name, seed=20 + seed, lens=lens, pieces=pieces)
     got, ref, _ = run(pa, pb, variant=variant)
     U.assert_close_rounded(got, ref, pb.workload.dtype, f"random batch {seed} variant {variant}")
+
+
+@pytest.mark.parametrize("nseq", [4096, 4100])
+def test_prefill_many_sequences(pa, nseq):
+    """Thousands of sequences (decode tokens and short pieces): the prep kernel
+    lists tiles from a shared-memory prefix sum up to 4096 sequences and per
+    sequence beyond; both against the oracle on every row."""
+    rng = np.random.default_rng(nseq)
+    lens = rng.integers(1, 65, nseq)
+    pieces = np.minimum(lens, np.where(rng.random(nseq) < 0.9, 1, rng.integers(1, 40, nseq)))
+    pieces[rng.random(nseq) < 0.05] = 0
+    pb = W.make_prefill_batch("llama8b", seed=40, lens=lens.tolist(), pieces=pieces.tolist())
+    got, ref, _ = run(pa, pb, variant=3)
+    U.assert_close_rounded(got, ref, "bf16", f"{nseq} sequences")
