@@ -17,7 +17,8 @@
 //                        schedules: it takes items from an atomic counter
 //                        (one ahead) and stages each item's partition record
 //                        and block ids in a two-slot item ring.  Warp 1 (one
-//                        thread) streams each block's K and V tiles into a
+//                        thread; FP8: warps 1 and 2, alternate stages)
+//                        streams each block's K and V tiles into a
 //                        ring of shared-memory stages with TMA (128-byte
 //                        swizzle), completion on mbarriers, without ever
 //                        waiting on global memory.  The other warps consume blocks
@@ -735,7 +736,11 @@ constexpr size_t align_up_c(size_t x, size_t a) { return (x + a - 1) / a * a; }
 template <typename T, int D, int NC, int S, bool kFma, bool kFp8 = false>
 struct AttendCfg {
   static_assert(S % NC == 0, "within an item, each ring stage must be consumed by one warp");
-  static constexpr int kThreads = 32 * (NC + 2);  // scheduler, TMA, NC consumers
+  // copy warps: FP8 stages (4 KB as two 2 KB boxes) drain faster than one
+  // thread issues their copies, so two warps issue alternate stages
+  static constexpr int kIss = kFp8 ? 2 : 1;
+  static_assert(S % kIss == 0, "each ring stage must be refilled by one copy warp");
+  static constexpr int kThreads = 32 * (NC + 1 + kIss);  // scheduler, copy warps, NC consumers
   static constexpr int kKBytes = kFp8 ? kBlock * D : Tile<D>::kKVBytes;  // K part of a stage
   static constexpr int kStageBytes = kFp8 ? 2 * kBlock * D : Tile<D>::kStageBytes;
   static constexpr size_t kStagesOff = 0;
@@ -750,10 +755,9 @@ struct AttendCfg {
   static constexpr size_t kBytes = kAbortOff + 16 + 1024;  // + slack to 1024-align the base
 };
 
-template <typename T, int D, int NC, int S, bool kFma, int HPG, bool kFp8 = false>
-__global__ void __launch_bounds__(32 * (NC + 2))
-    attend_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const DecodeParams P) {
+template <typename T, int D, int NC, int S, bool kFma, int HPG, bool kFp8>
+__device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                            const DecodeParams& P) {
   using Cfg = AttendCfg<T, D, NC, S, kFma, kFp8>;
   using State = typename std::conditional<
       kFp8, Fp8State<T, D>,
@@ -782,7 +786,7 @@ __global__ void __launch_bounds__(32 * (NC + 2))
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&item_full[s], 1);
-      mbar_init(&item_empty[s], NC + 1);  // consumers + the TMA thread
+      mbar_init(&item_empty[s], NC + Cfg::kIss);  // consumers + the copy threads
       mbar_init(&merge_full[s], NC);
     }
     *abort_flag = 0;
@@ -840,10 +844,13 @@ __global__ void __launch_bounds__(32 * (NC + 2))
     return;
   }
 
-  if (warp == 1) {
+  if (warp <= Cfg::kIss) {
     // ---------------------------------------------------------------- TMA
-    // One thread streams every block of every item into the stage ring.
+    // One thread per copy warp streams the blocks into the stage ring; with
+    // two copy warps, warp 1 + i issues the blocks g with g % 2 == i of the
+    // CTA's block stream, so each stage is refilled by one thread, in order.
     if (lane != 0) return;
+    const uint32_t iss = static_cast<uint32_t>(warp - 1);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     const int64_t y_oob = P.num_blocks * P.hkv * kBlock;  // one past the pool: reads as zeros
@@ -859,6 +866,7 @@ __global__ void __launch_bounds__(32 * (NC + 2))
         break;
       }
       for (int j = 0; j < inf.nblk; ++j, ++g) {
+        if (g % Cfg::kIss != iss) continue;  // the other copy warp's stage
         const int st = g % S;
         ok = mbar_wait(&empty[st], ((g / S) & 1) ^ 1, abort_flag, err);
         if (!ok) break;
@@ -883,6 +891,7 @@ __global__ void __launch_bounds__(32 * (NC + 2))
       // Abort: let the copies this CTA issued land before it exits.
       const uint32_t lo = g > static_cast<uint32_t>(S) ? g - S : 0;
       for (uint32_t k = lo; k < g; ++k) {
+        if (k % Cfg::kIss != iss) continue;
         unsigned long long t0 = global_timer_ns();
         while (!mbar_try_wait(&full[k % S], (k / S) & 1) &&
                global_timer_ns() - t0 < kWaitLimitNs / 4) {
@@ -893,7 +902,7 @@ __global__ void __launch_bounds__(32 * (NC + 2))
   }
 
   // ---------------------------------------------------------------- consumers
-  const int w = warp - 2;
+  const int w = warp - 1 - Cfg::kIss;
   const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
   float* scr = scratch + (kFma ? w * FmaScratch<D>::kFloats : 0);
   State st;
@@ -963,6 +972,25 @@ __global__ void __launch_bounds__(32 * (NC + 2))
       }
     }
   }
+}
+
+// The tensor maps live in kernel parameter space (__grid_constant__); the body
+// takes their addresses for the copies.
+template <typename T, int D, int NC, int S, bool kFma, int HPG>
+__global__ void __launch_bounds__(32 * (NC + 2))
+    attend_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const DecodeParams P) {
+  attend_body<T, D, NC, S, kFma, HPG, false>(tm_k, tm_v, P);
+}
+
+// FP8 caches: two copy warps, two CTAs per SM (16 stages of 4 KB each).  One
+// copy thread per CTA left the FP8 kernel short of copies in flight at this
+// tile size (316 vs 309 us on the Llama-3-70B-shaped batch).
+template <typename T, int D, int NC, int S>
+__global__ void __launch_bounds__(32 * (NC + 3), 2)
+    attend_fp8_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const DecodeParams P) {
+  attend_body<T, D, NC, S, false, 1, true>(tm_k, tm_v, P);
 }
 
 // ---------------------------------------------------------------------------
@@ -1354,7 +1382,12 @@ template <typename T, int D, int NC, int S, bool kFma, int HPG, bool kFp8 = fals
 bool launch_attend(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& P,
                    int64_t max_items, cudaStream_t stream, std::string* why) {
   using Cfg = AttendCfg<T, D, NC, S, kFma, kFp8>;
-  auto kern = attend_kernel<T, D, NC, S, kFma, HPG, kFp8>;
+  void (*kern)(CUtensorMap, CUtensorMap, DecodeParams);
+  if constexpr (kFp8) {
+    kern = attend_fp8_kernel<T, D, NC, S>;
+  } else {
+    kern = attend_kernel<T, D, NC, S, kFma, HPG>;
+  }
   static int occ_cache[64] = {0};  // per device ordinal
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1538,10 +1571,10 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   const int64_t max_items = L.max_parts * a.num_kv_heads;
   const int variant = a.variant == 0 ? 2 : a.variant;
   bool ok;
-  if (a.fp8) {  // head_dim 128 only; 8 stages of 4 KB let three CTAs share an SM
+  if (a.fp8) {  // head_dim 128 only; 16 stages of 4 KB, two copy warps, two CTAs per SM
     ok = a.dtype == 1
-             ? launch_attend<__nv_bfloat16, 128, 4, 8, false, 1, true>(tk, tv, P, max_items, s, why)
-             : launch_attend<__half, 128, 4, 8, false, 1, true>(tk, tv, P, max_items, s, why);
+             ? launch_attend<__nv_bfloat16, 128, 4, 16, false, 1, true>(tk, tv, P, max_items, s, why)
+             : launch_attend<__half, 128, 4, 16, false, 1, true>(tk, tv, P, max_items, s, why);
   } else if (a.dtype == 1) {
     ok = a.head_dim == 128
              ? dispatch_attend<__nv_bfloat16, 128>(variant, P.G, tk, tv, P, max_items, s, why)
