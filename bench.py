@@ -209,6 +209,16 @@ def gpu_identity(local_rank):
 
 # --------------------------------------------------------------------------- CPU oracle
 
+REF_RUN_S = 150.0   # default oracle time of a whole reference-arm run (warm-up + timed steps), s
+
+
+def ref_step_budget(args):
+    """Seconds of oracle work per reference-arm step, so that the whole
+    ``--steps K --warmup W`` run stays within ``--ref-seconds`` whatever K and
+    W are."""
+    return args.ref_seconds / max(1, args.steps + args.warmup)
+
+
 def oracle_sample_rows(lens, n_long):
     """Rows of the workload keeping its short/long mix: n_long of the long
     sequences and 9 x n_long of the short ones (all when the mix is flat)."""
@@ -277,34 +287,51 @@ def prefill_flops(lens, pieces, hq, d):
     return 4 * total * hq * d
 
 
+class PrefillOracleSample:
+    """One iteration of the chunked workload (by default the last, whose rows
+    are the most expensive) set up once for the fp64 oracle; ``run(n_rows)``
+    times it on ``n_rows`` query rows spread over the prompt piece and scales
+    to FLOP/s."""
+
+    def __init__(self, threads=None, seed=0, iteration=None):
+        import oracle
+        oracle.build()
+        from paged_kv_cache_blocks_gb300 import workloads as W
+        self.oracle = oracle
+        self.threads = threads or len(os.sched_getaffinity(0))
+        self.iteration = iteration or W.CHUNK_PIECES
+        self.pb = W.make_prefill_batch("chunked", seed=seed, iteration=self.iteration,
+                                       poison=False)
+        kc, vc = self.pb.placed_pools()
+        self.q = self.pb.q.numpy().view(np.uint16)
+        self.kc, self.vc = kc.numpy().view(np.uint16), vc.numpy().view(np.uint16)
+        self.n = int(self.pb.pieces[0])
+
+    def run(self, n_rows):
+        pb, w = self.pb, self.pb.workload
+        rows = np.linspace(0, self.n - 1, n_rows).astype(np.int64)
+        t0 = time.perf_counter()
+        self.oracle.prefill(self.q, self.kc, self.vc, pb.block_tables, pb.seq_lens, pb.q_offsets,
+                            w.scale, w.dtype, rows=rows, threads=self.threads)
+        dt = time.perf_counter() - t0
+        base = int(pb.seq_lens[0]) - self.n
+        fl = sum(4 * (base + int(r) + 1) * w.num_q_heads * w.head_dim for r in rows)
+        return fl / dt / 1e12, dt, (f"{n_rows} query tokens of piece {self.iteration} of 8 of the "
+                                    f"30000-token prompt (positions {base + rows[0]}.."
+                                    f"{base + rows[-1]}, all 64 heads), fp64, "
+                                    f"{self.threads} OpenMP threads")
+
+
 def prefill_cpu_baseline(threads=None, n_rows=None, seed=0, budget_s=12.0):
-    """The fp64 oracle on query rows spread over the last iteration's prompt
-    piece (the most expensive rows), scaled to FLOP/s; ``n_rows=None`` sizes
-    the sample to about ``budget_s`` seconds from an 8-row probe."""
+    """The fp64 oracle on query rows of the last iteration's prompt piece,
+    scaled to FLOP/s; ``n_rows=None`` sizes the sample to about ``budget_s``
+    seconds from an 8-row probe."""
+    smp = PrefillOracleSample(threads, seed)
     if n_rows is None:
-        v, sec, cores, _ = prefill_cpu_baseline(threads, 8, seed)
+        _, sec, _ = smp.run(8)
         n_rows = int(max(8, min(3750, round(8 * budget_s / max(sec, 1e-3)))))
-    import oracle
-    oracle.build()
-    from paged_kv_cache_blocks_gb300 import workloads as W
-    threads = threads or len(os.sched_getaffinity(0))
-    pb = W.make_prefill_batch("chunked", seed=seed, iteration=W.CHUNK_PIECES, poison=False)
-    w = pb.workload
-    kc, vc = pb.placed_pools()
-    n = int(pb.pieces[0])
-    rows = np.linspace(0, n - 1, n_rows).astype(np.int64)
-    q = pb.q.numpy().view(np.uint16)
-    kcn, vcn = kc.numpy().view(np.uint16), vc.numpy().view(np.uint16)
-    t0 = time.perf_counter()
-    oracle.prefill(q, kcn, vcn, pb.block_tables, pb.seq_lens, pb.q_offsets, w.scale, w.dtype,
-                   rows=rows, threads=threads)
-    dt = time.perf_counter() - t0
-    base = int(pb.seq_lens[0]) - n
-    fl = sum(4 * (base + int(r) + 1) * w.num_q_heads * w.head_dim for r in rows)
-    return fl / dt / 1e12, dt, threads, (f"{n_rows} query tokens of the 8th piece of the "
-                                         f"30000-token prompt (positions {base + rows[0]}.."
-                                         f"{base + rows[-1]}, all 64 heads), fp64, "
-                                         f"{threads} OpenMP threads")
+    v, dt, sample = smp.run(n_rows)
+    return v, dt, smp.threads, sample
 
 
 def run_prefill(args, rank, world, local_rank):
@@ -505,26 +532,40 @@ def cow_pairs(seed):
     return perm[:COW_PAIRS].clone(), perm[COW_PAIRS:2 * COW_PAIRS].clone()
 
 
+class CowOracleSample:
+    """``pairs`` block pairs of the copy workload's shape in a pool of
+    2 x pairs blocks, set up once; ``run()`` times the oracle's block copy
+    (single-threaded C, plus the copies of the caches its Python wrapper
+    returns, which grow with the pool)."""
+
+    def __init__(self, pairs):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.pairs = pairs
+        g = np.random.default_rng(7)
+        nb = 2 * pairs
+        self.kc = g.integers(0, 1 << 16, (nb, 8, 16, 128), dtype=np.uint16)
+        self.vc = g.integers(0, 1 << 16, (nb, 8, 16, 128), dtype=np.uint16)
+        perm = g.permutation(nb).astype(np.int32)
+        self.src, self.dst = perm[:pairs], perm[pairs:]
+        oracle.copy_blocks(self.kc[:4], self.vc[:4], self.src[:0], self.dst[:0])  # load the library
+        self.sample = (f"{pairs} pairs in a pool of {nb} blocks of the same shape "
+                       "(oracle_copy_blocks, one thread, with the wrapper's copies of both caches)")
+
+    def run(self):
+        t0 = time.perf_counter()
+        self.oracle.copy_blocks(self.kc, self.vc, self.src, self.dst)
+        sec = time.perf_counter() - t0
+        moved = 2 * self.pairs * 2 * 8 * 16 * 128 * 2
+        return moved / sec / 1e9, sec
+
+
 def cow_cpu_baseline(pairs=COW_PAIRS):
-    """The oracle's block copy (single-threaded C, plus the copies of the
-    caches its Python wrapper returns) on a sample: `pairs` pairs in a pool of
-    2 x pairs blocks of the same shape."""
-    import oracle
-    oracle.build()
-    g = np.random.default_rng(7)
-    nb = 2 * pairs
-    kc = g.integers(0, 1 << 16, (nb, 8, 16, 128), dtype=np.uint16)
-    vc = g.integers(0, 1 << 16, (nb, 8, 16, 128), dtype=np.uint16)
-    perm = g.permutation(nb).astype(np.int32)
-    src, dst = perm[:pairs], perm[pairs:]
-    oracle.copy_blocks(kc[:4], vc[:4], src[:0], dst[:0])   # load the library
-    t0 = time.perf_counter()
-    oracle.copy_blocks(kc, vc, src, dst)
-    sec = time.perf_counter() - t0
-    moved = 2 * pairs * 2 * 8 * 16 * 128 * 2
-    return moved / sec / 1e9, sec, (f"{pairs} pairs in a pool of {nb} blocks of the same shape "
-                                    "(oracle_copy_blocks, one thread, with the wrapper's copies "
-                                    "of both caches)")
+    """The oracle's block copy on a sample of ``pairs`` pairs."""
+    smp = CowOracleSample(pairs)
+    v, sec = smp.run()
+    return v, sec, smp.sample
 
 
 def run_cow(args, rank, world, local_rank):
@@ -653,21 +694,24 @@ def run_cow(args, rank, world, local_rank):
 
 
 def run_reference_cow(args, rank, world):
-    """The oracle's block copy as the reference arm of the copy workload."""
+    """The oracle's block copy as the reference arm of the copy workload:
+    each step the same sample of pairs, sized from a 64-pair probe so that
+    the whole run fits ``--ref-seconds``."""
     if rank != 0:
         return 0
-    vals = []
-    for _ in range(args.warmup + args.steps):
-        v, sec, sample = cow_cpu_baseline()
-        vals.append((v, sec))
-    v = statistics.fmean(x for x, _ in vals[args.warmup:])
-    sec = statistics.fmean(s for _, s in vals[args.warmup:])
+    _, t64 = CowOracleSample(64).run()
+    pairs = int(max(16, min(COW_PAIRS, 64 * ref_step_budget(args) // max(t64, 1e-6))))
+    smp = CowOracleSample(pairs)
+    vals = [smp.run() for _ in range(args.warmup + args.steps)][args.warmup:]
+    v = statistics.fmean(x for x, _ in vals)
+    sec = statistics.fmean(t for _, t in vals)
     line = {"impl": "reference", "metric": COW_METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": {"workload": DESCR["cow"], "parallelism": "oracle, one thread"},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
-                             "cpu_model": cpu_model()},
+            "data": "synthetic", "config": {"workload": DESCR["cow"], "parallelism": "oracle, one thread",
+                                            "sample": smp.sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": smp.sample, "cpu_model": cpu_model()},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -682,13 +726,20 @@ def run_reference(args, rank, world):
     from paged_kv_cache_blocks_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]
     threads = len(os.sched_getaffinity(0))
-    lens_all = W.workload_lengths(args.workload, 0)
-    per_step = min(12.0, 150.0 / max(1, args.steps + args.warmup))
+    lens_all = np.asarray(W.workload_lengths(args.workload, 0))
+    # each step the same sample of the workload's sequences, as large as the
+    # per-step budget allows: probe the smallest sample that keeps the
+    # short/long mix, scale it up, or fall back to short sequences alone
+    budget = ref_step_budget(args)
+    mixed = bool((lens_all > 10 * np.median(lens_all)).any())
     rows = oracle_sample_rows(lens_all, 1)
-    t1, lens, _ = time_oracle(args.workload, rows, threads)
-    if (np.asarray(lens_all) > 10 * np.median(lens_all)).any():
-        n_long = int(max(1, min(26, round(per_step / max(t1, 1e-3)))))
-        rows = oracle_sample_rows(lens_all, n_long)
+    t1, _, _ = time_oracle(args.workload, rows, threads)
+    if t1 <= budget:
+        rows = oracle_sample_rows(lens_all, int(min(26 if mixed else len(lens_all), budget // t1)))
+    elif mixed:
+        short_rows = np.flatnonzero(lens_all <= 10 * np.median(lens_all))
+        ts, _, _ = time_oracle(args.workload, short_rows[:1], threads)
+        rows = short_rows[:int(max(1, min(len(short_rows), budget // max(ts, 1e-6))))]
     import oracle as O
     b = W.make_batch(args.workload, seed=0, poison=False,
                      lens_override=np.asarray(lens_all)[rows].tolist())
@@ -1147,22 +1198,32 @@ def run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped=F
 
 
 def run_reference_prefill(args, rank, world):
-    """The oracle as the reference arm of the chunked workload: each step a
-    bounded sample of query rows, FLOP/s scaled from that sample."""
+    """The oracle as the reference arm of the chunked workload: each step the
+    same sample of query rows, sized from a four-row probe so that the whole
+    run fits ``--ref-seconds``; FLOP/s scaled from the sample."""
     if rank != 0:
         return 0
-    threads = len(os.sched_getaffinity(0))
+    budget = ref_step_budget(args)
+    smp = PrefillOracleSample()
+    _, t4, _ = smp.run(4)
+    if t4 / 4 > budget:
+        # one row of the last piece (~28k visible keys) is over the budget:
+        # take rows of the first piece (at most 3,750 visible keys) instead
+        smp = PrefillOracleSample(iteration=1)
+        _, t4, _ = smp.run(4)
+    n_rows = int(max(1, min(smp.n, budget // max(t4 / 4, 1e-6))))
     for _ in range(args.warmup):
-        prefill_cpu_baseline(threads, n_rows=1)
-    vals = []
-    t0 = time.perf_counter()
+        smp.run(n_rows)
+    vals, secs = [], []
     for _ in range(args.steps):
-        v, sec, cores, sample = prefill_cpu_baseline(threads, n_rows=1)
+        v, sec, sample = smp.run(n_rows)
         vals.append(v)
-    dt = (time.perf_counter() - t0) / max(1, args.steps)
+        secs.append(sec)
     val = statistics.fmean(vals)
+    threads = smp.threads
     line = {"impl": "reference", "metric": PREFILL_METRIC, "value": val, "unit": "TFLOP/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": statistics.fmean(secs) * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": DESCR["chunked"], "sample": sample},
             "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -1184,6 +1245,9 @@ def main():
     ap.add_argument("--variant", default="auto", choices=sorted(VARIANTS))
     ap.add_argument("--impl", default="pa", choices=["pa", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--ref-seconds", type=float, default=REF_RUN_S,
+                    help="--impl reference: oracle seconds for the whole run; each step's "
+                         "sample of the workload is sized to fit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fp8", action="store_true",

@@ -4,6 +4,7 @@ import json
 import os
 import subprocess
 import sys
+import time
 
 import pytest
 
@@ -21,9 +22,11 @@ def _bench(args, env_extra=None):
                           env=env, capture_output=True, text=True, timeout=600)
 
 
-@pytest.mark.parametrize("workload,unit", [("tiny", "GB/s"), ("chunked", "TFLOP/s")])
-def test_reference_arm_prints_one_contract_line(workload, unit):
-    r = _bench(["--workload", workload, "--steps", "1", "--warmup", "0"])
+@pytest.mark.parametrize("workload,unit,seconds", [("tiny", "GB/s", "4"),
+                                                   ("chunked", "TFLOP/s", "4"),
+                                                   ("cow", "GB/s", "0.05")])
+def test_reference_arm_prints_one_contract_line(workload, unit, seconds):
+    r = _bench(["--workload", workload, "--steps", "1", "--warmup", "0", "--ref-seconds", seconds])
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -47,3 +50,17 @@ def test_reference_arm_other_ranks_exit_without_work():
                {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_reference_arm_sizes_its_sample_to_the_run_budget():
+    """Many steps shrink each step's sample instead of stretching the run:
+    the mixed 70B-shaped batch at 400 steps and a 6 s budget still ends
+    quickly, with the steps asked for."""
+    t0 = time.perf_counter()
+    r = _bench(["--steps", "400", "--warmup", "3", "--ref-seconds", "6"])
+    elapsed = time.perf_counter() - t0
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][0])
+    assert d["steps"] == 400 and d["warmup"] == 3
+    assert d["ms_per_step"] < 1000 * 6 / 403 * 3      # about the per-step budget
+    assert elapsed < 120
