@@ -197,11 +197,17 @@ int pa_copy_blocks(void* d_k_cache, void* d_v_cache, int64_t num_blocks, int32_t
  *                    initialisation and are overwritten by every call, so
  *                    calls sharing one workspace must not overlap in time.
  *
+ * Built shapes: dtype PA_F16 or PA_BF16, head_dim 64 or 128, G =
+ * num_q_heads / num_kv_heads of 1, 2, 4 or 8 (query heads h*G .. h*G+G-1
+ * share KV head h); anything else returns PA_ERR_UNSUPPORTED.
+ *
  * Accumulation is fp32 (online softmax over 16-token blocks; sequences
- * longer than 512 tokens are split into 512-token partitions whose partial
- * results a second kernel merges), with one rounding to the element type at
- * the end.  Bad device data never faults: it is clamped or read as zeros
- * and flagged in the workspace (pa_decode_check). */
+ * longer than one partition are split into partitions of 512, 1024 or 2048
+ * tokens -- the prep kernel takes the largest that still leaves every SM
+ * enough work -- whose partial results a second kernel merges), with one
+ * rounding to the element type at the end.  Bad device data never faults:
+ * it is clamped or read as zeros and flagged in the workspace
+ * (pa_decode_check). */
 size_t pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                  int32_t max_seq_len);
 
