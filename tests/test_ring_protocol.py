@@ -15,7 +15,12 @@ no consumer ever reads a stage holding another block: safe for every S that
 is a multiple of NC, unsafe (stale reads or deadlock) for S = 6 or 10 with
 NC = 4.  The alternative rule (block g of the CTA's whole stream to consumer
 g % NC) is safe too, but makes the per-warp grouping of sums depend on
-scheduling, so outputs would not be bit-reproducible."""
+scheduling, so outputs would not be bit-reproducible.
+
+The FP8 kernel has two copy threads: thread p refills the stages of the
+blocks g with g % 2 == p, in order, each independently of the other (one
+may run ahead).  The model runs P independent producers the same way and
+checks that the protocol stays safe with them."""
 import random
 
 import pytest
@@ -49,7 +54,7 @@ class Barrier:
             self.pending = self.count
 
 
-def simulate(S, NC, rule, items, seed):
+def simulate(S, NC, rule, items, seed, producers=1):
     """Returns the number of stale reads (0 = protocol safe), or -1 if the
     protocol deadlocks (nobody can move for a long time)."""
     rng = random.Random(seed)
@@ -73,7 +78,8 @@ def simulate(S, NC, rule, items, seed):
 
     cons = [{"it": 0, "list": blocks_of(w, 0), "pos": 0, "at_merge": False} for w in range(NC)]
     merge_arrived = [0] * len(items)
-    next_issue = 0
+    assert S % producers == 0           # each stage has one producer
+    next_issue = list(range(producers))  # producer p issues blocks p, p + P, ...
     stale = 0
     t = 0
     done = [False] * NC
@@ -87,15 +93,17 @@ def simulate(S, NC, rule, items, seed):
             _, s, blk = rec
             stage_tag[s] = blk
             full[s].complete_tx(1)
-        actor = rng.randrange(NC + 1)
-        if actor == NC:                 # producer issues the next block
-            if next_issue < total:
-                s, r = next_issue % S, next_issue // S
+        actor = rng.randrange(NC + producers)
+        if actor >= NC:                 # producer p issues its next block
+            p = actor - NC
+            nxt = next_issue[p]
+            if nxt < total:
+                s, r = nxt % S, nxt // S
                 if empty[s].try_wait((r & 1) ^ 1):
                     full[s].expect_tx(1)
-                    stage_tag[s] = ("landing", next_issue)
-                    in_flight.append((t + rng.randint(1, 40), s, next_issue))
-                    next_issue += 1
+                    stage_tag[s] = ("landing", nxt)
+                    in_flight.append((t + rng.randint(1, 40), s, nxt))
+                    next_issue[p] += producers
             continue
         c = cons[actor]
         if done[actor]:
@@ -135,8 +143,18 @@ def test_stage_multiple_of_consumers_never_reads_a_stale_stage(S, NC, rule):
         assert simulate(S, NC, rule, random_items(rng, 12), seed) == 0
 
 
+@pytest.mark.parametrize("producers", [1, 2])
 @pytest.mark.parametrize("S", [6, 10])
-def test_stages_not_a_multiple_of_consumers_are_unsafe(S):
+def test_stages_not_a_multiple_of_consumers_are_unsafe(S, producers):
     rng = random.Random(7)
-    results = [simulate(S, 4, "item", random_items(rng, 12), seed) for seed in range(10)]
+    results = [simulate(S, 4, "item", random_items(rng, 12), seed, producers)
+               for seed in range(10)]
     assert any(r != 0 for r in results)     # stale reads or deadlock
+
+
+@pytest.mark.parametrize("rule", ["item", "global"])
+@pytest.mark.parametrize("S,NC", [(16, 4), (8, 4), (4, 4), (8, 2), (8, 8)])
+def test_two_producers_on_alternate_stages_never_read_a_stale_stage(S, NC, rule):
+    rng = random.Random(S * 1000 + NC)
+    for seed in range(40):
+        assert simulate(S, NC, rule, random_items(rng, 12), seed, producers=2) == 0
