@@ -17,6 +17,7 @@ Parts:
 Every function cites the passage it follows in its own docstring or in the
 header of ``pa_oracle.c``.
 """
+import concurrent.futures
 import ctypes
 import os
 import subprocess
@@ -287,3 +288,80 @@ def prefill(q, k_cache, v_cache, block_tables, seq_lens, q_offsets, scale, dtype
     if rc != 0:
         raise MemoryError("oracle_prefill could not allocate its gather buffers")
     return out
+
+
+def prefill_dense(q, k_cache, v_cache, block_tables, seq_lens, q_offsets, scale, dtype, rows=None,
+                  block_size=16, row_chunk=256, handle=None):
+    """The same result as :func:`prefill` -- fp64 causal attention of every
+    query token of each sequence's piece over the sequence's paged K/V -- with
+    numpy's matrix product as the step that forms the dot products, for
+    pieces of thousands of tokens over tens of thousands of keys, where the
+    scalar loops of :func:`prefill` take tens of minutes.
+
+    Definition, as for :func:`prefill` ("Yerel LLM sistemlerinde
+    backpressure ve olcekleme", section "4. Prefill ve decode"; "vLLM ve
+    Triton ile maliyet optimizasyonu", section 03, the scaled dot-product
+    attention paragraph): sequence b holds seq_lens[b] tokens; its piece is
+    the last n_b = q_offsets[b+1] - q_offsets[b] of them, so query j sits at
+    position p = seq_lens[b] - n_b + j and sees tokens 0 .. p.  Query head i
+    reads KV head i // G.  Steps, per sequence and KV head: gather the
+    sequence's K and V through its table row into contiguous fp64 arrays
+    (:func:`gather`, exact); then per query head and group of query rows
+    (rows are independent, so grouping them changes nothing):
+    S = scale * Q K^T, entries of keys past each row's position set to -inf,
+    each row's maximum subtracted, exp, P = exp / row sum, out = P V.
+    Returns out [len(rows), Hq, D] float64 (rows default: all).
+    """
+    q = _c(q, np.uint16)
+    block_tables, seq_lens = _c(block_tables, np.int32), _c(seq_lens, np.int32)
+    q_offsets = _c(q_offsets, np.int32)
+    Tq, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    G = Hq // Hkv
+    B = seq_lens.shape[0]
+    assert Hq % Hkv == 0 and q_offsets.shape == (B + 1,) and q_offsets[0] == 0
+    assert q_offsets[-1] == Tq
+    want = np.zeros(Tq, bool)
+    if rows is None:
+        want[:] = True
+    else:
+        rows = np.asarray(rows, np.int64)
+        if rows.size and (rows.min() < 0 or rows.max() >= Tq):
+            raise ValueError("prefill_dense: a row is out of range")
+        want[rows] = True
+    qd = bits_to_double(q, dtype, handle=handle)
+    out = np.zeros((Tq, Hq, D), np.float64)
+    for b in range(B):
+        a, e = int(q_offsets[b]), int(q_offsets[b + 1])
+        n, L = e - a, int(seq_lens[b])
+        if n < 0 or n > L:
+            raise ValueError("prefill_dense: a piece is longer than its sequence, or q_offsets "
+                             "decreases")
+        if n == 0 or not want[a:e].any():
+            continue
+        pos = L - n + np.arange(n)                      # position of each query of the piece
+
+        def one_kv_head(h, a=a, n=n, L=L, pos=pos, b=b):
+            K = gather(k_cache, dtype, block_tables[b], L, h, block_size, handle)
+            V = gather(v_cache, dtype, block_tables[b], L, h, block_size, handle)
+            for c0 in range(0, n, row_chunk):
+                rr = np.arange(c0, min(n, c0 + row_chunk))
+                rr = rr[want[a + rr]]
+                if rr.size == 0:
+                    continue
+                hi = int(pos[rr[-1]]) + 1               # keys any of these rows can see
+                future = np.arange(hi)[None, :] > pos[rr][:, None]
+                for g in range(G):
+                    i = h * G + g
+                    S = qd[a + rr, i, :] @ K[:hi].T
+                    S *= scale
+                    S[future] = -np.inf
+                    S -= S.max(axis=1, keepdims=True)
+                    np.exp(S, out=S)                    # S now holds the unnormalised weights
+                    out[a + rr, i, :] = (S @ V[:hi]) / S.sum(axis=1, keepdims=True)
+
+        # KV heads are independent and write disjoint outputs; numpy and the
+        # gather release the interpreter lock, so they run in threads
+        with concurrent.futures.ThreadPoolExecutor(max_workers=min(Hkv, os.cpu_count() or 1)) as ex:
+            list(ex.map(one_kv_head, range(Hkv)))
+    return out if rows is None else out[rows]

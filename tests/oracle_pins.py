@@ -420,9 +420,88 @@ def pin_prefill_relabel_invariance(oracle, handle=None):
     assert np.array_equal(a, b)
 
 
+# ---- the dense form of the prefill oracle (matrix products as a step) ---------------
+
+def _prefill_dense(oracle, pb, handle, rows=None, pools=None):
+    w = pb.workload
+    kc, vc = pb.placed_pools() if pools is None else pools
+    return oracle.prefill_dense(pb.q.numpy().view(np.uint16), kc.numpy().view(np.uint16),
+                                vc.numpy().view(np.uint16), pb.block_tables, pb.seq_lens,
+                                pb.q_offsets, w.scale, w.dtype, rows=rows, handle=handle)
+
+
+def pin_prefill_dense_matches_sdpa(oracle, handle=None):
+    """The library routine on every row of the small batches, both mask forms."""
+    for pb in prefill_batches():
+        got = _prefill_dense(oracle, pb, handle)
+        for causal in (False, True):
+            err = np.max(np.abs(got - sdpa_prefill_reference(pb, causal)))
+            assert err <= 1e-12, ("dense", pb.workload.name, causal, err)
+
+
+def pin_prefill_dense_matches_loop_form(oracle, handle=None):
+    """The scalar-loop prefill oracle (itself pinned to the library routine,
+    causality, closed forms and relabelling) on the small batches and on
+    rows across the first piece of the 30,000-token chunked workload (a piece
+    of 3,750 tokens, 64 query heads, several row groups), to 1e-12."""
+    for pb in prefill_batches():
+        err = np.max(np.abs(_prefill_dense(oracle, pb, handle) - _prefill(oracle, pb, handle)))
+        assert err <= 1e-12, ("dense vs loop", pb.workload.name, err)
+    pb = W.make_prefill_batch("chunked", seed=0, iteration=1)
+    rows = np.array([0, 1, 255, 256, 257, 1000, 1875, 3000, 3749, 3750, 3769], np.int64)
+    kc, vc = pb.placed_pools()
+    err = np.max(np.abs(_prefill_dense(oracle, pb, handle, rows=rows, pools=(kc, vc))
+                        - _prefill(oracle, pb, handle, rows=rows, pools=(kc, vc))))
+    assert err <= 1e-12, ("dense vs loop, chunked rows", err)
+
+
+def pin_prefill_dense_causal_and_closed_forms(oracle, handle=None):
+    """A query never sees a later token (only the last row changes when the
+    last token's K/V change); position 0 of a whole prompt gives its own v
+    exactly; constant V gives the constant; relabelling the physical blocks
+    gives bit-identical output; a subset of rows gives those rows."""
+    pb = prefill_batches()[1]
+    kc, vc = pb.placed_pools()
+    full = _prefill_dense(oracle, pb, handle, pools=(kc, vc))
+    b = 4
+    last = int(pb.seq_lens[b]) - 1
+    s = int(pb.block_tables[b, last // 16]) * 16 + last % 16
+    kc2, vc2 = kc.clone(), vc.clone()
+    kc2[s // 16, :, s % 16, :] = pb.new_k[0]
+    vc2[s // 16, :, s % 16, :] = -vc2[s // 16, :, s % 16, :]
+    mod = _prefill_dense(oracle, pb, handle, pools=(kc2, vc2))
+    q1 = int(pb.q_offsets[b + 1])
+    same = np.ones(pb.num_q_tokens, bool)
+    same[q1 - 1] = False
+    assert np.max(np.abs(full[same] - mod[same])) <= 1e-15, "a query saw a later token"
+    assert not np.allclose(full[q1 - 1], mod[q1 - 1]), "the last query missed its own token"
+    rows = np.array([q1 - 1, 0, 37, 38, 53, q1 - 64], np.int64)
+    assert np.max(np.abs(_prefill_dense(oracle, pb, handle, rows=rows) - full[rows])) <= 1e-14
+    perm = np.random.default_rng(9).permutation(pb.num_blocks)
+    inv = torch.from_numpy(np.argsort(perm))
+    pb2 = W.PrefillBatch(**{**pb.__dict__, "block_tables": perm[pb.block_tables].astype(np.int32)})
+    assert np.array_equal(_prefill_dense(oracle, pb2, handle, pools=(kc[inv], vc[inv])), full)
+    tb = prefill_batches()[0]                          # tiny: fp16, d 64, G 2
+    w = tb.workload
+    got = _prefill_dense(oracle, tb, handle)
+    for bb in range(len(tb.seq_lens)):
+        if tb.pieces[bb] == tb.seq_lens[bb]:
+            q0 = int(tb.q_offsets[bb])
+            v0 = lib_f64(tb.contiguous_kv(bb)[1][0], w.dtype)
+            for i in range(w.num_q_heads):
+                assert np.array_equal(got[q0, i], v0[i // w.group_size]), ("dense position 0", bb, i)
+    tkc, tvc = tb.placed_pools()
+    tvc = torch.full_like(tvc, int(np.float16(-1.25).view(np.int16)))
+    got = _prefill_dense(oracle, tb, handle, pools=(tkc, tvc))
+    assert np.allclose(got, -1.25, rtol=0, atol=1e-14), "dense constant V"
+
+
+DENSE_PINS = [pin_prefill_dense_matches_sdpa, pin_prefill_dense_matches_loop_form,
+              pin_prefill_dense_causal_and_closed_forms]
+
 ALL_PINS = [pin_kv_bytes, pin_bits, pin_cache_write_golden, pin_copy_blocks_golden,
             pin_e4m3_codes, pin_cache_write_fp8_golden, pin_decode_fp8_reduces_to_decode,
             pin_gather_is_contiguous_source,
             pin_matches_sdpa, pin_relabel_invariance, pin_closed_forms,
             pin_prefill_matches_sdpa, pin_prefill_causal_and_rows, pin_prefill_closed_forms,
-            pin_prefill_relabel_invariance]
+            pin_prefill_relabel_invariance] + DENSE_PINS

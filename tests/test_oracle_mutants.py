@@ -81,3 +81,40 @@ def test_some_pin_catches_mutant(oracle_mod, tmp_path, name, occurrence):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin detects mutant {name}"
+
+
+# Plausible mistakes in the dense (matrix-product) form of the prefill
+# oracle, planted in a copy of its Python source.
+PY_MUTANTS = {
+    "dense_scale_dropped": ("S *= scale", "S *= 1.0"),
+    "dense_mask_off_by_one": ("np.arange(hi)[None, :] > pos[rr][:, None]",
+                              "np.arange(hi)[None, :] >= pos[rr][:, None]"),
+    "dense_not_normalised": ("/ S.sum(axis=1, keepdims=True)", "/ 1.0"),
+    "dense_gqa_mapping": ("i = h * G + g", "i = g * Hkv + h"),
+    "dense_pv_reads_keys": ("(S @ V[:hi])", "(S @ K[:hi])"),
+    "dense_position_base": ("pos = L - n + np.arange(n)", "pos = np.arange(n)"),
+    "dense_last_key_dropped": ("hi = int(pos[rr[-1]]) + 1", "hi = int(pos[rr[-1]])"),
+    "dense_max_not_subtracted": ("S -= S.max(axis=1, keepdims=True)", "S -= 0.0"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_some_pin_catches_dense_mutant(oracle_mod, name):
+    import inspect
+    import textwrap
+    import types
+    src = textwrap.dedent(inspect.getsource(oracle_mod.prefill_dense))
+    old, new = PY_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} missing from prefill_dense"
+    ns = dict(vars(oracle_mod))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    shim = types.SimpleNamespace(**{k: getattr(oracle_mod, k) for k in dir(oracle_mod)
+                                    if not k.startswith("__")})
+    shim.prefill_dense = ns["prefill_dense"]
+    caught = []
+    for pin in P.DENSE_PINS:
+        try:
+            pin(shim)
+        except Exception:     # a failed check, or a mutant that cannot even run
+            caught.append(pin.__name__)
+    assert caught, f"no pin detects mutant {name}"
