@@ -48,7 +48,9 @@ typedef enum {
     PA_ERR_INVALID = 1,      /* bad argument, shape, id or size */
     PA_ERR_OOM = 2,          /* the allocator's free queue cannot cover the request */
     PA_ERR_UNSUPPORTED = 3,  /* dtype / head_dim / group size with no compiled kernel */
-    PA_ERR_SHARED_WRITE = 4, /* reserved: write into a block held by several sequences */
+    PA_ERR_SHARED_WRITE = 4, /* pa_seq_append_slots: a write would land in a block held by
+                                several sequences and the call gave no room to report
+                                the copy-on-write pair that must precede it */
     PA_ERR_CUDA = 5,         /* a CUDA call failed (launch, tensor map, copy) */
     PA_ERR_DEVICE = 6        /* a kernel flagged bad data (see pa_decode_check) */
 } pa_status;
@@ -61,8 +63,11 @@ enum {
     PA_DEVERR_SEQ_LEN = 1,   /* a seq_len < 0 or > max_seq_len: clamped into range */
     PA_DEVERR_BLOCK_ID = 2,  /* a block id outside [0, num_blocks): read as zeros */
     PA_DEVERR_TIMEOUT = 4,   /* an internal wait gave up; the output is not valid */
-    PA_DEVERR_GROUP = 8      /* pa_decode_grouped: a group's offsets or shared prefix were
+    PA_DEVERR_GROUP = 8,     /* pa_decode_grouped: a group's offsets or shared prefix were
                                 invalid; those sequences were decoded without sharing */
+    PA_DEVERR_PLAN = 16      /* PA_DECODE_REUSE_PLAN: the workspace's plan did not fit this
+                                call (records outside its buffers were skipped, or a length
+                                differed from seq_lens); the output is not valid */
 };
 
 const char* pa_last_error_string(void);
@@ -124,9 +129,16 @@ int pa_seq_free(pa_alloc_t* a, int64_t seq_id);
  *                    updated in place with the entries that changed
  *   seq_lens_io      [n_seqs]                optional (NULL): new lengths
  *
- * All or nothing: if the free queue cannot cover the call (new blocks plus
- * copy targets), or cow_capacity or max_blocks is too small, nothing changes
- * and PA_ERR_OOM / PA_ERR_INVALID is returned. */
+ * All or nothing, and nothing changes when the call fails:
+ *   PA_ERR_INVALID       unknown or repeated sequence, or a row would need
+ *                        more than max_blocks entries;
+ *   PA_ERR_SHARED_WRITE  a token would be written into a block another
+ *                        sequence still holds and the copy-on-write pairs do
+ *                        not fit cow_capacity (or the cow arrays are NULL):
+ *                        the write would change the other holders' tokens;
+ *   PA_ERR_OOM           the free queue cannot cover the new blocks plus the
+ *                        copy targets.
+ * The checks run in that order. */
 int pa_seq_append_slots(pa_alloc_t* a, const int64_t* seq_ids, int32_t n_seqs,
                         int32_t tokens_each, int64_t* slot_mapping_out,
                         int32_t* cow_src_out, int32_t* cow_dst_out, int32_t cow_capacity,
@@ -222,11 +234,21 @@ int pa_decode(const void* d_q, const void* d_k_cache, const void* d_v_cache, int
 enum {
     /* Reuse the plan the previous decode on this workspace computed (its
      * partition list and merge records): the prep kernel is skipped.  The
-     * caller guarantees that seq_lens, block_tables, num_seqs, max_seq_len,
-     * the head counts, head_dim and (for pa_decode_grouped) the groups are
-     * those of that call, and that it completed on this stream or one
-     * ordered after it; q, the caches and out may differ -- e.g. the layers
-     * of one decode step.  Not for pa_prefill. */
+     * caller guarantees that seq_lens, num_seqs, max_seq_len, the head
+     * counts, head_dim and (for pa_decode_grouped) the groups are those of
+     * that call, and that it runs on this stream or one ordered after it;
+     * q, the caches, block_tables' entries and out may differ -- e.g. the
+     * layers of one decode step.  Not for pa_prefill.
+     *   Checked on the host: the library records, per device and workspace
+     *   address, the shapes (num_seqs, max_blocks_per_seq, max_seq_len, head
+     *   counts, head_dim, number of groups) of the last planning call; a
+     *   reuse without a matching record returns PA_ERR_INVALID and launches
+     *   nothing.  A prefill on the workspace drops its record.
+     *   Checked on the device: plan records that do not fit this call's
+     *   workspace and sequences are skipped, and a planned length that
+     *   differs from seq_lens is flagged; both set PA_DEVERR_PLAN.  Stale
+     *   plan data therefore never addresses memory outside the call's
+     *   buffers. */
     PA_DECODE_REUSE_PLAN = 1
 };
 
@@ -237,7 +259,16 @@ typedef struct {
     int32_t flags;           /* PA_DECODE_* bits (decode calls only) */
     void* event_before_main; /* optional cudaEvent_t recorded just before the attention */
     void* event_after_main;  /* kernel and just after it, on the same stream */
-    int64_t reserved[4];
+    int32_t partition_tokens; /* decode calls: 0 = the prep kernel chooses (the default);
+                                512, 1024 or 2048 = split every sequence into partitions of
+                                exactly this many tokens (a sequence no longer than one
+                                partition is then not split at all); anything else is
+                                PA_ERR_INVALID.  Ignored with PA_DECODE_REUSE_PLAN (the
+                                plan keeps its size).  The result is the same up to the
+                                fp32 summation order, which the tests use to compare split
+                                and unsplit decodes of one sequence. */
+    int32_t reserved32;
+    int64_t reserved[3];
 } pa_decode_opts;
 
 int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache,
@@ -392,6 +423,9 @@ int pa_selftest_bounded_wait(int64_t limit_ns, int32_t* d_status, void* stream);
  *   - Calls no cudaMalloc/cudaFree or other allocating routine.
  *   - The first call on a device looks up the array's device address (and
  *     may load the module); make that first call before any stream capture.
+ *     The address is kept for the process: after cudaDeviceReset the
+ *     array may move, so do not call this entry point again on a device
+ *     that was reset.
  *   - Every call on a device shares the array and leaves its contents
  *     behind; each call rewrites what it reads, but calls whose kernels may
  *     overlap on the GPU (unordered streams) race on it and must not be

@@ -32,13 +32,18 @@ ones):
 * append_slots is all-or-nothing: if the free queue cannot cover every new
   block (and copy-on-write target) of the call, nothing changes and OOM is
   returned.
+* A call that would write into a block other sequences still hold, but
+  gives no room (``cow_capacity``) to report the copy that must come first,
+  is refused with SHARED_WRITE before anything changes: the write would
+  alter the other holders' tokens ("vLLM ve Triton", section 03, the
+  copy-on-write paragraph).  This check precedes the OOM check.
 * A fork shares the blocks covering the parent's first ``prefix_tokens``
   tokens.  If the last of them is only partly covered, the next write into
   it from either holder triggers copy-on-write.
 * Sequence ids are handed out as 0, 1, 2, ... and never reused.
 """
 
-OK, ERR_INVALID, ERR_OOM = 0, 1, 2
+OK, ERR_INVALID, ERR_OOM, ERR_SHARED_WRITE = 0, 1, 2, 4
 
 
 class AllocError(Exception):
@@ -107,11 +112,21 @@ class AllocatorModel:
         need += max(0, -(-(n + tokens - have) // bs))
         return need
 
-    def append_slots(self, seq_ids, tokens_each):
-        """Returns (slot_mapping, cow_pairs); slot order is seq-major."""
+    def _writes_shared(self, s, tokens):
+        """True when the sequence's next token lands in a block another holds."""
+        n = s["len"]
+        return (tokens > 0 and bool(s["table"]) and n % self.block_size != 0
+                and self.ref[s["table"][-1]] > 1)
+
+    def append_slots(self, seq_ids, tokens_each, cow_capacity=None):
+        """Returns (slot_mapping, cow_pairs); slot order is seq-major.
+        ``cow_capacity``: room for copy-on-write pairs (None = unlimited)."""
         if tokens_each < 0 or len(set(seq_ids)) != len(seq_ids):
             raise AllocError(ERR_INVALID, "bad token count or repeated sequence")
         seqs = [self._get(sid) for sid in seq_ids]
+        n_shared = sum(1 for s in seqs if self._writes_shared(s, tokens_each))
+        if cow_capacity is not None and n_shared > cow_capacity:
+            raise AllocError(ERR_SHARED_WRITE, "write into a shared block without room for its copy")
         if sum(self._needs(s, tokens_each) for s in seqs) > len(self.free):
             raise AllocError(ERR_OOM, "free queue exhausted")
         bs = self.block_size

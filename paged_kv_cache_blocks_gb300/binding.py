@@ -16,7 +16,8 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_UNSUPPORTED, PA_ERR_SHARED_WRITE, PA_ERR_CUDA, \
     PA_ERR_DEVICE = range(7)
 PA_F16, PA_BF16 = 0, 1
-PA_DEVERR_SEQ_LEN, PA_DEVERR_BLOCK_ID, PA_DEVERR_TIMEOUT, PA_DEVERR_GROUP = 1, 2, 4, 8
+PA_DEVERR_SEQ_LEN, PA_DEVERR_BLOCK_ID, PA_DEVERR_TIMEOUT, PA_DEVERR_GROUP, PA_DEVERR_PLAN = \
+    1, 2, 4, 8, 16
 BLOCK_SIZE = 16
 
 _STATUS = {0: "PA_OK", 1: "PA_ERR_INVALID", 2: "PA_ERR_OOM", 3: "PA_ERR_UNSUPPORTED",
@@ -37,7 +38,8 @@ class PaStats(ctypes.Structure):
 class PaDecodeOpts(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("event_before_main", ctypes.c_void_p), ("event_after_main", ctypes.c_void_p),
-                ("reserved", ctypes.c_int64 * 4)]
+                ("partition_tokens", ctypes.c_int32), ("reserved32", ctypes.c_int32),
+                ("reserved", ctypes.c_int64 * 3)]
 
 
 _lib = None
@@ -46,13 +48,14 @@ _lib = None
 PA_DECODE_REUSE_PLAN = 1
 
 
-def _opts(variant, events, stream, flags=0):
+def _opts(variant, events, stream, flags=0, partition_tokens=0):
     """pa_decode_opts for a call, or None for the defaults."""
-    if not (variant or events or flags):
+    if not (variant or events or flags or partition_tokens):
         return None
     o = PaDecodeOpts()
     o.variant = variant
     o.flags = flags
+    o.partition_tokens = partition_tokens
     if events:
         for e in events:       # torch creates the CUDA event lazily, on first record
             if not e.cuda_event:
@@ -148,6 +151,12 @@ def _need(cond, what):
         raise TypeError(what)
 
 
+def _need_reuse_workspace(reuse_plan, workspace):
+    """A reused plan lives in the planning call's workspace: a fresh one has none."""
+    if reuse_plan and workspace is None:
+        raise ValueError("reuse_plan needs the workspace of the call that made the plan")
+
+
 # --------------------------------------------------------------------------- device calls
 
 def pa_cache_write(k, v, slot_mapping, k_cache, v_cache, dtype=None, stream=None):
@@ -176,7 +185,8 @@ def pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim, max_seq_len):
 
 
 def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0, out=None,
-              workspace=None, dtype=None, variant=0, events=None, stream=None, reuse_plan=False):
+              workspace=None, dtype=None, variant=0, events=None, stream=None, reuse_plan=False,
+              partition_tokens=0):
     """out[b, i] = softmax(scale q[b,i] K_b^T) V_b over each sequence's paged K/V.
 
     q [B, Hq, D]; caches [NB, Hkv, 16, D]; block_tables [B, max_blocks] int32;
@@ -185,8 +195,10 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0,
     allocated when None).  ``events`` = (before, after) torch.cuda.Event pair
     recorded around the attention kernel.  ``reuse_plan``: skip the prep
     kernel and reuse the plan of the previous call on this workspace (same
-    lengths, tables and shapes; e.g. the later layers of one step).
+    lengths and shapes; e.g. the later layers of one step).
+    ``partition_tokens``: 0 (the prep kernel chooses) or 512 / 1024 / 2048.
     """
+    _need_reuse_workspace(reuse_plan, workspace)
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens)
     _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
           "block_tables and seq_lens must be int32")
@@ -196,12 +208,11 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, max_seq_len=0,
     msl = max_seq_len if max_seq_len > 0 else mb * BLOCK_SIZE
     if out is None:
         out = torch.empty_like(q)
-    need = pa_decode_workspace_bytes(B, Hq, D, msl)
     if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    if reuse_plan and workspace is None:
-        raise ValueError("reuse_plan needs the workspace of the planning call")
-    opts = _opts(variant, events, stream, PA_DECODE_REUSE_PLAN if reuse_plan else 0)
+        workspace = torch.empty(max(pa_decode_workspace_bytes(B, Hq, D, msl), 256),
+                                dtype=torch.uint8, device=q.device)
+    opts = _opts(variant, events, stream, PA_DECODE_REUSE_PLAN if reuse_plan else 0,
+                 partition_tokens)
     rc = lib().pa_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), NB, _ptr(block_tables), mb,
                             _ptr(seq_lens), B, msl, Hq, Hkv, D, float(scale), _dtype_code(q, dtype),
                             _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream), opts)
@@ -215,6 +226,8 @@ def pa_decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, max_se
     64 MiB static device array inside libpa (batches needing more are
     rejected).  Allocates nothing itself when ``out`` is given."""
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens)
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_tables and seq_lens must be int32")
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
@@ -247,7 +260,12 @@ def pa_decode_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_len
                   reuse_plan=False):
     """pa_decode over E4M3 caches (see pa_cache_write_fp8 for the layout);
     ``events`` and ``reuse_plan`` as for pa_decode."""
+    _need_reuse_workspace(reuse_plan, workspace)
     _need_cuda(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_lens)
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_tables and seq_lens must be int32")
+    _need(k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32,
+          "k_scale and v_scale must be float32")
     B, Hq, D = q.shape
     NB, Hkv = k_cache8.shape[0], k_cache8.shape[1]
     mb = block_tables.shape[1]
@@ -276,7 +294,10 @@ def pa_decode_grouped(q, k_cache, v_cache, block_tables, seq_lens, scale, group_
     """pa_decode where contiguous groups of sequences share a prefix:
     group_offsets [G+1] and group_prefix_tokens [G] are int32 CUDA tensors.
     ``events`` bracket the attention kernel over the members' own tokens."""
+    _need_reuse_workspace(reuse_plan, workspace)
     _need_cuda(q, k_cache, v_cache, block_tables, seq_lens, group_offsets, group_prefix_tokens)
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_tables and seq_lens must be int32")
     _need(group_offsets.dtype == torch.int32 and group_prefix_tokens.dtype == torch.int32,
           "group_offsets and group_prefix_tokens must be int32")
     B, Hq, D = q.shape

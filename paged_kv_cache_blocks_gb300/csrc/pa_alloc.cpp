@@ -155,8 +155,12 @@ int pa_seq_append_slots(pa_alloc_t* a, const int64_t* seq_ids, int32_t n_seqs, i
         return fail(PA_ERR_INVALID, "pa_seq_append_slots: a table row would exceed max_blocks");
     }
   }
+  // A write into a block other sequences still hold must be preceded by a
+  // copy; a call that cannot report the copy would write into the shared block.
   if (n_cow > 0 && (!cow_src_out || !cow_dst_out || n_cow > cow_capacity))
-    return fail(PA_ERR_INVALID, "pa_seq_append_slots: copy-on-write pairs exceed cow_capacity");
+    return fail(PA_ERR_SHARED_WRITE,
+                "pa_seq_append_slots: a write would land in a shared block and the copy-on-write "
+                "pairs exceed cow_capacity");
   if (need > static_cast<int64_t>(a->free_q.size()))
     return fail(PA_ERR_OOM, "pa_seq_append_slots: free queue cannot cover the request");
 

@@ -2,7 +2,12 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <map>
+#include <mutex>
 #include <string>
+#include <utility>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/pa.h"
 #include "pa_device.cuh"
@@ -29,6 +34,64 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool supported_head_dim(int32_t d) { return d == 64 || d == 128; }
 
+// An NVTX range around one library call, visible to Nsight tools (no cost
+// beyond a function-pointer check when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Shapes of the decode call that last planned into a workspace (keyed by
+// device and workspace address).  A call with PA_DECODE_REUSE_PLAN is refused
+// unless its workspace holds a plan made for the same shapes, so a stale or
+// foreign workspace never reaches the kernels as a plan.  A prefill on the
+// workspace, or a planning call that fails, drops the record.
+struct PlanShape {
+  int32_t num_seqs, max_blocks_per_seq, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+      num_groups;
+  bool operator==(const PlanShape& o) const {
+    return num_seqs == o.num_seqs && max_blocks_per_seq == o.max_blocks_per_seq &&
+           max_seq_len == o.max_seq_len && num_q_heads == o.num_q_heads &&
+           num_kv_heads == o.num_kv_heads && head_dim == o.head_dim && num_groups == o.num_groups;
+  }
+};
+using PlanKey = std::pair<int, uintptr_t>;
+constexpr size_t kMaxPlanRecords = 4096;  // beyond this the oldest-keyed records are dropped
+std::mutex g_plan_mu;
+std::map<PlanKey, PlanShape> g_plans;
+
+PlanKey plan_key(const void* ws) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    dev = -1;
+  }
+  return PlanKey(dev, reinterpret_cast<uintptr_t>(ws));
+}
+
+bool plan_matches(const void* ws, const PlanShape& shape) {
+  const PlanKey k = plan_key(ws);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  auto it = g_plans.find(k);
+  return it != g_plans.end() && it->second == shape;
+}
+
+void plan_forget(const void* ws) {
+  const PlanKey k = plan_key(ws);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  g_plans.erase(k);
+}
+
+void plan_record(const void* ws, const PlanShape& shape) {
+  const PlanKey k = plan_key(ws);
+  std::lock_guard<std::mutex> lock(g_plan_mu);
+  if (g_plans.size() >= kMaxPlanRecords && g_plans.find(k) == g_plans.end())
+    g_plans.erase(g_plans.begin());
+  g_plans[k] = shape;
+}
+
 }  // namespace
 
 extern "C" {
@@ -40,6 +103,7 @@ const char* pa_version(void) { return "libpa 0.1 (sm_103a)"; }
 int pa_cache_write(const void* d_k, const void* d_v, const int64_t* d_slot_mapping, int32_t num_tokens,
                    int32_t num_kv_heads, int32_t head_dim, void* d_k_cache, void* d_v_cache,
                    int64_t num_blocks, int32_t dtype, void* stream) {
+  NvtxRange nvtx("pa_cache_write");
   if (num_tokens < 0) return fail(PA_ERR_INVALID, "pa_cache_write: num_tokens < 0");
   if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_cache_write: dtype");
   if (!supported_head_dim(head_dim))
@@ -62,6 +126,7 @@ int pa_cache_write_fp8(const void* d_k, const void* d_v, const int64_t* d_slot_m
                        int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim,
                        const float* d_k_scale, const float* d_v_scale, void* d_k_cache8,
                        void* d_v_cache8, int64_t num_blocks, int32_t dtype, void* stream) {
+  NvtxRange nvtx("pa_cache_write_fp8");
   if (num_tokens < 0) return fail(PA_ERR_INVALID, "pa_cache_write_fp8: num_tokens < 0");
   if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_cache_write_fp8: dtype");
   if (head_dim != 128) return fail(PA_ERR_UNSUPPORTED, "pa_cache_write_fp8: head_dim must be 128");
@@ -83,6 +148,7 @@ int pa_cache_write_fp8(const void* d_k, const void* d_v, const int64_t* d_slot_m
 int pa_copy_blocks(void* d_k_cache, void* d_v_cache, int64_t num_blocks, int32_t num_kv_heads,
                    int32_t head_dim, const int32_t* d_src, const int32_t* d_dst, int32_t n_pairs,
                    void* stream) {
+  NvtxRange nvtx("pa_copy_blocks");
   if (n_pairs < 0) return fail(PA_ERR_INVALID, "pa_copy_blocks: n_pairs < 0");
   if (!supported_head_dim(head_dim))
     return fail(PA_ERR_UNSUPPORTED, "pa_copy_blocks: head_dim must be 64 or 128");
@@ -148,6 +214,9 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
     return fail(PA_ERR_INVALID, "pa_decode: opts->variant must be 0, 1 or 2");
   if (opts && (opts->flags & ~PA_DECODE_REUSE_PLAN))
     return fail(PA_ERR_INVALID, "pa_decode: unknown opts->flags bits");
+  if (opts && opts->partition_tokens != 0 && opts->partition_tokens != pa::kPartTokens &&
+      opts->partition_tokens != 2 * pa::kPartTokens && opts->partition_tokens != 4 * pa::kPartTokens)
+    return fail(PA_ERR_INVALID, "pa_decode: opts->partition_tokens must be 0, 512, 1024 or 2048");
   if (num_seqs == 0) return PA_OK;
   const int64_t per_seq_parts = (max_seq_len + pa::kPartTokens - 1) / pa::kPartTokens;
   if (static_cast<int64_t>(num_seqs) * per_seq_parts * num_kv_heads > INT32_MAX)
@@ -168,6 +237,16 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
     return fail(PA_ERR_INVALID, num_groups > 0
                                     ? "pa_decode_grouped: workspace smaller than pa_decode_grouped_workspace_bytes()"
                                     : "pa_decode: workspace smaller than pa_decode_workspace_bytes()");
+
+  const bool reuse = opts && (opts->flags & PA_DECODE_REUSE_PLAN);
+  const PlanShape shape{num_seqs, max_blocks_per_seq, max_seq_len, num_q_heads, num_kv_heads,
+                        head_dim, num_groups};
+  if (reuse && !plan_matches(d_workspace, shape))
+    return fail(PA_ERR_INVALID,
+                "pa_decode: PA_DECODE_REUSE_PLAN needs a workspace planned by a decode call "
+                "with the same num_seqs, max_blocks_per_seq, max_seq_len, head counts, head_dim "
+                "and groups");
+  if (!reuse) plan_forget(d_workspace);
 
   pa::DecodeArgs a;
   a.q = d_q;
@@ -190,7 +269,8 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
   a.variant = opts ? opts->variant : 0;
   a.ev_before = opts ? opts->event_before_main : nullptr;
   a.ev_after = opts ? opts->event_after_main : nullptr;
-  a.reuse_plan = opts && (opts->flags & PA_DECODE_REUSE_PLAN);
+  a.reuse_plan = reuse;
+  a.partition_tokens = opts ? opts->partition_tokens : 0;
   a.group_off = d_group_offsets;
   a.group_prefix = d_group_prefix_tokens;
   a.num_groups = num_groups;
@@ -199,7 +279,12 @@ int decode_common(const void* d_q, const void* d_k_cache, const void* d_v_cache,
   a.v_scale = d_v_scale;
   std::string why;
   int rc = pa::decode_launch(a, &why);
-  return rc ? fail(rc, why) : PA_OK;
+  if (rc) {
+    plan_forget(d_workspace);
+    return fail(rc, why);
+  }
+  if (!reuse) plan_record(d_workspace, shape);
+  return PA_OK;
 }
 
 }  // namespace
@@ -211,6 +296,7 @@ int pa_decode_ex(const void* d_q, const void* d_k_cache, const void* d_v_cache, 
                  int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                  int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
                  size_t workspace_bytes, void* stream, const pa_decode_opts* opts) {
+  NvtxRange nvtx("pa_decode");
   return decode_common(d_q, d_k_cache, d_v_cache, num_blocks, d_block_tables, max_blocks_per_seq,
                        d_seq_lens, num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, scale,
                        dtype, d_out, d_workspace, workspace_bytes, stream, opts, nullptr, nullptr, 0);
@@ -228,6 +314,7 @@ int pa_decode_fp8(const void* d_q, const void* d_k_cache8, const void* d_v_cache
                   int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                   int32_t head_dim, float scale, int32_t dtype, void* d_out, void* d_workspace,
                   size_t workspace_bytes, void* stream, const pa_decode_opts* opts) {
+  NvtxRange nvtx("pa_decode_fp8");
   if (!d_k_scale) return fail(PA_ERR_INVALID, "pa_decode_fp8: NULL k_scale");
   if (opts && opts->variant == 1)
     return fail(PA_ERR_UNSUPPORTED, "pa_decode_fp8: only the tensor-core variant exists");
@@ -245,6 +332,7 @@ int pa_decode_grouped(const void* d_q, const void* d_k_cache, const void* d_v_ca
                       const int32_t* d_group_prefix_tokens, int32_t num_groups, void* d_out,
                       void* d_workspace, size_t workspace_bytes, void* stream,
                       const pa_decode_opts* opts) {
+  NvtxRange nvtx("pa_decode_grouped");
   if (num_groups <= 0 && num_seqs > 0)
     return fail(PA_ERR_INVALID, "pa_decode_grouped: num_groups must be >= 1");
   return decode_common(d_q, d_k_cache, d_v_cache, num_blocks, d_block_tables, max_blocks_per_seq,
@@ -277,6 +365,7 @@ int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, in
                int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                float scale, int32_t dtype, void* d_out, void* d_workspace, size_t workspace_bytes,
                void* stream, const pa_decode_opts* opts) {
+  NvtxRange nvtx("pa_prefill");
   if (num_seqs < 0 || num_q_tokens < 0)
     return fail(PA_ERR_INVALID, "pa_prefill: num_seqs and num_q_tokens must be >= 0");
   if (dtype != PA_F16 && dtype != PA_BF16) return fail(PA_ERR_UNSUPPORTED, "pa_prefill: dtype");
@@ -300,8 +389,8 @@ int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, in
   if (!std::isfinite(scale)) return fail(PA_ERR_INVALID, "pa_prefill: scale is not finite");
   if (opts && opts->variant != 0 && opts->variant != 2 && opts->variant != 3)
     return fail(PA_ERR_UNSUPPORTED, "pa_prefill: variant must be 0 (auto), 2 (mma.sync) or 3 (tcgen05)");
-  if (opts && opts->flags != 0)
-    return fail(PA_ERR_INVALID, "pa_prefill: opts->flags must be 0");
+  if (opts && (opts->flags != 0 || opts->partition_tokens != 0))
+    return fail(PA_ERR_INVALID, "pa_prefill: opts->flags and opts->partition_tokens must be 0");
   if (opts && opts->variant == 3 && head_dim != 128)
     return fail(PA_ERR_UNSUPPORTED, "pa_prefill: the tcgen05 variant needs head_dim 128");
   if (num_seqs == 0 || num_q_tokens == 0) return PA_OK;
@@ -338,12 +427,14 @@ int pa_prefill(const void* d_q, const void* d_k_cache, const void* d_v_cache, in
   a.ev_before = opts ? opts->event_before_main : nullptr;
   a.ev_after = opts ? opts->event_after_main : nullptr;
   a.variant = opts ? opts->variant : 0;
+  plan_forget(d_workspace);  // the prefill overwrites the workspace
   std::string why;
   int rc = pa::prefill_launch(a, &why);
   return rc ? fail(rc, why) : PA_OK;
 }
 
 int pa_decode_check(const void* d_workspace, void* stream, int32_t* error_bits) {
+  NvtxRange nvtx("pa_decode_check");
   if (!d_workspace || !error_bits) return fail(PA_ERR_INVALID, "pa_decode_check: NULL argument");
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("pa_decode_check: ") + cudaGetErrorString(e));

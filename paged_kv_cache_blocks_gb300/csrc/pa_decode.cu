@@ -70,6 +70,9 @@ struct DecodeParams {
   const float* v_scale;
   float2* ml;
   float* acc;
+  int64_t max_parts;  // partition records the workspace holds
+  int64_t max_rows;   // partial-result rows it holds (partitions + shared-prefix chunks)
+  int64_t max_pitems; // shared-prefix work items it holds
   int64_t num_blocks;
   int32_t max_blocks;
   int32_t num_seqs;
@@ -118,7 +121,7 @@ __device__ __forceinline__ int group_of(const DecodeParams& P, int b) {
 constexpr int kPrepCache = 4096;  // sequences whose (length, start) prep keeps in shared memory
 
 __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint4,
-                                                    int target_full_items) {
+                                                    int target_full_items, int force_pt) {
   __shared__ int sw[32];
   __shared__ int2 s_ls[kPrepCache];  // (clamped length, first token of the partitions)
   __shared__ int s_full[3];
@@ -187,11 +190,14 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
   atomicAdd(&s_full[1], f2);
   atomicAdd(&s_full[2], f4);
   __syncthreads();
+  // force_pt (512 / 1024 / 2048, or 0 to choose) fixes the size instead
   int pt = kPartTokens, total_full = s_full[0];
-  if (static_cast<int64_t>(s_full[2]) * P.hkv >= target_full_items) {
+  if (force_pt == 4 * kPartTokens ||
+      (force_pt == 0 && static_cast<int64_t>(s_full[2]) * P.hkv >= target_full_items)) {
     pt = 4 * kPartTokens;
     total_full = s_full[2];
-  } else if (static_cast<int64_t>(s_full[1]) * P.hkv >= target_full_items) {
+  } else if (force_pt == 2 * kPartTokens ||
+             (force_pt == 0 && static_cast<int64_t>(s_full[1]) * P.hkv >= target_full_items)) {
     pt = 2 * kPartTokens;
     total_full = s_full[1];
   }
@@ -798,21 +804,54 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     // ------------------------------------------------------------ scheduler
     // Takes work items from the atomic counter one item ahead and stages each
     // item's partition record and block ids in the item ring, so the TMA warp
-    // never waits on global memory between items.
-    const int32_t n_items = *reinterpret_cast<volatile int32_t*>(&P.ws->n_items);
+    // never waits on global memory between items.  The plan may be one a
+    // caller reuses from an earlier call (PA_DECODE_REUSE_PLAN), so it is not
+    // trusted: an item count beyond the workspace's capacity is cut, a record
+    // that is not a partition of this call's sequences is skipped, and a
+    // length that differs from seq_lens marks the plan stale; each is flagged
+    // (kErrPlan) and no index leaves its buffer.
     const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
+    const bool pt_ok = pt == kPartTokens || pt == 2 * kPartTokens || pt == 4 * kPartTokens;
+    int32_t n_items = *reinterpret_cast<volatile int32_t*>(&P.ws->n_items);
+    if (!pt_ok || n_items < 0 || n_items > P.max_parts * P.hkv) {
+      if (lane == 0) atomicOr(err, kErrPlan);
+      n_items = pt_ok ? static_cast<int32_t>(min(static_cast<int64_t>(max(n_items, 0)),
+                                                 P.max_parts * P.hkv))
+                      : 0;
+    }
     uint32_t g = 0;  // blocks of this CTA's stream before the next item
     int next = 0;
     if (lane == 0) next = atomicAdd(&P.ws->next_item, 1);
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
-      const int item = __shfl_sync(0xffffffffu, next, 0);
       bool ok = true;
-      if (lane == 0) {
-        ok = mbar_wait(&item_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, err);
-        if (ok && item < n_items) next = atomicAdd(&P.ws->next_item, 1);
-      }
+      if (lane == 0) ok = mbar_wait(&item_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, err);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      int item, part = 0, h = 0, first_tok = 0, nblk = 0;
+      PartInfo pi;
+      for (;;) {  // the next item whose record is a partition of this call
+        item = __shfl_sync(0xffffffffu, next, 0);
+        if (item < 0) {  // the work counter itself was not reset: no item is taken
+          if (lane == 0) atomicOr(err, kErrPlan);
+          item = n_items;
+        }
+        if (lane == 0 && item < n_items) next = atomicAdd(&P.ws->next_item, 1);
+        if (item >= n_items) break;
+        part = item / P.hkv;
+        h = item - part * P.hkv;
+        pi = P.parts[part];
+        const int64_t ft = static_cast<int64_t>(pi.start) + static_cast<int64_t>(pi.p) * pt;
+        if (pi.b >= 0 && pi.b < P.num_seqs && pi.len > 0 && pi.len <= P.max_seq_len &&
+            pi.start >= 0 && pi.start % kBlock == 0 && pi.p >= 0 && pi.nparts >= 1 && ft < pi.len) {
+          first_tok = static_cast<int>(ft);
+          nblk = min(pt / kBlock, (pi.len - first_tok + kBlock - 1) / kBlock);
+          int L = P.seq_lens[pi.b];
+          L = L < 0 ? 0 : min(L, P.max_seq_len);
+          if (L != pi.len && lane == 0) atomicOr(err, kErrPlan);  // planned for other lengths
+          break;
+        }
+        if (lane == 0) atomicOr(err, kErrPlan);
+      }
       if (item >= n_items) {
         if (lane == 0) {
           info[slot].b = -1;
@@ -820,10 +859,6 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
         }
         break;
       }
-      const int part = item / P.hkv, h = item - part * P.hkv;
-      const PartInfo pi = P.parts[part];
-      const int first_tok = pi.start + pi.p * pt;
-      const int nblk = min(pt / kBlock, (pi.len - first_tok + kBlock - 1) / kBlock);
       const int32_t* trow = P.tables + static_cast<int64_t>(pi.b) * P.max_blocks + first_tok / kBlock;
       for (int j = lane; j < nblk; j += 32) {
         int32_t id = trow[j];
@@ -1008,7 +1043,14 @@ __global__ void __launch_bounds__(kMergeThreads, 1024 / kMergeThreads) merge_ker
   // one float4 column of the G x D block per thread; U partials in flight
   constexpr int kE = 1;
   constexpr int U = 8;
-  const int n_work = *reinterpret_cast<volatile int32_t*>(&P.ws->n_split) * P.hkv;
+  // the merge records may come from a reused plan: a count beyond the
+  // workspace and records that do not fit it are skipped and flagged
+  int n_split = *reinterpret_cast<volatile int32_t*>(&P.ws->n_split);
+  if (n_split < 0 || n_split > P.num_seqs) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&P.ws->error_bits, kErrPlan);
+    n_split = n_split < 0 ? 0 : P.num_seqs;
+  }
+  const int n_work = n_split * P.hkv;
   const int G = P.G;
   const int n4 = G * D / 4;
   const int t = threadIdx.x;
@@ -1028,6 +1070,21 @@ __global__ void __launch_bounds__(kMergeThreads, 1024 / kMergeThreads) merge_ker
     const MergeInfo mi = P.split[wi / P.hkv];
     const int h = wi - (wi / P.hkv) * P.hkv;
     const int64_t head0 = static_cast<int64_t>(h) * G;
+    // every count is bounded by the workspace before it is used (int64 sums:
+    // no record can overflow them), so every partial index stays inside it
+    const int64_t nfull = mi.nfull, nsuf = mi.nsuf, nchunks = mi.nchunks;
+    const bool fits =
+        mi.b >= 0 && mi.b < P.num_seqs && nfull >= 0 && nfull <= P.max_parts &&
+        (nsuf == nfull || nsuf == nfull + 1) && nchunks >= 0 && nchunks <= P.max_rows &&
+        nsuf + nchunks >= 1 &&
+        (nfull == 0 || (mi.first_full >= 0 && mi.first_full + nfull <= P.max_parts)) &&
+        (nsuf == nfull || (mi.tail >= 0 && mi.tail < P.max_parts)) &&
+        (nchunks == 0 ||
+         (mi.pfirst >= 0 && mi.pstride >= 1 && mi.pfirst + (nchunks - 1) * mi.pstride < P.max_rows));
+    if (!fits) {
+      if (t == 0) atomicOr(&P.ws->error_bits, kErrPlan);
+      continue;
+    }
     const int nparts = mi.nsuf + mi.nchunks;
     int e4[kE], gk[kE];
     float m[kE], l[kE];
@@ -1121,7 +1178,12 @@ __global__ void __launch_bounds__(kPrefixWarps * 32)
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPrefixChunkBlocks * Cfg::kStageBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 1);
   int* err = &P.ws->error_bits;
-  const int n_work = *reinterpret_cast<volatile int32_t*>(&P.ws->n_pitems) * P.hkv;
+  int n_pitems = *reinterpret_cast<volatile int32_t*>(&P.ws->n_pitems);
+  if (n_pitems < 0 || n_pitems > P.max_pitems) {  // a reused plan that does not fit
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(err, kErrPlan);
+    n_pitems = n_pitems < 0 ? 0 : static_cast<int>(P.max_pitems);
+  }
+  const int n_work = n_pitems * P.hkv;
   if (blockIdx.x >= n_work) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -1133,16 +1195,32 @@ __global__ void __launch_bounds__(kPrefixWarps * 32)
   }
   __syncthreads();
   const int64_t y_oob = P.num_blocks * P.hkv * kBlock;
-  uint32_t n_local = 0;
-  for (int wi = blockIdx.x; wi < n_work; wi += gridDim.x, ++n_local) {
+  uint32_t n_local = 0;  // items this CTA has loaded (the barrier's phase)
+  for (int wi = blockIdx.x; wi < n_work; wi += gridDim.x) {
     const int4 item = P.pitems[wi / P.hkv];
     const int h = wi - (wi / P.hkv) * P.hkv;
     const int grp = item.x, chunk = item.y, tile = item.z;
+    // the item may come from a reused plan: one that does not describe a
+    // chunk of this call's groups inside the workspace is skipped (uniformly:
+    // every thread reads the same values)
+    if (grp < 0 || grp >= P.num_groups || chunk < 0 || tile < 0) {
+      if (tid == 0) atomicOr(err, kErrPlan);
+      continue;
+    }
     const int off = P.group_off[grp];
-    const int M = P.group_off[grp + 1] - off;
+    const int64_t M64 = static_cast<int64_t>(P.group_off[grp + 1]) - off;
     const int4 gi = P.group_info[grp];
     const int pre = P.group_prefix[grp];
-    const int nblk = min(kPrefixChunkBlocks, pre / kBlock - chunk * kPrefixChunkBlocks);
+    const int64_t nblk64 = min(static_cast<int64_t>(kPrefixChunkBlocks),
+                               static_cast<int64_t>(pre / kBlock) - static_cast<int64_t>(chunk) * kPrefixChunkBlocks);
+    if (off < 0 || M64 < 1 || off + M64 > P.num_seqs || pre <= 0 || pre % kBlock != 0 || nblk64 < 1 ||
+        static_cast<int64_t>(chunk) * kPrefixChunkBlocks + nblk64 > P.max_blocks ||
+        static_cast<int64_t>(tile) * kPrefixRows >= M64 * G || gi.x < 0 ||
+        static_cast<int64_t>(gi.x) + (static_cast<int64_t>(chunk) + 1) * M64 > P.max_rows) {
+      if (tid == 0) atomicOr(err, kErrPlan);
+      continue;
+    }
+    const int M = static_cast<int>(M64), nblk = static_cast<int>(nblk64);
     if (tid == 0) {
       // the prefix blocks are those of the group's first member
       const int32_t* trow = P.tables + static_cast<int64_t>(off) * P.max_blocks + chunk * kPrefixChunkBlocks;
@@ -1263,6 +1341,7 @@ __global__ void __launch_bounds__(kPrefixWarps * 32)
     // every warp is done with the stages before the next item's copies
     __syncthreads();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    ++n_local;
   }
 }
 
@@ -1434,11 +1513,15 @@ bool dispatch_attend(int variant, int G, const CUtensorMap& tk, const CUtensorMa
 }  // namespace
 
 // One side stream and a fork/join event pair per device, created on first
-// use and kept for the process.  Reusing the events is safe: a stream wait
-// uses the record that precedes it.
+// use and kept for the process.  Reusing the events is safe as long as one
+// call's record-then-wait sequence is not interleaved with another's (a
+// stream wait uses the record that precedes it): a grouped decode holds the
+// device's `use` lock from the fork record until its stream has waited on
+// the join, so host threads calling it concurrently take turns there.
 struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex use;
 };
 
 SideStream* side_stream(std::string* why) {
@@ -1458,7 +1541,11 @@ SideStream* side_stream(std::string* why) {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
     if (e != cudaSuccess) {
       *why = std::string("side stream: ") + cudaGetErrorString(e);
-      ss = SideStream{};
+      if (ss.join) cudaEventDestroy(ss.join);
+      if (ss.fork) cudaEventDestroy(ss.fork);
+      if (ss.stream) cudaStreamDestroy(ss.stream);
+      ss.stream = nullptr;
+      ss.fork = ss.join = nullptr;
       return nullptr;
     }
   }
@@ -1513,6 +1600,9 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   P.num_groups = grouped ? a.num_groups : 0;
   P.ml = reinterpret_cast<float2*>(ws + L.off_ml);
   P.acc = reinterpret_cast<float*>(ws + L.off_acc);
+  P.max_parts = L.max_parts;
+  P.max_rows = L.max_parts + L.max_prefix;
+  P.max_pitems = L.max_prefix;
   P.num_blocks = a.num_blocks;
   P.max_blocks = a.max_blocks_per_seq;
   P.num_seqs = a.num_seqs;
@@ -1536,6 +1626,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   cudaStream_t s = static_cast<cudaStream_t>(a.stream);
   const int row_uint4 = a.num_q_heads * a.head_dim * 2 / 16;
   cudaEvent_t join_after_attend = nullptr;
+  std::unique_lock<std::mutex> side_lock;  // held from the fork record to the wait on the join
   int dev0 = 0, n_sm = 0;
   cudaGetDevice(&dev0);
   cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev0);
@@ -1543,7 +1634,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   // the plan (partition list, merge records, counters) depends only on the
   // lengths, tables and shapes: a caller may reuse the workspace's plan
   if (!a.reuse_plan) {
-    prep_kernel<<<1, 1024, 0, s>>>(P, row_uint4, 16 * n_sm);
+    prep_kernel<<<1, 1024, 0, s>>>(P, row_uint4, 16 * n_sm, a.partition_tokens);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
       *why = std::string("prep launch: ") + cudaGetErrorString(e);
@@ -1556,6 +1647,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
     // caller's stream with events, so it overlaps the attention kernel.
     SideStream* side = side_stream(why);
     if (!side) return 5;
+    side_lock = std::unique_lock<std::mutex>(side->use);
     cudaEventRecord(side->fork, s);
     cudaStreamWaitEvent(side->stream, side->fork, 0);
     bool okp = a.dtype == 1
@@ -1586,6 +1678,7 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   if (!ok) return 5;
   if (a.ev_after) cudaEventRecord(static_cast<cudaEvent_t>(a.ev_after), s);
   if (join_after_attend) cudaStreamWaitEvent(s, join_after_attend, 0);
+  if (side_lock.owns_lock()) side_lock.unlock();
 
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);

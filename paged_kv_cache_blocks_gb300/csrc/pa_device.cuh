@@ -23,6 +23,7 @@ constexpr int kErrSeqLen = 1;
 constexpr int kErrBlockId = 2;
 constexpr int kErrTimeout = 4;
 constexpr int kErrGroup = 8;
+constexpr int kErrPlan = 16;  // a reused plan did not fit this call: its records were skipped
 
 // A wait that has not completed after this long gives up (ns of globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

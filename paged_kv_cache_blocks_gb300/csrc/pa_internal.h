@@ -39,6 +39,7 @@ struct DecodeArgs {
   const float* k_scale = nullptr;         // [num_kv_heads] (device), FP8 only
   const float* v_scale = nullptr;
   bool reuse_plan = false;                // skip the prep kernel: the workspace holds the plan
+  int32_t partition_tokens = 0;           // 0: chosen by the prep kernel; else 512 / 1024 / 2048
 };
 
 // Both return 0 on success or a pa_status code, with *why set on failure.

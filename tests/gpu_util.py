@@ -62,6 +62,18 @@ def oracle_out(b, layer=0, rows=None, pools=None):
     return oracle.decode(q, kc, vc, tab, lens, w.scale, w.dtype)
 
 
+_ORACLE_CACHE = {}
+
+
+def oracle_out_cached(name, layer=0, num_layers=None):
+    """oracle_out of every row of a default workload batch, computed once per
+    process (several tests compare the same full-size batch)."""
+    key = (name, layer, num_layers)
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = oracle_out(batch(name, num_layers=num_layers), layer)
+    return _ORACLE_CACHE[key]
+
+
 def assert_close(got, ref, what=""):
     got = np.asarray(got, np.float64)
     assert got.shape == ref.shape

@@ -77,6 +77,32 @@ def test_errors_are_codes(binding):
     assert e.value.code == binding.PA_ERR_UNSUPPORTED
 
 
+def test_shared_write_without_room_for_its_copy(binding):
+    """A write into a block another sequence still holds, with no room to
+    report the copy that must come first, is PA_ERR_SHARED_WRITE and changes
+    nothing; with room it moves the writer onto a copy (same as the model)."""
+    from oracle.allocator import ERR_SHARED_WRITE
+    a, m = binding.Allocator(8), AllocatorModel(8, 16)
+    s, t = a.seq_create(), m.seq_create()
+    a.append_slots([s], 40)
+    m.append_slots([t], 40)
+    c, mc = a.seq_fork(s, 40), m.seq_fork(t, 40)     # block 2 of both is partly filled and shared
+    before = a.stats()
+    with pytest.raises(binding.PaError) as e:
+        a.append_slots([c], 1, cow_capacity=0)
+    with pytest.raises(AllocError) as me:
+        m.append_slots([mc], 1, cow_capacity=0)
+    assert e.value.code == binding.PA_ERR_SHARED_WRITE == me.value.code == ERR_SHARED_WRITE
+    assert a.stats() == before
+    same_state(m, a, [s, c])
+    got, want = a.append_slots([c], 1, cow_capacity=1), m.append_slots([mc], 1, cow_capacity=1)
+    assert got == want and len(got[1]) == 1
+    # a whole shared block is never written: the next token starts a new block
+    d, md = a.seq_fork(s, 32), m.seq_fork(t, 32)
+    assert a.append_slots([d], 1, cow_capacity=0) == m.append_slots([md], 1, cow_capacity=0)
+    same_state(m, a, [s, c, d])
+
+
 def test_table_and_lengths_updated_in_place(binding):
     a = binding.Allocator(16, list(range(15, -1, -1)))
     ids = [a.seq_create() for _ in range(3)]
@@ -94,7 +120,7 @@ def test_random_sequences_match_model(binding):
     hyp = pytest.importorskip("hypothesis")
     st = pytest.importorskip("hypothesis.strategies")
 
-    ops = st.lists(st.tuples(st.sampled_from(["new", "app", "app2", "fork", "free"]),
+    ops = st.lists(st.tuples(st.sampled_from(["new", "app", "app2", "app0", "fork", "free"]),
                              st.integers(0, 7), st.integers(0, 40)), max_size=50)
 
     @hyp.settings(max_examples=120, deadline=None)
@@ -110,16 +136,17 @@ def test_random_sequences_match_model(binding):
                 live.append(x)
                 continue
             sid = live[i % len(live)]
-            if op in ("app", "app2"):
-                group = [sid] if op == "app" else sorted(set([sid, live[(i + 1) % len(live)]]))
+            if op in ("app", "app2", "app0"):
+                group = [sid] if op != "app2" else sorted(set([sid, live[(i + 1) % len(live)]]))
+                cap = 0 if op == "app0" else None   # app0: no room for copy-on-write pairs
                 try:
-                    want = m.append_slots(group, n)
+                    want = m.append_slots(group, n, cow_capacity=cap)
                 except AllocError as e:
                     with pytest.raises(binding.PaError) as ge:
-                        a.append_slots(group, n)
+                        a.append_slots(group, n, cow_capacity=cap)
                     assert ge.value.code == e.code
                 else:
-                    got = a.append_slots(group, n)
+                    got = a.append_slots(group, n, cow_capacity=cap)
                     assert got[0] == want[0] and got[1] == want[1]
             elif op == "fork":
                 k = min(n, m.seqs[sid]["len"])

@@ -35,9 +35,7 @@ def test_fullstep_groups(pa):
     b = U.batch("fullstep", num_layers=1)
     got, bits = run_grouped(pa, b)
     assert bits == 0
-    assert np.isfinite(got).all()
-    rows = np.array([0, 1, 31, 32, 63, 64, 100, 127])
-    U.assert_close(got[rows], U.oracle_out(b, rows=rows), "fullstep grouped")
+    U.assert_close(got, U.oracle_out_cached("fullstep", num_layers=1), "fullstep grouped")
     q, kc, vc, tab, lens = U.device_inputs(b)
     plain = pa.pa_decode(q, kc, vc, tab, lens, b.workload.scale).double().cpu().numpy()
     assert np.max(np.abs(got - plain)) <= 1e-2

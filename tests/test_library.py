@@ -126,8 +126,78 @@ def test_decode_rejects_unknown_flags(L):
     assert L.pa_prefill(*_prefill_args(opts=ctypes.byref(o))) == 1
 
 
+def test_decode_partition_tokens_checked(L):
+    from paged_kv_cache_blocks_gb300 import binding as b
+    o = b.PaDecodeOpts()
+    for bad in (256, 513, 4096, -512):
+        o.partition_tokens = bad
+        assert L.pa_decode_ex(*_decode_args(), ctypes.byref(o)) == b.PA_ERR_INVALID
+        assert b"partition_tokens" in L.pa_last_error_string()
+    o.partition_tokens = 512
+    assert L.pa_prefill(*_prefill_args(opts=ctypes.byref(o))) == b.PA_ERR_INVALID
+    assert ctypes.sizeof(b.PaDecodeOpts) == 56     # the size the struct had before the field
+
+
 def test_selftest_rejects_bad_arguments(L):
     P = ctypes.c_void_p
     assert L.pa_selftest_bounded_wait(0, P(1 << 20), None) == 1
     assert L.pa_selftest_bounded_wait(2_000_000_000, P(1 << 20), None) == 1
     assert L.pa_selftest_bounded_wait(1000, P(0), None) == 1
+
+
+def test_reuse_plan_needs_a_planned_workspace(L):
+    """PA_DECODE_REUSE_PLAN on a workspace no decode call planned (or planned
+    for other shapes) is refused on the host, before anything is launched."""
+    from paged_kv_cache_blocks_gb300 import binding as b
+    o = b.PaDecodeOpts()
+    o.flags = b.PA_DECODE_REUSE_PLAN
+    for ws in (1 << 24, (1 << 24) + 256 * 7):
+        rc = L.pa_decode_ex(*_decode_args(ws=ws), ctypes.byref(o))
+        assert rc == b.PA_ERR_INVALID
+        assert b"PA_DECODE_REUSE_PLAN" in L.pa_last_error_string()
+    P = ctypes.c_void_p
+    a = _decode_args(ws=1 << 24)
+    p = P(1 << 20)
+    rc = L.pa_decode_fp8(a[0], a[1], a[2], p, p, *a[3:], ctypes.byref(o))
+    assert rc == b.PA_ERR_INVALID and b"PA_DECODE_REUSE_PLAN" in L.pa_last_error_string()
+    rc = L.pa_decode_grouped(*a[:14], p, p, 2, *a[14:], ctypes.byref(o))
+    assert rc == b.PA_ERR_INVALID and b"PA_DECODE_REUSE_PLAN" in L.pa_last_error_string()
+
+
+def test_reuse_plan_without_workspace_raises_before_any_call(monkeypatch):
+    """The binding refuses reuse_plan without the planning call's workspace
+    before it allocates or calls into the library (all three decode calls)."""
+    import torch
+    from paged_kv_cache_blocks_gb300 import binding as b
+
+    def no_call():
+        raise AssertionError("the library must not be reached")
+    monkeypatch.setattr(b, "lib", no_call)
+    t = torch.zeros(1)
+    with pytest.raises(ValueError, match="reuse_plan"):
+        b.pa_decode(t, t, t, t, t, 0.1, reuse_plan=True)
+    with pytest.raises(ValueError, match="reuse_plan"):
+        b.pa_decode_fp8(t, t, t, t, t, t, t, 0.1, reuse_plan=True)
+    with pytest.raises(ValueError, match="reuse_plan"):
+        b.pa_decode_grouped(t, t, t, t, t, 0.1, t, t, reuse_plan=True)
+
+
+def test_noalloc_binding_checks_index_types(monkeypatch):
+    """int64 block tables or lengths are refused (they would be read as pairs
+    of int32 words) before the library is called."""
+    import torch
+    from paged_kv_cache_blocks_gb300 import binding as b
+
+    def no_call():
+        raise AssertionError("the library must not be reached")
+    monkeypatch.setattr(b, "lib", no_call)
+    monkeypatch.setattr(b, "_need_cuda", lambda *ts: None)
+    q = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
+    kc = torch.zeros(4, 2, 16, 128, dtype=torch.bfloat16)
+    for tab, lens in ((torch.zeros(2, 3, dtype=torch.int64), torch.ones(2, dtype=torch.int32)),
+                      (torch.zeros(2, 3, dtype=torch.int32), torch.ones(2, dtype=torch.int64))):
+        with pytest.raises(TypeError, match="int32"):
+            b.pa_decode_noalloc(q, kc, kc, tab, lens, 0.1, out=q)
+        with pytest.raises(TypeError, match="int32"):
+            b.pa_decode_fp8(q, kc, kc, torch.ones(2), torch.ones(2), tab, lens, 0.1, out=q,
+                            workspace=torch.zeros(256, dtype=torch.uint8))

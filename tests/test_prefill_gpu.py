@@ -100,17 +100,47 @@ def test_prefill_one_query_head_per_kv_head(pa):
         del W.WORKLOADS["g1"], W._SEED_SALT["g1"]
 
 
+_CHUNKED_REF = {}
+
+
+def chunked_reference(pb, iteration):
+    """Every output row of one iteration of the chunked workload from the
+    oracle's dense form (the loop form would take tens of minutes on the
+    last pieces), computed once per process."""
+    if iteration not in _CHUNKED_REF:
+        w = pb.workload
+        kc, vc = pb.placed_pools()
+        _CHUNKED_REF[iteration] = oracle.prefill_dense(
+            pb.q.numpy().view(np.uint16), kc.numpy().view(np.uint16), vc.numpy().view(np.uint16),
+            pb.block_tables, pb.seq_lens, pb.q_offsets, w.scale, w.dtype)
+    return _CHUNKED_REF[iteration]
+
+
 @pytest.mark.parametrize("iteration,variant", [(1, 3), (8, 3), (8, 2)])
-def test_prefill_chunked_workload_sampled(pa, iteration, variant):
-    """The full chunked workload (30000-token prompt, piece k of 8, plus 20
-    decode tokens): rows across the piece (first, last, tile edges) and every
-    decode token, computed one by one by the oracle."""
+def test_prefill_chunked_workload_all_rows(pa, iteration, variant):
+    """The full chunked workload (30000-token prompt, piece k of 8 -- 3,750
+    query tokens over up to 30,000 keys -- plus 20 decode tokens), in the
+    launch configuration the bench times: every output row against the
+    oracle.  The pools the GPU cache write produced are byte-identical to the
+    oracle's placement first."""
     pb = W.make_prefill_batch("chunked", seed=0, iteration=iteration)
-    n = int(pb.pieces[0])
-    rows = np.unique(np.concatenate([[0, 1, 15, 16, 17, n // 2, n - 17, n - 16, n - 2, n - 1],
-                                     np.arange(n, pb.num_q_tokens)])).astype(np.int64)
-    got, ref, _ = run(pa, pb, rows=rows, variant=variant)
-    U.assert_close_rounded(got, ref, "bf16", f"chunked iteration {iteration} variant {variant}")
+    w = pb.workload
+    kc, vc = U.to_dev(pb.k_cache, w.dtype), U.to_dev(pb.v_cache, w.dtype)
+    pa.pa_cache_write(U.to_dev(pb.new_k, w.dtype), U.to_dev(pb.new_v, w.dtype),
+                      torch.from_numpy(pb.slot_mapping).cuda(), kc, vc)
+    pk, pv = pb.placed_pools()
+    assert np.array_equal(_u16(kc), pk.numpy().view(np.uint16))
+    assert np.array_equal(_u16(vc), pv.numpy().view(np.uint16))
+    ws = torch.empty(pa.pa_prefill_workspace_bytes(len(pb.seq_lens), pb.num_q_tokens,
+                                                   w.num_q_heads, w.num_kv_heads),
+                     dtype=torch.uint8, device="cuda")
+    out = pa.pa_prefill(U.to_dev(pb.q, w.dtype), kc, vc, torch.from_numpy(pb.block_tables).cuda(),
+                        torch.from_numpy(pb.seq_lens).cuda(), torch.from_numpy(pb.q_offsets).cuda(),
+                        w.scale, workspace=ws, variant=variant)
+    torch.cuda.synchronize()
+    assert pa.pa_decode_check(ws) == 0
+    U.assert_close_rounded(out.double().cpu().numpy(), chunked_reference(pb, iteration), "bf16",
+                           f"chunked iteration {iteration} variant {variant}")
 
 
 def test_prefill_decode_tokens_match_pa_decode(pa):

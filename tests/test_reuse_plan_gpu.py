@@ -83,3 +83,122 @@ def test_reuse_plan_grouped_and_fp8(pa):
     full = pa.pa_decode_fp8(q, k8, v8, ks, ks, tab, sl, b8.workload.scale)
     torch.cuda.synchronize()
     assert torch.equal(reused, full)
+
+
+def test_reuse_with_other_shapes_is_refused(pa):
+    """A workspace planned for one batch refuses reuse with another batch's
+    shapes (and after a prefill overwrote it): PA_ERR_INVALID on the host,
+    nothing launched, the output buffer untouched."""
+    a = W.make_batch("llama8b", seed=11, lens_override=[100, 700, 1500, 33])
+    bb = W.make_batch("llama8b", seed=12, lens_override=[100, 700, 1500, 33, 9])
+    w = a.workload
+    ws = torch.empty(pa.pa_decode_workspace_bytes(5, w.num_q_heads, w.head_dim, 2048),
+                     dtype=torch.uint8, device="cuda")
+    q, kc, vc, tab, sl = U.device_inputs(a)
+    pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=2048, workspace=ws)
+    torch.cuda.synchronize()
+    qb, kb, vb, tb, lb = U.device_inputs(bb)
+    for kw in (dict(max_seq_len=2048), dict(max_seq_len=1600)):
+        out = torch.full_like(qb, float("nan"))
+        with pytest.raises(pa.PaError) as e:
+            pa.pa_decode(qb, kb, vb, tb, lb, w.scale, out=out, workspace=ws, reuse_plan=True, **kw)
+        assert e.value.code == pa.PA_ERR_INVALID
+        torch.cuda.synchronize()
+        assert torch.isnan(out).all()
+    # same shapes as the planning call: accepted
+    out = pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=2048, workspace=ws,
+                       reuse_plan=True)
+    torch.cuda.synchronize()
+    assert pa.pa_decode_check(ws) == 0
+    U.assert_close(out.double().cpu().numpy(), U.oracle_out(a), "reuse, same shapes")
+    # a grouped call's plan is not a plain decode's plan
+    with pytest.raises(pa.PaError) as e:
+        goff = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
+        gpre = torch.zeros(1, dtype=torch.int32, device="cuda")
+        big = torch.empty(pa.pa_decode_grouped_workspace_bytes(4, w.num_q_heads, w.head_dim, 2048),
+                          dtype=torch.uint8, device="cuda")
+        pa.pa_decode_grouped(q, kc, vc, tab, sl, w.scale, goff, gpre, max_seq_len=2048,
+                             workspace=big, reuse_plan=True)
+    assert e.value.code == pa.PA_ERR_INVALID
+
+
+def test_reuse_with_stale_lengths_is_flagged(pa):
+    """Reuse with the planned shapes but other lengths: the plan is a valid
+    plan of the workspace, so nothing leaves its buffers, and the lengths that
+    differ from the plan's set PA_DEVERR_PLAN.  A planning call afterwards is
+    clean and correct."""
+    a = W.make_batch("llama8b", seed=13, lens_override=[300, 2000, 40, 1200])
+    w = a.workload
+    q, kc, vc, tab, sl = U.device_inputs(a)
+    ws = torch.empty(pa.pa_decode_workspace_bytes(4, w.num_q_heads, w.head_dim, 2048),
+                     dtype=torch.uint8, device="cuda")
+    pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=2048, workspace=ws)
+    assert pa.pa_decode_check(ws) == 0
+    shorter = (sl - 17).clamp(min=1)
+    pa.pa_decode(q, kc, vc, tab, shorter, w.scale, max_seq_len=2048, workspace=ws, reuse_plan=True)
+    assert pa.pa_decode_check(ws) & pa.PA_DEVERR_PLAN
+    out = pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=2048, workspace=ws)
+    assert pa.pa_decode_check(ws) == 0
+    U.assert_close(out.double().cpu().numpy(), U.oracle_out(a), "after a stale reuse")
+
+
+def _plan_words(B, msl):
+    """int32 words of the workspace that hold the plan: header, partition
+    records, per-sequence first partitions and merge records (the layout of
+    the decode workspace: a 256-byte header, then 32-byte partition records
+    for B x ceil(msl / 512) partitions, then 8 bytes and 32 bytes per
+    sequence, each region starting on a 256-byte boundary)."""
+    up = lambda x: (x + 255) // 256 * 256
+    max_parts = B * -(-msl // 512)
+    off_seq_first = up(256 + 32 * max_parts)
+    off_split = up(off_seq_first + 8 * B)
+    end = up(off_split + 32 * B)
+    return end // 4
+
+
+@pytest.mark.parametrize("mode", ["random", "random-valid-header", "perturbed", "negative-counter"])
+def test_corrupted_plan_is_skipped_not_followed(pa, mode):
+    """The plan lives in caller memory, so a reuse must not trust it: after a
+    planning call the plan is overwritten (seeded: random words mixing small
+    integers around the valid ranges, large and negative ones and zeros; or
+    the true plan with words shifted by small amounts; or a work counter
+    left negative) and reused.  The kernels' own bounds checks skip every
+    record that does not fit the call's buffers and set PA_DEVERR_PLAN; the
+    context stays usable and a planning call afterwards is correct."""
+    a = W.make_batch("llama70b", seed=14, lens_override=[5000, 300, 17, 2100, 9000, 1])
+    w = a.workload
+    q, kc, vc, tab, sl = U.device_inputs(a)
+    B, msl = 6, 9000
+    ws = torch.empty(pa.pa_decode_workspace_bytes(B, w.num_q_heads, w.head_dim, msl),
+                     dtype=torch.uint8, device="cuda")
+    pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=msl, workspace=ws)
+    torch.cuda.synchronize()
+    nw = _plan_words(B, msl)
+    plan = ws.view(torch.int32)[:nw].cpu()
+    g = torch.Generator().manual_seed(500 + len(mode))
+    n = nw
+    kind = torch.randint(0, 4, (n,), generator=g)
+    small = torch.randint(-3, 40, (n,), generator=g, dtype=torch.int32)
+    near = torch.randint(0, 3000, (n,), generator=g, dtype=torch.int32)
+    wide = torch.randint(-2**31, 2**31 - 1, (n,), generator=g, dtype=torch.int64).to(torch.int32)
+    if mode == "perturbed":
+        shift = torch.randint(-40, 41, (n,), generator=g, dtype=torch.int32)
+        words = torch.where(kind < 2, plan + shift, plan)
+    elif mode == "negative-counter":
+        words = plan.clone()
+        words[3] = -5                  # the attention kernel's work counter
+    else:
+        words = torch.where(kind == 0, small, torch.where(kind == 1, near,
+                            torch.where(kind == 2, wide, torch.zeros_like(small))))
+        if mode == "random-valid-header":
+            words[2], words[3], words[4], words[6] = 10 ** 6, 0, 5, 512
+    words[0] = 0                      # error bits
+    ws.view(torch.int32)[:nw].copy_(words.cuda())
+    pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=msl, workspace=ws, reuse_plan=True)
+    bits = pa.pa_decode_check(ws)
+    assert not bits & pa.PA_DEVERR_TIMEOUT
+    if mode != "perturbed":           # a shifted plan may still fit (then nothing is flagged)
+        assert bits & pa.PA_DEVERR_PLAN
+    out = pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=msl, workspace=ws)
+    assert pa.pa_decode_check(ws) == 0
+    U.assert_close(out.double().cpu().numpy(), U.oracle_out(a), f"after a corrupted plan ({mode})")

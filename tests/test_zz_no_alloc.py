@@ -2,9 +2,10 @@
 allocate device memory (its scratch is a static 64 MiB array in libpa).
 
 It must give the same output as pa_decode with a caller-provided workspace,
-on two calls in a row (the static scratch keeps the previous call's
-contents, which the next call must not depend on).  This file is collected
-last so that a failure here never hides the other tests."""
+and stay within the decode tolerance of the fp64 oracle, on two calls in a
+row (the static scratch keeps the previous call's contents, which the next
+call must not depend on).  This file is collected last so that a failure
+here never hides the other tests."""
 import numpy as np
 import pytest
 import torch
@@ -26,6 +27,7 @@ def test_noalloc_matches_pa_decode_twice(pa):
         ref = pa.pa_decode(q, kc, vc, tab, lens, b.workload.scale)
         torch.cuda.synchronize()
         ref = ref.double().cpu().numpy()
+        exact = U.oracle_out(b)
         for _ in range(2):
             out = torch.full_like(q, float("nan"))
             pa.pa_decode_noalloc(q, kc, vc, tab, lens, b.workload.scale, out=out)
@@ -34,6 +36,7 @@ def test_noalloc_matches_pa_decode_twice(pa):
             assert np.isfinite(got).all()
             err = np.abs(got - ref)
             assert err.max() <= U.MAX_ABS and err.mean() <= U.MEAN_ABS, (name, err.max())
+            U.assert_close(got, exact, f"noalloc {name} vs oracle")
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch(pa):
