@@ -422,6 +422,18 @@ def run_prefill(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = run_prefill_e2e(args, pa, its, w, dev, barrier, dist, world, flops)
+    # ---- every decode config of the workload table, measured the same way ---------
+    per_config = None
+    if args.per_config and world == 1 and not args.fp8 and not grouped:
+        per_config = {}
+        for name in PER_CONFIG:
+            try:
+                per_config[name] = measure_config(pa, W, name, args.steps, args.warmup, dev,
+                                                  measured_peaks()[0],
+                                                  with_oracle=not args.no_cpu_baseline)
+            except Exception as ex:   # report, do not hide
+                per_config[name] = {"error": repr(ex)}
+
     if rank != 0:
         return 0
     cpu = None
@@ -654,6 +666,18 @@ def run_cow(args, rank, world, local_rank):
                "steps": steps, "ms_per_step": sec * 1e3,
                "path": "per step: H2D (pinned) source and destination ids -> pa_copy_blocks -> "
                        "D2H of one copied K block; synchronised after the last step"}
+    # ---- every decode config of the workload table, measured the same way ---------
+    per_config = None
+    if args.per_config and world == 1 and not args.fp8 and not grouped:
+        per_config = {}
+        for name in PER_CONFIG:
+            try:
+                per_config[name] = measure_config(pa, W, name, args.steps, args.warmup, dev,
+                                                  measured_peaks()[0],
+                                                  with_oracle=not args.no_cpu_baseline)
+            except Exception as ex:   # report, do not hide
+                per_config[name] = {"error": repr(ex)}
+
     if rank != 0:
         return 0
     cpu = None
@@ -866,10 +890,16 @@ def run_pa(args, rank, world, local_rank):
     t_host0 = time.time()
     start.record(stream)
     for i in range(args.steps):
-        step(ev_pairs[i])
+        step()
     stop.record(stream)
     barrier()
     t_host1 = time.time()
+    # the attention kernel alone: the same steps again with events around each
+    # of its launches (kept out of the step timing above: an event recorded
+    # between two kernels keeps the second from starting during the first's tail)
+    for i in range(args.steps):
+        step(ev_pairs[i])
+    barrier()
     if sampler:
         time.sleep(0.15)
         sampler.stop()
@@ -899,6 +929,18 @@ def run_pa(args, rank, world, local_rank):
     e2e = run_e2e(args, pa, W, b, w, dt, dev, variant, barrier, world, dist, grouped,
                   (k_sc, v_sc) if args.fp8 else None) \
         if not args.no_e2e else None
+
+    # ---- every decode config of the workload table, measured the same way ---------
+    per_config = None
+    if args.per_config and world == 1 and not args.fp8 and not grouped:
+        per_config = {}
+        for name in PER_CONFIG:
+            try:
+                per_config[name] = measure_config(pa, W, name, args.steps, args.warmup, dev,
+                                                  measured_peaks()[0],
+                                                  with_oracle=not args.no_cpu_baseline)
+            except Exception as ex:   # report, do not hide
+                per_config[name] = {"error": repr(ex)}
 
     if rank != 0:
         return 0
@@ -934,6 +976,8 @@ def run_pa(args, rank, world, local_rank):
         "hbm_frac_step": (kvb / (ms_step * 1e-3) / 1e9) / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
+                     "nominal_peak": NOMINAL_HBM_GBS,
                      "traffic_gbs": traffic / (kern_avg * 1e-3) / 1e9 if traffic else None,
                      "traffic_frac": traffic / (kern_avg * 1e-3) / 1e9 / peak if traffic else None,
                      "kernel": "attend_fp8_kernel" if args.fp8 else "attend_kernel", "kernel_ms": kern_avg,
@@ -946,11 +990,167 @@ def run_pa(args, rank, world, local_rank):
         "gpu_launches": ((3 + int(grouped)) * nl + 1) * args.steps,
         "clocks": clocks,
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     if cpu is not None:
         cpu["cpu_model"] = cpu_model()
         line["cpu_baseline"] = cpu
     print(json.dumps(line), flush=True)
     return 0
+
+
+# --------------------------------------------------------------------------- every decode config
+
+PER_CONFIG = ("tiny", "llama8b", "llama70b", "long", "fullstep")
+L2_BYTES = 129 * 1000 * 1000          # GB300 L2, for the flush decision
+NOMINAL_HBM_GBS = 7900.0              # GB300 HBM3e nominal bandwidth (context only)
+
+
+def cache_write_bytes(T, hkv, d, elem=2):
+    """One cache write: k and v rows read, the same bytes written."""
+    return 2 * 2 * T * hkv * d * elem
+
+
+def oracle_config_times(name, b):
+    """The fp64 oracle on one layer of the config's batch (its own host
+    cores, all of them), and on one thread over its first two sequences."""
+    import oracle
+    oracle.build()
+    from paged_kv_cache_blocks_gb300 import workloads as W
+    w = b.workload
+    kc, vc = W.place_new_tokens(b, 0)
+    kc, vc = kc.cpu().numpy().view(np.uint16), vc.cpu().numpy().view(np.uint16)
+    q = b.layers[0].q.cpu().numpy().view(np.uint16)
+    threads = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    oracle.decode(q, kc, vc, b.block_tables, b.seq_lens, w.scale, w.dtype, threads=threads)
+    t_all = time.perf_counter() - t0
+    n1 = min(2, len(b.seq_lens))
+    t0 = time.perf_counter()
+    oracle.decode(q[:n1], kc, vc, b.block_tables[:n1], b.seq_lens[:n1], w.scale, w.dtype, threads=1)
+    t_one = time.perf_counter() - t0
+    tok_all, tok_one = int(b.seq_lens.sum()), int(b.seq_lens[:n1].sum())
+    return {"oracle_layer_s": t_all, "oracle_threads": threads,
+            "oracle_kv_gbs": logical_kv_bytes(b.seq_lens, w.num_kv_heads, w.head_dim) / t_all / 1e9,
+            "oracle_1thread_layer_s_est": t_one * tok_all / max(tok_one, 1),
+            "oracle_1thread_sample": f"{n1} sequences ({tok_one} tokens), scaled by tokens"}
+
+
+def measure_config(pa, W, name, steps, warmup, dev, peak, with_oracle=True):
+    """One decode config measured the way the headline is: a step = per
+    layer pa_cache_write of every sequence's new token + pa_decode (layers
+    after the first reuse the first layer's plan), CUDA events around each
+    step and around each attention launch.  Configs whose KV is under 4x the
+    L2 size get the L2 flushed (a 256 MB write, then a 256 MB read) before
+    every step, outside the timed region; the others stream more than L2
+    holds anyway."""
+    w = W.WORKLOADS[name]
+    b = W.make_batch(name, seed=0, poison=False, device="cuda")
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
+    layers = [(Lr.q.view(dt), Lr.k_cache.view(dt), Lr.v_cache.view(dt), Lr.new_k.view(dt),
+               Lr.new_v.view(dt)) for Lr in b.layers]
+    nl = len(layers)
+    tab = torch.from_numpy(b.block_tables).to(dev)
+    lens = torch.from_numpy(b.seq_lens).to(dev)
+    slots = torch.from_numpy(b.slot_mapping).to(dev)
+    msl = int(b.seq_lens.max())
+    ws = torch.empty(pa.pa_decode_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(layers[0][0])
+    kvb = logical_kv_bytes(b.seq_lens, Hkv, D) * nl
+    flush = kvb < 4 * L2_BYTES
+    if flush:
+        flush_w = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+        flush_r = torch.zeros(64 * 2 ** 20, dtype=torch.int32, device=dev)
+
+    def l2_flush():
+        # write a buffer twice the L2 size, then read another one: the dirty
+        # lines the write leaves are written back during the read, so the
+        # timed step starts with an L2 of clean, unrelated lines
+        flush_w.zero_()
+        torch.max(flush_r)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        for li, (q, kc, vc, nk, nv) in enumerate(layers):
+            pa.pa_cache_write(nk, nv, slots, kc, vc)
+            pa.pa_decode(q, kc, vc, tab, lens, w.scale, max_seq_len=msl, out=out, workspace=ws,
+                         events=evs[li] if evs else None, reuse_plan=li > 0)
+
+    for _ in range(warmup):
+        if flush:
+            l2_flush()
+        step()
+    torch.cuda.synchronize()
+    if pa.pa_decode_check(ws):
+        raise RuntimeError(f"{name}: device error bits during warm-up")
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    st_ev = [(mk(), mk()) for _ in range(steps)]
+    k_ev = [[(mk(), mk()) for _ in range(nl)] for _ in range(steps)]
+    for row in k_ev:
+        for a, z in row:
+            a.record(stream)
+            z.record(stream)
+    torch.cuda.synchronize()
+    # steps timed as a whole (events only around each step), then the same
+    # steps with events around each attention launch for the kernel's time
+    for i in range(steps):
+        if flush:
+            l2_flush()
+        st_ev[i][0].record(stream)
+        step()
+        st_ev[i][1].record(stream)
+    for i in range(steps):
+        if flush:
+            l2_flush()
+        step(k_ev[i])
+    torch.cuda.synchronize()
+    step_ms = statistics.fmean(a.elapsed_time(z) for a, z in st_ev)
+    kern_ms = statistics.fmean(a.elapsed_time(z) for row in k_ev for a, z in row)
+    part_tokens = int(ws[24:28].view(torch.int32).item())
+    alg = algorithmic_bytes(b.seq_lens, Hq, Hkv, D, part_tokens=part_tokens)
+    step_alg = nl * (alg + cache_write_bytes(B, Hkv, D))
+    r = {"workload": DESCR[name], "num_seqs": B, "layers": nl,
+         "kv_tokens_per_layer": int(b.seq_lens.sum()), "logical_kv_bytes_per_step": kvb,
+         "ms_per_step": step_ms, "us_per_step": step_ms * 1e3,
+         "kv_gbs": kvb / (step_ms * 1e-3) / 1e9,
+         "seqs_steps_per_s": B / (step_ms * 1e-3),
+         "attend_us_per_launch": kern_ms * 1e3,
+         "attend_frac": alg / (kern_ms * 1e-3) / 1e9 / peak,
+         "step_alg_frac": step_alg / (step_ms * 1e-3) / 1e9 / peak,
+         "partition_tokens": part_tokens,
+         "l2": "flushed before every step (256 MB written, then 256 MB read; not timed)" if flush
+               else f"not flushed: {kvb / 1e9:.2f} GB of KV per step vs 129 MB L2"}
+    if name == "tiny":   # latency-bound: report time only
+        for k in ("kv_gbs", "attend_frac", "step_alg_frac"):
+            r.pop(k)
+    if name == "fullstep":
+        goff, gpre = (torch.from_numpy(x).to(dev) for x in b.group_arrays())
+        gws = torch.empty(pa.pa_decode_grouped_workspace_bytes(B, Hq, D, msl), dtype=torch.uint8,
+                          device=dev)
+
+        def gstep():
+            for li, (q, kc, vc, nk, nv) in enumerate(layers):
+                pa.pa_cache_write(nk, nv, slots, kc, vc)
+                pa.pa_decode_grouped(q, kc, vc, tab, lens, w.scale, goff, gpre, max_seq_len=msl,
+                                     out=out, workspace=gws, reuse_plan=li > 0)
+        for _ in range(warmup):
+            gstep()
+        a, z = mk(), mk()
+        a.record(stream)
+        for _ in range(steps):
+            gstep()
+        z.record(stream)
+        torch.cuda.synchronize()
+        r["grouped_ms_per_step"] = a.elapsed_time(z) / steps
+        r["unique_kv_bytes_per_step"] = b.unique_kv_bytes() * nl
+    if with_oracle:
+        r.update(oracle_config_times(name, b))
+        if nl > 1:
+            r["oracle_note"] = f"one layer timed; a {nl}-layer step takes {nl}x"
+    del layers, b
+    torch.cuda.empty_cache()
+    return r
 
 
 def time_graph(step, steps, warmup, stream, barrier, dist, dev, units, world):
@@ -1256,6 +1456,8 @@ def main():
                     help="decode shared-prefix groups with pa_decode_grouped (fullstep)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="skip timing the step replayed from a CUDA graph")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip measuring every decode config after the headline")
     args = ap.parse_args()
     if args.fp8 and args.grouped:
         ap.error("--fp8 and --grouped do not combine (the shared-prefix kernel reads 16-bit caches)")

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(256)
                        const int64_t* __restrict__ slot_mapping, int64_t n_chunks, int chunks_per_token,
                        int chunks_per_row, int hkv, uint4* __restrict__ k_cache,
                        uint4* __restrict__ v_cache, int64_t num_blocks) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n_chunks) return;
   const int64_t t = i / chunks_per_token;
@@ -48,11 +50,12 @@ int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping
   const int threads = 256;
   const int64_t blocks = (n_chunks + threads - 1) / threads;
   dim3 grid(static_cast<unsigned>(blocks), 2);
-  cache_write_kernel<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, n_chunks,
-      chunks_per_token, chunks_per_row, num_kv_heads, static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), num_blocks);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(cache_write_kernel, grid, dim3(threads), 0,
+                             static_cast<cudaStream_t>(stream), static_cast<const uint4*>(k),
+                             static_cast<const uint4*>(v), slot_mapping, n_chunks, chunks_per_token,
+                             chunks_per_row, num_kv_heads, static_cast<uint4*>(k_cache),
+                             static_cast<uint4*>(v_cache), num_blocks);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("cache_write launch: ") + cudaGetErrorString(e);
     return 5;

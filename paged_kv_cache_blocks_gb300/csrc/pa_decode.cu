@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
   __shared__ int s_hist[kMaxPartBlocks + 1];
   __shared__ int s_nsplit, s_total_tail, s_groups_ok;
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();  // the attention kernel may set up while the plan is made
   if (tid == 0) {
     P.ws->error_bits = 0;
     s_full[0] = s_full[1] = s_full[2] = 0;
@@ -798,7 +800,13 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == 1) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
   __syncthreads();
+  pdl_wait();               // the plan, q and the caches are ready from here on
+  pdl_launch_dependents();  // the merge kernel may be scheduled (it waits for this grid)
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler
@@ -886,8 +894,6 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     // CTA's block stream, so each stage is refilled by one thread, in order.
     if (lane != 0) return;
     const uint32_t iss = static_cast<uint32_t>(warp - 1);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
     const int64_t y_oob = P.num_blocks * P.hkv * kBlock;  // one past the pool: reads as zeros
     uint32_t g = 0;  // blocks issued by this CTA
     bool ok = true;
@@ -1043,6 +1049,8 @@ __global__ void __launch_bounds__(kMergeThreads, 1024 / kMergeThreads) merge_ker
   // one float4 column of the G x D block per thread; U partials in flight
   constexpr int kE = 1;
   constexpr int U = 8;
+  pdl_wait();
+  pdl_launch_dependents();
   // the merge records may come from a reused plan: a count beyond the
   // workspace and records that do not fit it are skipped and flagged
   int n_split = *reinterpret_cast<volatile int32_t*>(&P.ws->n_split);
@@ -1487,8 +1495,9 @@ bool launch_attend(const CUtensorMap& tk, const CUtensorMap& tv, const DecodePar
   int64_t grid = occ_cache[slot];
   if (grid > max_items) grid = max_items;
   if (grid < 1) grid = 1;
-  kern<<<static_cast<unsigned>(grid), Cfg::kThreads, Cfg::kBytes, stream>>>(tk, tv, P);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(Cfg::kThreads),
+                             Cfg::kBytes, stream, tk, tv, P);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("attend launch: ") + cudaGetErrorString(e);
     return false;
@@ -1634,8 +1643,9 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   // the plan (partition list, merge records, counters) depends only on the
   // lengths, tables and shapes: a caller may reuse the workspace's plan
   if (!a.reuse_plan) {
-    prep_kernel<<<1, 1024, 0, s>>>(P, row_uint4, 16 * n_sm, a.partition_tokens);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(prep_kernel, dim3(1), dim3(1024), 0, s, P, row_uint4, 16 * n_sm,
+                               static_cast<int>(a.partition_tokens));
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
       *why = std::string("prep launch: ") + cudaGetErrorString(e);
       return 5;
@@ -1690,23 +1700,24 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
   if (mgrid > sms * (1024 / mthreads)) mgrid = sms * (1024 / mthreads);
   if (mgrid < 1) mgrid = 1;
-  const unsigned mg = static_cast<unsigned>(mgrid);
+  const dim3 mg(static_cast<unsigned>(mgrid));
+  cudaError_t e;
   if (a.dtype == 1) {
     if (a.head_dim == 128) {
-      if (wide) merge_kernel<__nv_bfloat16, 128, 256><<<mg, 256, 0, s>>>(P);
-      else merge_kernel<__nv_bfloat16, 128, 128><<<mg, 128, 0, s>>>(P);
+      e = wide ? launch_pdl(merge_kernel<__nv_bfloat16, 128, 256>, mg, dim3(256), 0, s, P)
+               : launch_pdl(merge_kernel<__nv_bfloat16, 128, 128>, mg, dim3(128), 0, s, P);
     } else {
-      merge_kernel<__nv_bfloat16, 64, 128><<<mg, 128, 0, s>>>(P);
+      e = launch_pdl(merge_kernel<__nv_bfloat16, 64, 128>, mg, dim3(128), 0, s, P);
     }
   } else {
     if (a.head_dim == 128) {
-      if (wide) merge_kernel<__half, 128, 256><<<mg, 256, 0, s>>>(P);
-      else merge_kernel<__half, 128, 128><<<mg, 128, 0, s>>>(P);
+      e = wide ? launch_pdl(merge_kernel<__half, 128, 256>, mg, dim3(256), 0, s, P)
+               : launch_pdl(merge_kernel<__half, 128, 128>, mg, dim3(128), 0, s, P);
     } else {
-      merge_kernel<__half, 64, 128><<<mg, 128, 0, s>>>(P);
+      e = launch_pdl(merge_kernel<__half, 64, 128>, mg, dim3(128), 0, s, P);
     }
   }
-  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     *why = std::string("merge launch: ") + cudaGetErrorString(e);
     return 5;

@@ -10,6 +10,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 namespace pa {
 
@@ -100,6 +101,40 @@ inline WsLayout ws_layout(int64_t num_seqs, int64_t num_q_heads, int64_t head_di
   L.off_acc = o;         o = align_up(o + sizeof(float) * rows * num_q_heads * head_dim, 256);
   L.total = o;
   return L;
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  The decode step's kernels (cache write,
+// prep, attention, merge) are launched so that each may start while the
+// kernel before it on the stream drains: its launch and prologue (barrier
+// set-up, tensor-map prefetch) overlap the predecessor's tail.  Every such
+// kernel executes pdl_wait() before its first global-memory access: that
+// returns once the preceding kernel has completed and its writes are
+// visible, so stream order is kept for every byte (a no-op for a plain
+// launch).  pdl_launch_dependents() lets the next kernel be scheduled (it,
+// too, waits before touching memory).
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kern` on `stream` with programmatic stream serialisation allowed.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------

@@ -92,32 +92,34 @@ def test_reuse_with_other_shapes_is_refused(pa):
     a = W.make_batch("llama8b", seed=11, lens_override=[100, 700, 1500, 33])
     bb = W.make_batch("llama8b", seed=12, lens_override=[100, 700, 1500, 33, 9])
     w = a.workload
-    ws = torch.empty(pa.pa_decode_workspace_bytes(5, w.num_q_heads, w.head_dim, 2048),
+    ws = torch.empty(pa.pa_decode_workspace_bytes(5, w.num_q_heads, w.head_dim, 1500),
                      dtype=torch.uint8, device="cuda")
     q, kc, vc, tab, sl = U.device_inputs(a)
-    pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=2048, workspace=ws)
+    pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=1500, workspace=ws)
     torch.cuda.synchronize()
     qb, kb, vb, tb, lb = U.device_inputs(bb)
-    for kw in (dict(max_seq_len=2048), dict(max_seq_len=1600)):
-        out = torch.full_like(qb, float("nan"))
+    for args in ((qb, kb, vb, tb, lb, 1500),       # another batch size
+                 (q, kc, vc, tab, sl, 1400)):       # another max_seq_len
+        out = torch.full_like(args[0], float("nan"))
         with pytest.raises(pa.PaError) as e:
-            pa.pa_decode(qb, kb, vb, tb, lb, w.scale, out=out, workspace=ws, reuse_plan=True, **kw)
+            pa.pa_decode(*args[:5], w.scale, max_seq_len=args[5], out=out, workspace=ws,
+                         reuse_plan=True)
         assert e.value.code == pa.PA_ERR_INVALID
         torch.cuda.synchronize()
         assert torch.isnan(out).all()
     # same shapes as the planning call: accepted
-    out = pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=2048, workspace=ws,
+    out = pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=1500, workspace=ws,
                        reuse_plan=True)
     torch.cuda.synchronize()
     assert pa.pa_decode_check(ws) == 0
     U.assert_close(out.double().cpu().numpy(), U.oracle_out(a), "reuse, same shapes")
-    # a grouped call's plan is not a plain decode's plan
+    # a workspace no grouped call planned is refused to a grouped reuse
     with pytest.raises(pa.PaError) as e:
         goff = torch.tensor([0, 4], dtype=torch.int32, device="cuda")
         gpre = torch.zeros(1, dtype=torch.int32, device="cuda")
-        big = torch.empty(pa.pa_decode_grouped_workspace_bytes(4, w.num_q_heads, w.head_dim, 2048),
+        big = torch.empty(pa.pa_decode_grouped_workspace_bytes(4, w.num_q_heads, w.head_dim, 1500),
                           dtype=torch.uint8, device="cuda")
-        pa.pa_decode_grouped(q, kc, vc, tab, sl, w.scale, goff, gpre, max_seq_len=2048,
+        pa.pa_decode_grouped(q, kc, vc, tab, sl, w.scale, goff, gpre, max_seq_len=1500,
                              workspace=big, reuse_plan=True)
     assert e.value.code == pa.PA_ERR_INVALID
 
@@ -130,14 +132,15 @@ def test_reuse_with_stale_lengths_is_flagged(pa):
     a = W.make_batch("llama8b", seed=13, lens_override=[300, 2000, 40, 1200])
     w = a.workload
     q, kc, vc, tab, sl = U.device_inputs(a)
-    ws = torch.empty(pa.pa_decode_workspace_bytes(4, w.num_q_heads, w.head_dim, 2048),
+    msl = 2000
+    ws = torch.empty(pa.pa_decode_workspace_bytes(4, w.num_q_heads, w.head_dim, msl),
                      dtype=torch.uint8, device="cuda")
-    pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=2048, workspace=ws)
+    pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=msl, workspace=ws)
     assert pa.pa_decode_check(ws) == 0
     shorter = (sl - 17).clamp(min=1)
-    pa.pa_decode(q, kc, vc, tab, shorter, w.scale, max_seq_len=2048, workspace=ws, reuse_plan=True)
+    pa.pa_decode(q, kc, vc, tab, shorter, w.scale, max_seq_len=msl, workspace=ws, reuse_plan=True)
     assert pa.pa_decode_check(ws) & pa.PA_DEVERR_PLAN
-    out = pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=2048, workspace=ws)
+    out = pa.pa_decode(q, kc, vc, tab, sl, w.scale, max_seq_len=msl, workspace=ws)
     assert pa.pa_decode_check(ws) == 0
     U.assert_close(out.double().cpu().numpy(), U.oracle_out(a), "after a stale reuse")
 
