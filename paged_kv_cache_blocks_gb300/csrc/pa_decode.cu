@@ -828,8 +828,9 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
                       : 0;
     }
     uint32_t g = 0;  // blocks of this CTA's stream before the next item
-    int next = 0;
-    if (lane == 0) next = atomicAdd(&P.ws->next_item, 1);
+    // Item blockIdx.x is this CTA's first (no atomic on the critical path of
+    // the kernel's start); the work counter hands out the rest from gridDim.x.
+    int next = static_cast<int>(blockIdx.x);
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       bool ok = true;
@@ -843,7 +844,13 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
           if (lane == 0) atomicOr(err, kErrPlan);
           item = n_items;
         }
-        if (lane == 0 && item < n_items) next = atomicAdd(&P.ws->next_item, 1);
+        if (lane == 0 && item < n_items) {
+          const int r = atomicAdd(&P.ws->next_item, 1);
+          // a counter the last call did not leave at 0 (a negative one is
+          // flagged above on its next use) never yields a wrapped index
+          next = r < 0 ? -1 : (r > INT32_MAX - static_cast<int>(gridDim.x) ? n_items
+                                                                          : static_cast<int>(gridDim.x) + r);
+        }
         if (item >= n_items) break;
         part = item / P.hkv;
         h = item - part * P.hkv;
@@ -853,9 +860,6 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
             pi.start >= 0 && pi.start % kBlock == 0 && pi.p >= 0 && pi.nparts >= 1 && ft < pi.len) {
           first_tok = static_cast<int>(ft);
           nblk = min(pt / kBlock, (pi.len - first_tok + kBlock - 1) / kBlock);
-          int L = P.seq_lens[pi.b];
-          L = L < 0 ? 0 : min(L, P.max_seq_len);
-          if (L != pi.len && lane == 0) atomicOr(err, kErrPlan);  // planned for other lengths
           break;
         }
         if (lane == 0) atomicOr(err, kErrPlan);
@@ -881,6 +885,11 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
         info[slot] = ItemInfo{pi.b, h, pi.p, pi.len, pi.nparts, nblk, static_cast<int32_t>(g), part,
                               pi.start, 0};
         mbar_arrive(&item_full[slot]);
+        // a plan made for other lengths is flagged (after the item is out: the
+        // check costs a global load the copies need not wait for)
+        int L = P.seq_lens[pi.b];
+        L = L < 0 ? 0 : min(L, P.max_seq_len);
+        if (L != pi.len) atomicOr(err, kErrPlan);
       }
       g += nblk;
     }
