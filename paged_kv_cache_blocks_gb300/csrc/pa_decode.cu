@@ -646,24 +646,26 @@ struct Fp8State {
     const int g = lane >> 2, t = lane & 3;
     float s[4] = {0.f, 0.f, 0.f, 0.f};
     {
-      // two independent accumulation chains (even / odd k-steps) halve the
-      // dependent mma latency of a block
-      float s2[4] = {0.f, 0.f, 0.f, 0.f};
+      // four independent accumulation chains (one per 32-dim step) keep the
+      // dependent mma latency of a block to one product
+      float sp[D / 32][4];
       const int tok = fp8_sigma((lane & 7) + 8 * ((lane >> 3) & 1));
       const int cofs = lane >> 4;
 #pragma unroll
       for (int kk = 0; kk < D / 32; ++kk) {
         uint32_t r0, r1, r2, r3;
         ldmatrix_x4(r0, r1, r2, r3, sK + swz128(tok, 2 * kk + cofs));
-        Mma<__half>::run(s, e4m3x2_to_half2(r0 & 0xffff), e4m3x2_to_half2(r1 & 0xffff),
-                         e4m3x2_to_half2(r0 >> 16), e4m3x2_to_half2(r1 >> 16), qb[2 * kk][0],
-                         qb[2 * kk][1]);
-        Mma<__half>::run(s2, e4m3x2_to_half2(r2 & 0xffff), e4m3x2_to_half2(r3 & 0xffff),
-                         e4m3x2_to_half2(r2 >> 16), e4m3x2_to_half2(r3 >> 16), qb[2 * kk + 1][0],
-                         qb[2 * kk + 1][1]);
+        uint32_t a0, a2, a1, a3, b0, b2, b1, b3;
+        e4m3x4_to_half2x2(r0, &a0, &a2);
+        e4m3x4_to_half2x2(r1, &a1, &a3);
+        e4m3x4_to_half2x2(r2, &b0, &b2);
+        e4m3x4_to_half2x2(r3, &b1, &b3);
+        sp[kk][0] = sp[kk][1] = sp[kk][2] = sp[kk][3] = 0.f;
+        Mma<__half>::run(sp[kk], a0, a1, a2, a3, qb[2 * kk][0], qb[2 * kk][1]);
+        Mma<__half>::run(sp[kk], b0, b1, b2, b3, qb[2 * kk + 1][0], qb[2 * kk + 1][1]);
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) s[c] += s2[c];
+      for (int c = 0; c < 4; ++c) s[c] = (sp[0][c] + sp[1][c]) + (sp[2][c] + sp[3][c]);
     }
     const bool v0 = fp8_sigma(g) < nvalid, v1 = fp8_sigma(g + 8) < nvalid;
     const float x0 = v0 ? s[0] * sl : -INFINITY;
@@ -676,40 +678,62 @@ struct Fp8State {
       bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o2));
       bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o2));
     }
-    const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);
-    const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-    l[0] = l[0] * al0 + (p0 + p2);
-    l[1] = l[1] * al1 + (p1 + p3);
-    m[0] = mn0;
-    m[1] = mn1;
+    // Lazy rescaling: the reference maximum m moves only when a block's
+    // maximum exceeds it by more than 2^8 (log2 units), so the weights stay
+    // below 256 (exact in the fp16 P operand's range) and most blocks skip
+    // the rescale of l and o.  Exact either way: l and o are always relative
+    // to the same m.  The decision is warp-uniform (a vote over all lanes).
+    if (__any_sync(0xffffffffu, bm0 > m[0] + 8.f || bm1 > m[1] + 8.f)) {
+      const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);
+      const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
+      l[0] *= al0;
+      l[1] *= al1;
+      m[0] = mn0;
+      m[1] = mn1;
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
+      for (int mt = 0; mt < D / 16; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
     }
+    const float p0 = exp2f(x0 - m[0]), p1 = exp2f(x1 - m[1]);
+    const float p2 = exp2f(x2 - m[0]), p3 = exp2f(x3 - m[1]);
+    l[0] += p0 + p2;
+    l[1] += p1 + p3;
     const uint32_t b0 = movmatrix_trans(pack_half2(p0, p1));
     const uint32_t b1 = movmatrix_trans(pack_half2(p2, p3));
-    uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
-    if (nvalid < 16) {
-      mk0 = (4 * t < nvalid ? 0x0000ffffu : 0u) | (4 * t + 1 < nvalid ? 0xffff0000u : 0u);
-      mk1 = (4 * t + 2 < nvalid ? 0x0000ffffu : 0u) | (4 * t + 3 < nvalid ? 0xffff0000u : 0u);
-    }
-    {
-      const int row = (lane & 7) + 8 * ((lane >> 3) & 1) + 16 * (lane >> 4);
+    const int row = (lane & 7) + 8 * ((lane >> 3) & 1) + 16 * (lane >> 4);
+    if (nvalid == 16) {  // a full block: every V row is a token
 #pragma unroll
       for (int mm = 0; mm < D / 32; ++mm) {
         uint32_t r0, r1, r2, r3;
         ldmatrix_x4(r0, r1, r2, r3, sV + (32 * mm + row) * 16);
-        Mma<__half>::run(o[2 * mm], e4m3x2_to_half2(r0 & 0xffff) & mk0,
-                         e4m3x2_to_half2(r1 & 0xffff) & mk0, e4m3x2_to_half2(r0 >> 16) & mk1,
-                         e4m3x2_to_half2(r1 >> 16) & mk1, b0, b1);
-        Mma<__half>::run(o[2 * mm + 1], e4m3x2_to_half2(r2 & 0xffff) & mk0,
-                         e4m3x2_to_half2(r3 & 0xffff) & mk0, e4m3x2_to_half2(r2 >> 16) & mk1,
-                         e4m3x2_to_half2(r3 >> 16) & mk1, b0, b1);
+        uint32_t a0, a2, a1, a3, c0, c2, c1, c3;
+        e4m3x4_to_half2x2(r0, &a0, &a2);
+        e4m3x4_to_half2x2(r1, &a1, &a3);
+        e4m3x4_to_half2x2(r2, &c0, &c2);
+        e4m3x4_to_half2x2(r3, &c1, &c3);
+        Mma<__half>::run(o[2 * mm], a0, a1, a2, a3, b0, b1);
+        Mma<__half>::run(o[2 * mm + 1], c0, c1, c2, c3, b0, b1);
+      }
+    } else {
+      // Rows past the sequence end may hold anything (NaN included): zero
+      // them in the operand so 0 * garbage cannot reach the sum.
+      const uint32_t mk0 = (4 * t < nvalid ? 0x0000ffffu : 0u) | (4 * t + 1 < nvalid ? 0xffff0000u : 0u);
+      const uint32_t mk1 = (4 * t + 2 < nvalid ? 0x0000ffffu : 0u) | (4 * t + 3 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int mm = 0; mm < D / 32; ++mm) {
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4(r0, r1, r2, r3, sV + (32 * mm + row) * 16);
+        uint32_t a0, a2, a1, a3, c0, c2, c1, c3;
+        e4m3x4_to_half2x2(r0, &a0, &a2);
+        e4m3x4_to_half2x2(r1, &a1, &a3);
+        e4m3x4_to_half2x2(r2, &c0, &c2);
+        e4m3x4_to_half2x2(r3, &c1, &c3);
+        Mma<__half>::run(o[2 * mm], a0 & mk0, a1 & mk0, a2 & mk1, a3 & mk1, b0, b1);
+        Mma<__half>::run(o[2 * mm + 1], c0 & mk0, c1 & mk0, c2 & mk1, c3 & mk1, b0, b1);
       }
     }
   }

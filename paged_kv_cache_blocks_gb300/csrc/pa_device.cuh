@@ -319,6 +319,18 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t x) {
   return d;
 }
 
+// Four E4M3 bytes (one 32-bit register) -> two pairs of fp16: bytes 0-1
+// into *lo, bytes 2-3 into *hi, each exact.  The register is split into its
+// 16-bit halves inside the asm, so no mask or shift is spent on the pairs.
+__device__ __forceinline__ void e4m3x4_to_half2x2(uint32_t x, uint32_t* lo, uint32_t* hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(*lo), "=r"(*hi)
+      : "r"(x));
+}
+
 // Two fp32 -> two E4M3 bytes (lo -> low byte), round to nearest even,
 // saturated to +-448.
 __device__ __forceinline__ uint16_t float2_to_e4m3x2(float lo, float hi) {
