@@ -118,12 +118,19 @@ __device__ __forceinline__ int group_of(const DecodeParams& P, int b) {
 // 256-token chunks handled once per (group, KV head) by the prefix kernel for
 // all members together.  A group whose prefix is not a multiple of 16 or
 // longer than one of its members is flagged and decoded without sharing.
+constexpr int kMergeThreads = 512;  // split merge CTA: 512 / columns thread groups share the partials
 constexpr int kPrepCache = 4096;  // sequences whose (length, start) prep keeps in shared memory
+// dynamic shared memory of the prep kernel: per cached sequence (length,
+// first token), first full-partition record, partitions
+constexpr size_t kPrepSmem = kPrepCache * (sizeof(int2) + 2 * sizeof(int));
 
 __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint4,
                                                     int target_full_items, int force_pt) {
+  extern __shared__ int4 prep_smem[];
+  int2* s_ls = reinterpret_cast<int2*>(prep_smem);      // (clamped length, first token of the partitions)
+  int* s_first = reinterpret_cast<int*>(s_ls + kPrepCache);
+  int* s_np = s_first + kPrepCache;
   __shared__ int sw[32];
-  __shared__ int2 s_ls[kPrepCache];  // (clamped length, first token of the partitions)
   __shared__ int s_full[3];
   __shared__ int s_hist[kMaxPartBlocks + 1];
   __shared__ int s_nsplit, s_total_tail, s_groups_ok;
@@ -147,7 +154,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
       P.group_bad[g] = 0;
     }
   }
-  __syncthreads();
+  if (ng > 0) __syncthreads();  // (ng is the same for every thread)
   const bool use_groups = ng > 0 && s_groups_ok;
   if (ng > 0 && !use_groups && tid == 0) atomicOr(&P.ws->error_bits, kErrGroup);
   if (use_groups) {
@@ -159,17 +166,15 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
         atomicOr(&P.ws->error_bits, kErrGroup);
       }
     }
-  }
-  __syncthreads();
-  // first token of the attention kernel's partitions for each sequence,
-  // kept in seq_prefix[b].w (rewritten in full in pass B)
-  if (use_groups) {
+    __syncthreads();
+    // first token of the attention kernel's partitions for each sequence,
+    // kept in seq_prefix[b].w (rewritten in full in pass B)
     for (int b = tid; b < P.num_seqs; b += blockDim.x) {
       const int g = group_of(P, b);
       P.seq_prefix[b] = make_int4(g, 0, 0, P.group_bad[g] ? 0 : P.group_prefix[g]);
     }
+    __syncthreads();
   }
-  __syncthreads();
   const bool cached = P.num_seqs <= kPrepCache;
   if (cached) {
     for (int b = tid; b < P.num_seqs; b += blockDim.x)
@@ -275,7 +280,12 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
       const int first = carry_full + fo;
       const int tail_idx = r ? total_full + atomicAdd(&s_hist[(r + kBlock - 1) / kBlock], 1) : -1;
       P.seq_first[b] = make_int2(first, tail_idx);
-      for (int p = 0; p < nfull; ++p) P.parts[first + p] = PartInfo{b, p, L, nparts, st, 0, 0, 0};
+      if (cached) {  // the full-partition records are written below, by every thread
+        s_first[b] = first;
+        s_np[b] = nparts;
+      } else {
+        for (int p = 0; p < nfull; ++p) P.parts[first + p] = PartInfo{b, p, L, nparts, st, 0, 0, 0};
+      }
       if (r) P.parts[tail_idx] = PartInfo{b, nfull, L, nparts, st, 0, 0, 0};
       if (nparts > 1 || sp.z > 0)
         P.split[atomicAdd(&s_nsplit, 1)] =
@@ -284,6 +294,22 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
     carry_full += tot_f;
   }
   __syncthreads();
+  if (cached) {
+    // Full-partition records r = 0 .. total_full-1, consecutive threads on
+    // consecutive records (coalesced): record r belongs to the last sequence
+    // whose first record is <= r (sequences without full partitions share
+    // the next one's first index and are passed over).
+    for (int rr = tid; rr < total_full; rr += blockDim.x) {
+      int lo = 0, hi = P.num_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_first[mid] <= rr) lo = mid;
+        else hi = mid - 1;
+      }
+      const int2 ls = s_ls[lo];
+      P.parts[rr] = PartInfo{lo, rr - s_first[lo], ls.x, s_np[lo], ls.y, 0, 0, 0};
+    }
+  }
   if (tid == 0) {
     P.ws->n_parts = n_suffix;
     P.ws->n_suffix_parts = n_suffix;
@@ -1070,18 +1096,23 @@ __global__ void __launch_bounds__(32 * (NC + 3), 2)
 // ---------------------------------------------------------------------------
 // 3. merge of split sequences
 //
-// One 128-thread CTA per (sequence with several partial results, KV head),
-// up to 16 resident per SM so a whole batch's merges run in one wave.  The
-// prep kernel leaves everything a merge needs in one MergeInfo record.  Each
-// thread owns up to kE float4 columns of the G x D block (a partial is one
-// fully coalesced G*D*4-byte read), keeps U partials in flight and folds them
-// in with a running maximum, the same online rule as inside a partition.
+// One CTA per (sequence with several partial results, KV head).  The prep
+// kernel leaves everything a merge needs in one MergeInfo record.  Thread
+// (c, s) owns float4 column c of the G x D block (kCols columns, a partial
+// is one fully coalesced G*D*4-byte read) and the partials p = s, s + kSplit,
+// ... of the sequence, U of them in flight, folded with a running maximum
+// (the online rule used inside a partition); the kMergeSplit partial states
+// of a column are then combined through shared memory.  Splitting the
+// partials over 512 / kCols thread groups cuts the chain of dependent load
+// rounds of a long sequence (64 partials at G = 4: 8 rounds -> 2).
 
-template <typename T, int D, int kMergeThreads>
-__global__ void __launch_bounds__(kMergeThreads, 1024 / kMergeThreads) merge_kernel(const DecodeParams P) {
-  // one float4 column of the G x D block per thread; U partials in flight
-  constexpr int kE = 1;
-  constexpr int U = 8;
+template <typename T, int D, int kCols, int kThreads>
+__global__ void __launch_bounds__(kThreads, 1024 / kThreads)
+    merge_kernel(const DecodeParams P) {
+  constexpr int U = 6;
+  constexpr int kMergeSplit = kThreads / kCols;
+  __shared__ float4 s_o[kMergeSplit][kCols];
+  __shared__ float2 s_ml[kMergeSplit][kCols];
   pdl_wait();
   pdl_launch_dependents();
   // the merge records may come from a reused plan: a count beyond the
@@ -1095,12 +1126,13 @@ __global__ void __launch_bounds__(kMergeThreads, 1024 / kMergeThreads) merge_ker
   const int G = P.G;
   const int n4 = G * D / 4;
   const int t = threadIdx.x;
+  const int c = t % kCols, sp = t / kCols;
   const float4* acc4 = reinterpret_cast<const float4*>(P.acc);
   // the attention kernel has finished: its work counter is reset here, so
   // that a later call may reuse this workspace's plan without the prep kernel
   if (blockIdx.x == 0 && t == 0) P.ws->next_item = 0;
   // the empty softmax of a zero-length sequence: its output is defined as 0
-  for (int b = blockIdx.x * kMergeThreads + t; b < P.num_seqs; b += gridDim.x * kMergeThreads) {
+  for (int b = blockIdx.x * kThreads + t; b < P.num_seqs; b += gridDim.x * kThreads) {
     int L = P.seq_lens[b];
     if (L <= 0) {
       uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(P.out) + static_cast<int64_t>(b) * P.hq * D);
@@ -1127,63 +1159,65 @@ __global__ void __launch_bounds__(kMergeThreads, 1024 / kMergeThreads) merge_ker
       continue;
     }
     const int nparts = mi.nsuf + mi.nchunks;
-    int e4[kE], gk[kE];
-    float m[kE], l[kE];
-    float4 o[kE];
-#pragma unroll
-    for (int k = 0; k < kE; ++k) {
-      e4[k] = t + kMergeThreads * k;
-      gk[k] = min(4 * e4[k] / D, 7);
-      m[k] = -INFINITY;
-      l[k] = 0.f;
-      o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int p0 = 0; p0 < nparts; p0 += U) {
-      float4 a[U][kE];
-      float2 ml[U][kE];
+    const bool col = c < n4;
+    const int gk = min(4 * c / D, 7);
+    float m = -INFINITY, l = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p0 = sp; p0 < nparts; p0 += U * kMergeSplit) {
+      float4 a[U];
+      float2 ml[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int p = p0 + u;
-        if (p < nparts) {
+        const int p = p0 + u * kMergeSplit;
+        if (col && p < nparts) {
           const int64_t idx =
               p < mi.nsuf ? (p < mi.nfull ? mi.first_full + p : mi.tail)
                           : static_cast<int64_t>(mi.pfirst) + static_cast<int64_t>(p - mi.nsuf) * mi.pstride;
-#pragma unroll
-          for (int k = 0; k < kE; ++k)
-            if (e4[k] < n4) {
-              a[u][k] = __ldcg(&acc4[(idx * P.hq + head0) * (D / 4) + e4[k]]);
-              ml[u][k] = __ldcg(&P.ml[idx * P.hq + head0 + gk[k]]);
-            }
+          a[u] = __ldcg(&acc4[(idx * P.hq + head0) * (D / 4) + c]);
+          ml[u] = __ldcg(&P.ml[idx * P.hq + head0 + gk]);
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        if (p0 + u < nparts) {
-#pragma unroll
-          for (int k = 0; k < kE; ++k)
-            if (e4[k] < n4) {
-              const float mn = fmaxf(m[k], ml[u][k].x);
-              const float al = exp2f(m[k] - mn), wg = exp2f(ml[u][k].x - mn);
-              l[k] = fmaf(l[k], al, ml[u][k].y * wg);
-              o[k].x = fmaf(o[k].x, al, a[u][k].x * wg);
-              o[k].y = fmaf(o[k].y, al, a[u][k].y * wg);
-              o[k].z = fmaf(o[k].z, al, a[u][k].z * wg);
-              o[k].w = fmaf(o[k].w, al, a[u][k].w * wg);
-              m[k] = mn;
-            }
+        if (col && p0 + u * kMergeSplit < nparts) {
+          const float mn = fmaxf(m, ml[u].x);
+          const float al = exp2f(m - mn), wg = exp2f(ml[u].x - mn);
+          l = fmaf(l, al, ml[u].y * wg);
+          o.x = fmaf(o.x, al, a[u].x * wg);
+          o.y = fmaf(o.y, al, a[u].y * wg);
+          o.z = fmaf(o.z, al, a[u].z * wg);
+          o.w = fmaf(o.w, al, a[u].w * wg);
+          m = mn;
         }
       }
     }
+    s_o[sp][c] = o;
+    s_ml[sp][c] = make_float2(m, l);
+    __syncthreads();
+    if (sp == 0 && col) {
+      float M = -INFINITY;
 #pragma unroll
-    for (int k = 0; k < kE; ++k)
-      if (e4[k] < n4) {
-        const float inv = 1.f / l[k];
-        T* dst = static_cast<T*>(P.out) + (static_cast<int64_t>(mi.b) * P.hq + head0) * D + 4 * e4[k];
-        uint2 pk;
-        pk.x = pack2<T>(o[k].x * inv, o[k].y * inv);
-        pk.y = pack2<T>(o[k].z * inv, o[k].w * inv);
-        *reinterpret_cast<uint2*>(dst) = pk;
+      for (int k = 0; k < kMergeSplit; ++k) M = fmaxf(M, s_ml[k][c].x);
+      float Lsum = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kMergeSplit; ++k) {
+        const float wk = exp2f(s_ml[k][c].x - M);  // 0 for a group without partials
+        const float4 ok = s_o[k][c];
+        Lsum = fmaf(s_ml[k][c].y, wk, Lsum);
+        O.x = fmaf(ok.x, wk, O.x);
+        O.y = fmaf(ok.y, wk, O.y);
+        O.z = fmaf(ok.z, wk, O.z);
+        O.w = fmaf(ok.w, wk, O.w);
       }
+      const float inv = 1.f / Lsum;
+      T* dst = static_cast<T*>(P.out) + (static_cast<int64_t>(mi.b) * P.hq + head0) * D + 4 * c;
+      uint2 pk;
+      pk.x = pack2<T>(O.x * inv, O.y * inv);
+      pk.y = pack2<T>(O.z * inv, O.w * inv);
+      *reinterpret_cast<uint2*>(dst) = pk;
+    }
+    __syncthreads();  // s_o / s_ml are rewritten for the next work unit
   }
 }
 
@@ -1676,8 +1710,16 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   // the plan (partition list, merge records, counters) depends only on the
   // lengths, tables and shapes: a caller may reuse the workspace's plan
   if (!a.reuse_plan) {
-    cudaError_t e = launch_pdl(prep_kernel, dim3(1), dim3(1024), 0, s, P, row_uint4, 16 * n_sm,
-                               static_cast<int>(a.partition_tokens));
+    static bool prep_attr[64] = {false};
+    cudaError_t e = cudaSuccess;
+    if (!prep_attr[dev0 & 63]) {
+      e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kPrepSmem));
+      if (e == cudaSuccess) prep_attr[dev0 & 63] = true;
+    }
+    if (e == cudaSuccess)
+      e = launch_pdl(prep_kernel, dim3(1), dim3(1024), kPrepSmem, s, P, row_uint4, 16 * n_sm,
+                     static_cast<int>(a.partition_tokens));
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
       *why = std::string("prep launch: ") + cudaGetErrorString(e);
@@ -1726,28 +1768,43 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // one thread per float4 column of the G x D block: 256 threads for G = 8 at
-  // head_dim 128, else 128; a whole batch's merges fit in one wave
+  // one column of threads per float4 column of the G x D block (256 for G = 8
+  // at head_dim 128, else 128), 512 threads in all; a whole batch's merges
+  // fit in one wave
+  // Sequences of at most 8 partitions (of 512 tokens, the smallest) are
+  // merged by one thread group each, many CTAs per SM; longer ones by
+  // 512-thread CTAs whose groups share the partials.
   const bool wide = P.G * a.head_dim / 4 > 128;
-  const int mthreads = wide ? 256 : 128;
+  const bool split = (static_cast<int64_t>(a.max_seq_len) + kPartTokens - 1) / kPartTokens > 8;
+  const int mthreads = split ? kMergeThreads : (wide ? 256 : 128);
   int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
   if (mgrid > sms * (1024 / mthreads)) mgrid = sms * (1024 / mthreads);
   if (mgrid < 1) mgrid = 1;
-  const dim3 mg(static_cast<unsigned>(mgrid));
+  const dim3 mg(static_cast<unsigned>(mgrid)), mb(static_cast<unsigned>(mthreads));
   cudaError_t e;
   if (a.dtype == 1) {
     if (a.head_dim == 128) {
-      e = wide ? launch_pdl(merge_kernel<__nv_bfloat16, 128, 256>, mg, dim3(256), 0, s, P)
-               : launch_pdl(merge_kernel<__nv_bfloat16, 128, 128>, mg, dim3(128), 0, s, P);
+      if (wide)
+        e = split ? launch_pdl(merge_kernel<__nv_bfloat16, 128, 256, kMergeThreads>, mg, mb, 0, s, P)
+                  : launch_pdl(merge_kernel<__nv_bfloat16, 128, 256, 256>, mg, mb, 0, s, P);
+      else
+        e = split ? launch_pdl(merge_kernel<__nv_bfloat16, 128, 128, kMergeThreads>, mg, mb, 0, s, P)
+                  : launch_pdl(merge_kernel<__nv_bfloat16, 128, 128, 128>, mg, mb, 0, s, P);
     } else {
-      e = launch_pdl(merge_kernel<__nv_bfloat16, 64, 128>, mg, dim3(128), 0, s, P);
+      e = split ? launch_pdl(merge_kernel<__nv_bfloat16, 64, 128, kMergeThreads>, mg, mb, 0, s, P)
+                : launch_pdl(merge_kernel<__nv_bfloat16, 64, 128, 128>, mg, mb, 0, s, P);
     }
   } else {
     if (a.head_dim == 128) {
-      e = wide ? launch_pdl(merge_kernel<__half, 128, 256>, mg, dim3(256), 0, s, P)
-               : launch_pdl(merge_kernel<__half, 128, 128>, mg, dim3(128), 0, s, P);
+      if (wide)
+        e = split ? launch_pdl(merge_kernel<__half, 128, 256, kMergeThreads>, mg, mb, 0, s, P)
+                  : launch_pdl(merge_kernel<__half, 128, 256, 256>, mg, mb, 0, s, P);
+      else
+        e = split ? launch_pdl(merge_kernel<__half, 128, 128, kMergeThreads>, mg, mb, 0, s, P)
+                  : launch_pdl(merge_kernel<__half, 128, 128, 128>, mg, mb, 0, s, P);
     } else {
-      e = launch_pdl(merge_kernel<__half, 64, 128>, mg, dim3(128), 0, s, P);
+      e = split ? launch_pdl(merge_kernel<__half, 64, 128, kMergeThreads>, mg, mb, 0, s, P)
+                : launch_pdl(merge_kernel<__half, 64, 128, 128>, mg, mb, 0, s, P);
     }
   }
   if (e == cudaSuccess) e = cudaGetLastError();

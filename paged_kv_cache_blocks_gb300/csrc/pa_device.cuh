@@ -47,9 +47,10 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 // Per partition: sequence, partition index, clamped length, partial results of
 // the sequence, first token the partitions cover (after a shared prefix).
-struct PartInfo {
+struct alignas(16) PartInfo {
   int32_t b, p, len, nparts, start, pad0, pad1, pad2;
 };
+static_assert(sizeof(PartInfo) == 32, "two 16-byte words per partition record");
 
 // Everything the merge needs about one sequence with several partial results:
 // its partitions are first_full .. first_full+nfull-1, then tail (if nsuf >
