@@ -375,16 +375,29 @@ struct MmaState {
   __device__ __forceinline__ void block(uint32_t sK, uint32_t sV, int nvalid, float scale_log2,
                                         int lane, float*) {
     const int g = lane >> 2, t = lane & 3;
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    // S^T[token][head] = sum_d K[token][d] Q[head][d]
+    float s[4];
+    // S^T[token][head] = sum_d K[token][d] Q[head][d], as four independent
+    // accumulation chains (the dependent mma latency of a block is then two
+    // products at head_dim 128 instead of eight)
     {
+      constexpr int kChains = D / 16 < 4 ? D / 16 : 4;
+      float sp[kChains][4];
+#pragma unroll
+      for (int c = 0; c < kChains; ++c) sp[c][0] = sp[c][1] = sp[c][2] = sp[c][3] = 0.f;
       const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
       const int cofs = lane >> 4;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(a0, a1, a2, a3, chunk_addr(sK, r, 2 * ks + cofs));
-        Mma<T>::run(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        Mma<T>::run(sp[ks % kChains], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float acc = sp[0][e];
+#pragma unroll
+        for (int c = 1; c < kChains; ++c) acc += sp[c][e];
+        s[e] = acc;
       }
     }
     // s[0]: (token g, head 2t)  s[1]: (g, 2t+1)  s[2]: (g+8, 2t)  s[3]: (g+8, 2t+1)
@@ -399,34 +412,48 @@ struct MmaState {
       bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o2));
       bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o2));
     }
-    const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);  // finite: nvalid >= 1
-    const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-    l[0] = l[0] * al0 + (p0 + p2);
-    l[1] = l[1] * al1 + (p1 + p3);
-    m[0] = mn0;
-    m[1] = mn1;
+    // Lazy rescaling: the reference maximum m moves only when a block's
+    // maximum (finite: nvalid >= 1) exceeds it by more than 2^8 (log2
+    // units), so the weights stay below 256 -- inside the range of the 16-bit
+    // P operand -- and most blocks skip the rescale of l and o.  Exact either
+    // way: l and o are always relative to the same m.  The decision is
+    // warp-uniform (a vote over all lanes).
+    if (__any_sync(0xffffffffu, bm0 > m[0] + 8.f || bm1 > m[1] + 8.f)) {
+      const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);
+      const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
+      l[0] *= al0;
+      l[1] *= al1;
+      m[0] = mn0;
+      m[1] = mn1;
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
+      for (int mt = 0; mt < D / 16; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
     }
+    const float p0 = exp2f(x0 - m[0]), p1 = exp2f(x1 - m[1]);
+    const float p2 = exp2f(x2 - m[0]), p3 = exp2f(x3 - m[1]);
+    l[0] += p0 + p2;
+    l[1] += p1 + p3;
     // P[token][head] (accumulator layout) -> B operand (token = k, head = n)
     const uint32_t b0 = movmatrix_trans(pack2<T>(p0, p1));
     const uint32_t b1 = movmatrix_trans(pack2<T>(p2, p3));
-    // Rows past the sequence end may hold anything (NaN included): zero them
-    // in the V operand so 0 * garbage cannot reach the sum.
-    uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
-    if (nvalid < 16) {
-      mk0 = (2 * t < nvalid ? 0x0000ffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
-      mk1 = (2 * t + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
-    }
-    {
-      const int r = (lane & 7) + (lane >> 4) * 8;
-      const int cofs = (lane >> 3) & 1;
+    const int r = (lane & 7) + (lane >> 4) * 8;
+    const int cofs = (lane >> 3) & 1;
+    if (nvalid == 16) {  // a full block: every V row is a token
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(a0, a1, a2, a3, chunk_addr(sV, r, 2 * mt + cofs));
+        Mma<T>::run(o[mt], a0, a1, a2, a3, b0, b1);
+      }
+    } else {
+      // Rows past the sequence end may hold anything (NaN included): zero
+      // them in the V operand so 0 * garbage cannot reach the sum.
+      const uint32_t mk0 = (2 * t < nvalid ? 0x0000ffffu : 0u) | (2 * t + 1 < nvalid ? 0xffff0000u : 0u);
+      const uint32_t mk1 = (2 * t + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * t + 9 < nvalid ? 0xffff0000u : 0u);
 #pragma unroll
       for (int mt = 0; mt < D / 16; ++mt) {
         uint32_t a0, a1, a2, a3;
