@@ -406,19 +406,20 @@ struct MmaState {
     const float x1 = v0 ? s[1] * scale_log2 : -INFINITY;
     const float x2 = v1 ? s[2] * scale_log2 : -INFINITY;
     const float x3 = v1 ? s[3] * scale_log2 : -INFINITY;
+    // Lazy rescaling: the reference maximum m moves only when some score of
+    // the block exceeds it by more than 2^8 (log2 units), so the weights
+    // stay below 256 -- inside the range of the 16-bit P operand -- and most
+    // blocks need neither the block maximum (a shuffle reduction over the
+    // token rows) nor the rescale of l and o.  Exact either way: l and o are
+    // always relative to the same m.  Each lane tests its own scores; the
+    // decision is a vote over the warp.
     float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
-#pragma unroll
-    for (int o2 = 4; o2 < 32; o2 <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o2));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o2));
-    }
-    // Lazy rescaling: the reference maximum m moves only when a block's
-    // maximum (finite: nvalid >= 1) exceeds it by more than 2^8 (log2
-    // units), so the weights stay below 256 -- inside the range of the 16-bit
-    // P operand -- and most blocks skip the rescale of l and o.  Exact either
-    // way: l and o are always relative to the same m.  The decision is
-    // warp-uniform (a vote over all lanes).
     if (__any_sync(0xffffffffu, bm0 > m[0] + 8.f || bm1 > m[1] + 8.f)) {
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {  // block maximum (finite: nvalid >= 1)
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o2));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o2));
+      }
       const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);
       const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
       l[0] *= al0;
@@ -725,18 +726,18 @@ struct Fp8State {
     const float x1 = v0 ? s[1] * sl : -INFINITY;
     const float x2 = v1 ? s[2] * sl : -INFINITY;
     const float x3 = v1 ? s[3] * sl : -INFINITY;
+    // Lazy rescaling, as for the 16-bit caches: the reference maximum m
+    // moves only when some score of the block exceeds it by more than 2^8,
+    // so the weights stay below 256 (inside the fp16 P operand's range) and
+    // most blocks need neither the block maximum nor the rescale of l and o.
+    // Each lane tests its own scores; the decision is a vote over the warp.
     float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
-#pragma unroll
-    for (int o2 = 4; o2 < 32; o2 <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o2));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o2));
-    }
-    // Lazy rescaling: the reference maximum m moves only when a block's
-    // maximum exceeds it by more than 2^8 (log2 units), so the weights stay
-    // below 256 (exact in the fp16 P operand's range) and most blocks skip
-    // the rescale of l and o.  Exact either way: l and o are always relative
-    // to the same m.  The decision is warp-uniform (a vote over all lanes).
     if (__any_sync(0xffffffffu, bm0 > m[0] + 8.f || bm1 > m[1] + 8.f)) {
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {  // block maximum
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o2));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o2));
+      }
       const float mn0 = fmaxf(m[0], bm0), mn1 = fmaxf(m[1], bm1);
       const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
       l[0] *= al0;
