@@ -48,6 +48,17 @@ namespace pa {
 
 struct ItemInfo {
   int32_t b, h, p, len, nparts, nblk, g0, part, start, pad0;
+  float k_scale, v_scale;  // FP8 caches: the KV head's dequantisation scales
+};
+
+// The scheduler stages each item's G query rows in shared memory, one row per
+// query head, rows padded by 16 bytes so that the consumers' fragment loads
+// (8 rows x 4 lanes) fall in distinct banks.
+template <int D>
+struct QStage {
+  static constexpr int kRow = D + 8;                 // elements per staged row
+  static constexpr int kChunks = D * 2 / 16;         // 16-byte chunks per row
+  static constexpr int kSlotBytes = 8 * kRow * 2;    // up to G = 8 rows
 };
 
 struct DecodeParams {
@@ -193,9 +204,15 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
     f2 += n / (2 * kPartTokens);
     f4 += n / (4 * kPartTokens);
   }
-  atomicAdd(&s_full[0], f1);
-  atomicAdd(&s_full[1], f2);
-  atomicAdd(&s_full[2], f4);
+  // one shared atomic per warp: 1024 same-address atomics would serialise
+  f1 = __reduce_add_sync(0xffffffffu, f1);
+  f2 = __reduce_add_sync(0xffffffffu, f2);
+  f4 = __reduce_add_sync(0xffffffffu, f4);
+  if ((tid & 31) == 0) {
+    atomicAdd(&s_full[0], f1);
+    atomicAdd(&s_full[1], f2);
+    atomicAdd(&s_full[2], f4);
+  }
   __syncthreads();
   // force_pt (512 / 1024 / 2048, or 0 to choose) fixes the size instead
   int pt = kPartTokens, total_full = s_full[0];
@@ -265,6 +282,8 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
     const int r = (L - st) % pt;
     int tot_f;
     const int fo = block_exclusive_scan(nfull, sw, &tot_f);
+    bool need_merge = false;
+    MergeInfo mi{};
     if (b < P.num_seqs) {
       int4 sp = make_int4(0, 0, 0, st);
       if (use_groups) {
@@ -287,10 +306,15 @@ __global__ void __launch_bounds__(1024) prep_kernel(DecodeParams P, int row_uint
         for (int p = 0; p < nfull; ++p) P.parts[first + p] = PartInfo{b, p, L, nparts, st, 0, 0, 0};
       }
       if (r) P.parts[tail_idx] = PartInfo{b, nfull, L, nparts, st, 0, 0, 0};
-      if (nparts > 1 || sp.z > 0)
-        P.split[atomicAdd(&s_nsplit, 1)] =
-            MergeInfo{b, first, tail_idx, nfull, nfull + (r != 0), sp.x, sp.y, sp.z};
+      need_merge = nparts > 1 || sp.z > 0;
+      mi = MergeInfo{b, first, tail_idx, nfull, nfull + (r != 0), sp.x, sp.y, sp.z};
     }
+    // one shared atomic per warp for the merge-record slots
+    const unsigned mm = __ballot_sync(0xffffffffu, need_merge);
+    int slot0 = 0;
+    if ((tid & 31) == 0 && mm) slot0 = atomicAdd(&s_nsplit, __popc(mm));
+    slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+    if (need_merge) P.split[slot0 + __popc(mm & ((1u << (tid & 31)) - 1u))] = mi;
     carry_full += tot_f;
   }
   __syncthreads();
@@ -353,10 +377,10 @@ struct MmaState {
   float m[2], l[2];
   float o[D / 16][4];
 
-  __device__ __forceinline__ void begin(const DecodeParams& P, const ItemInfo& it, int lane, float*) {
+  __device__ __forceinline__ void begin(const DecodeParams& P, const ItemInfo& it, int lane, float*,
+                                        const T* qs) {
     const int g = lane >> 2, t = lane & 3;
-    const T* q = static_cast<const T*>(P.q) +
-                 (static_cast<int64_t>(it.b) * P.hq + it.h * P.G + g) * D;
+    const T* q = qs + g * QStage<D>::kRow;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       if (g < P.G) {
@@ -509,10 +533,10 @@ struct FmaState {
   int G;
 
   __device__ __forceinline__ void begin(const DecodeParams& P, const ItemInfo& it, int lane,
-                                        float* scr) {
+                                        float* scr, const T* qs) {
     G = P.G;
-    const T* q = static_cast<const T*>(P.q) + (static_cast<int64_t>(it.b) * P.hq + it.h * P.G) * D;
-    for (int e = lane; e < P.G * D; e += 32) scr[e] = to_float<T>(q[e]) * P.scale_log2;
+    for (int e = lane; e < P.G * D; e += 32)
+      scr[e] = to_float<T>(qs[(e / D) * QStage<D>::kRow + e % D]) * P.scale_log2;
 #pragma unroll
     for (int j = 0; j < HPG; ++j) {
       m[j] = -INFINITY;
@@ -672,10 +696,10 @@ struct Fp8State {
   float o[D / 16][4];
   float sl, vs;
 
-  __device__ __forceinline__ void begin(const DecodeParams& P, const ItemInfo& it, int lane, float*) {
+  __device__ __forceinline__ void begin(const DecodeParams& P, const ItemInfo& it, int lane, float*,
+                                        const T* qs) {
     const int g = lane >> 2, t = lane & 3;
-    const T* q = static_cast<const T*>(P.q) +
-                 (static_cast<int64_t>(it.b) * P.hq + it.h * P.G + g) * D;
+    const T* q = qs + g * QStage<D>::kRow;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
       if (g < P.G) {
@@ -687,8 +711,8 @@ struct Fp8State {
         qb[ks][0] = qb[ks][1] = 0u;
       }
     }
-    sl = P.scale_log2 * P.k_scale[it.h];
-    vs = P.v_scale[it.h];
+    sl = P.scale_log2 * it.k_scale;
+    vs = it.v_scale;
     m[0] = m[1] = -INFINITY;
     l[0] = l[1] = 0.f;
 #pragma unroll
@@ -837,7 +861,9 @@ struct AttendCfg {
   // full[S], empty[S], item_full[2], item_empty[2], merge_full[2]
   static constexpr size_t kInfoOff = kBarOff + (2 * S + 6) * sizeof(uint64_t);
   static constexpr size_t kIdsOff = kInfoOff + 2 * sizeof(ItemInfo);
-  static constexpr size_t kAbortOff = kIdsOff + 2 * kMaxPartBlocks * sizeof(int32_t);
+  static constexpr size_t kQOff = kIdsOff + 2 * kMaxPartBlocks * sizeof(int32_t);
+  static constexpr size_t kAbortOff = kQOff + 2 * QStage<D>::kSlotBytes;
+  static_assert(kQOff % 16 == 0 && QStage<D>::kSlotBytes % 16 == 0, "16-byte staged query rows");
   static constexpr size_t kBytes = kAbortOff + 16 + 1024;  // + slack to 1024-align the base
 };
 
@@ -861,6 +887,7 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
   uint64_t* merge_full = item_empty + 2;
   ItemInfo* info = reinterpret_cast<ItemInfo*>(smem + Cfg::kInfoOff);
   int32_t* ids = reinterpret_cast<int32_t*>(smem + Cfg::kIdsOff);
+  uint8_t* qstage = smem + Cfg::kQOff;  // two slots of staged query rows
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kAbortOff);
   int* err = &P.ws->error_bits;
 
@@ -949,19 +976,55 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
         }
         break;
       }
+      // the item's block ids, its G query rows and (FP8) the KV head's
+      // scales: every load issued before any store, one round trip in all
       const int32_t* trow = P.tables + static_cast<int64_t>(pi.b) * P.max_blocks + first_tok / kBlock;
-      for (int j = lane; j < nblk; j += 32) {
-        int32_t id = trow[j];
-        if (id < 0 || id >= P.num_blocks) {
-          atomicOr(err, kErrBlockId);
-          id = -1;
+      const uint4* qsrc = reinterpret_cast<const uint4*>(
+          static_cast<const T*>(P.q) + (static_cast<int64_t>(pi.b) * P.hq + h * P.G) * D);
+      const int nq = P.G * QStage<D>::kChunks;
+      constexpr int kIdIt = kMaxPartBlocks / 32, kQIt = 8 * QStage<D>::kChunks / 32;
+      int32_t idv[kIdIt];
+      uint4 qv[kQIt];
+#pragma unroll
+      for (int k = 0; k < kIdIt; ++k) {
+        const int j = lane + 32 * k;
+        idv[k] = j < nblk ? trow[j] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < kQIt; ++k) {
+        const int c = lane + 32 * k;
+        if (c < nq) qv[k] = qsrc[c];
+      }
+      float ksc = 0.f, vsc = 0.f;
+      if (kFp8 && lane == 0) {
+        ksc = P.k_scale[h];
+        vsc = P.v_scale[h];
+      }
+#pragma unroll
+      for (int k = 0; k < kIdIt; ++k) {
+        const int j = lane + 32 * k;
+        if (j < nblk) {
+          int32_t id = idv[k];
+          if (id < 0 || id >= P.num_blocks) {
+            atomicOr(err, kErrBlockId);
+            id = -1;
+          }
+          ids[slot * kMaxPartBlocks + j] = id;
         }
-        ids[slot * kMaxPartBlocks + j] = id;
+      }
+      uint8_t* qdst = qstage + slot * QStage<D>::kSlotBytes;
+#pragma unroll
+      for (int k = 0; k < kQIt; ++k) {
+        const int c = lane + 32 * k;
+        if (c < nq) {
+          const int row = c / QStage<D>::kChunks, ch = c - row * QStage<D>::kChunks;
+          *reinterpret_cast<uint4*>(qdst + row * QStage<D>::kRow * 2 + ch * 16) = qv[k];
+        }
       }
       __syncwarp();
       if (lane == 0) {
         info[slot] = ItemInfo{pi.b, h, pi.p, pi.len, pi.nparts, nblk, static_cast<int32_t>(g), part,
-                              pi.start, 0};
+                              pi.start, 0, ksc, vsc};
         mbar_arrive(&item_full[slot]);
         // a plan made for other lengths is flagged (after the item is out: the
         // check costs a global load the copies need not wait for)
@@ -1039,11 +1102,14 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     bool ok = mbar_wait(&item_full[slot], (it >> 1) & 1, abort_flag, err);
     if (!__all_sync(0xffffffffu, ok)) break;
     const ItemInfo inf = info[slot];
+    // the staged query rows are read before the slot is handed back
+    if (inf.b >= 0)
+      st.begin(P, inf, lane, scr,
+               reinterpret_cast<const T*>(qstage + slot * QStage<D>::kSlotBytes));
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
     if (inf.b < 0) break;
 
-    st.begin(P, inf, lane, scr);
     bool alive = true;
     // Block j of the item goes to consumer j % NC, so which warp sums which
     // blocks does not depend on scheduling (outputs are bit-reproducible).
