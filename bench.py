@@ -816,7 +816,7 @@ def run_pa(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     w = W.WORKLOADS[args.workload]
-    b = W.make_batch(args.workload, seed=rank, poison=False, device="cuda")
+    b = W.make_batch(args.workload, seed=rank, poison=False, device="cuda", num_layers=args.layers)
     dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     layers = [(Lr.q.view(dt), Lr.k_cache.view(dt), Lr.v_cache.view(dt), Lr.new_k.view(dt),
@@ -1456,6 +1456,9 @@ def main():
                     help="decode shared-prefix groups with pa_decode_grouped (fullstep)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="skip timing the step replayed from a CUDA graph")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decode only the first N layers of the workload (a smaller case to "
+                         "profile; the line's config then names N layers)")
     ap.add_argument("--no-per-config", dest="per_config", action="store_false",
                     help="skip measuring every decode config after the headline")
     args = ap.parse_args()

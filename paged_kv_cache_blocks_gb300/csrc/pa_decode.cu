@@ -860,7 +860,9 @@ struct AttendCfg {
   // thread issues their copies, so two warps issue alternate stages
   static constexpr int kIss = kFp8 ? 2 : 1;
   static_assert(S % kIss == 0, "each ring stage must be refilled by one copy warp");
-  static constexpr int kThreads = 32 * (NC + 1 + kIss);  // scheduler, copy warps, NC consumers
+  // scheduler, copy warps, NC consumers, combiner
+  static constexpr int kThreads = 32 * (NC + 2 + kIss);
+  static_assert((NC & (NC - 1)) == 0 && NC * 8 <= 32, "the combiner holds one lane per (residue, head)");
   static constexpr int kKBytes = kFp8 ? kBlock * D : Tile<D>::kKVBytes;  // K part of a stage
   static constexpr int kStageBytes = kFp8 ? 2 * kBlock * D : Tile<D>::kStageBytes;
   static constexpr size_t kStagesOff = 0;
@@ -868,8 +870,8 @@ struct AttendCfg {
   static constexpr size_t kScrOff = kMergeOff + 2 * sizeof(MergeSlot<D, NC>);
   static constexpr size_t kScrBytes = kFma ? NC * FmaScratch<D>::kFloats * sizeof(float) : 0;
   static constexpr size_t kBarOff = align_up_c(kScrOff + kScrBytes, 16);
-  // full[S], empty[S], item_full[2], item_empty[2], merge_full[2]
-  static constexpr size_t kInfoOff = kBarOff + (2 * S + 6) * sizeof(uint64_t);
+  // full[S], empty[S], item_full[2], item_empty[2], merge_full[2], merge_empty[2]
+  static constexpr size_t kInfoOff = kBarOff + (2 * S + 8) * sizeof(uint64_t);
   static constexpr size_t kIdsOff = kInfoOff + 2 * sizeof(ItemInfo);
   static constexpr size_t kQOff = kIdsOff + 2 * kMaxPartBlocks * sizeof(int32_t);
   static constexpr size_t kAbortOff = kQOff + 2 * QStage<D>::kSlotBytes;
@@ -895,6 +897,7 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
   uint64_t* item_full = empty + S;
   uint64_t* item_empty = item_full + 2;
   uint64_t* merge_full = item_empty + 2;
+  uint64_t* merge_empty = merge_full + 2;
   ItemInfo* info = reinterpret_cast<ItemInfo*>(smem + Cfg::kInfoOff);
   int32_t* ids = reinterpret_cast<int32_t*>(smem + Cfg::kIdsOff);
   uint8_t* qstage = smem + Cfg::kQOff;  // two slots of staged query rows
@@ -909,8 +912,9 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&item_full[s], 1);
-      mbar_init(&item_empty[s], NC + Cfg::kIss);  // consumers + the copy threads
+      mbar_init(&item_empty[s], NC + Cfg::kIss + 1);  // consumers, copy threads, combiner
       mbar_init(&merge_full[s], NC);
+      mbar_init(&merge_empty[s], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -1110,6 +1114,82 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     return;
   }
 
+  if (warp == Cfg::kIss + 1 + NC) {
+    // ------------------------------------------------------------ combiner
+    // Folds the NC consumer states of each item, in item order, into the
+    // output (one partition) or the partition's (max, sum, unnormalised
+    // output); the consumers meanwhile go on with the next item.  Residue
+    // class k of the item's blocks (j % NC == k) was summed by consumer
+    // (g0 + k) % NC; the classes are folded in the order k = 0 .. NC-1, so the
+    // arithmetic does not depend on where the item fell in the CTA's stream.
+    const int G = P.G;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it & 1;
+      bool ok = mbar_wait(&item_full[slot], (it >> 1) & 1, abort_flag, err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const ItemInfo inf = info[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      if (inf.b < 0) break;
+      ok = mbar_wait(&merge_full[slot], (it >> 1) & 1, abort_flag, err);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const MergeSlot<D, NC>& ms = merge[slot];
+      // lane (k, hd) = (lane >> 3, lane & 7): residue class k's maximum and sum
+      // for head hd; the head's largest maximum, the class weights and the
+      // sum over the classes (in class order) by lane (0, hd)
+      const int kk = lane >> 3, hh = lane & 7;
+      const int wk_slot = static_cast<int>((static_cast<uint32_t>(inf.g0) + kk) & (NC - 1));
+      const float mk = (kk < NC && hh < G) ? ms.m[wk_slot][hh] : -INFINITY;
+      const float lk = (kk < NC && hh < G) ? ms.l[wk_slot][hh] : 0.f;
+      float wts[NC];
+      float M = -INFINITY, Lsum = 0.f;
+#pragma unroll
+      for (int k = 0; k < NC; ++k) M = fmaxf(M, __shfl_sync(0xffffffffu, mk, k * 8 + hh));
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        wts[k] = exp2f(__shfl_sync(0xffffffffu, mk, k * 8 + hh) - M);
+        Lsum = fmaf(__shfl_sync(0xffffffffu, lk, k * 8 + hh), wts[k], Lsum);
+      }
+      const int head0 = inf.h * G;
+      const bool single = inf.nparts == 1;
+      constexpr int kD4 = D / 4;
+      for (int base = 0; base < G * kD4; base += 32) {  // whole warp each round (shuffles)
+        const int idx = base + lane;
+        const int hd = min(idx / kD4, G - 1), d4 = idx - (idx / kD4) * kD4;
+        const float Mh = __shfl_sync(0xffffffffu, M, hd);
+        const float Lh = __shfl_sync(0xffffffffu, Lsum, hd);
+        float wh[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) wh[k] = __shfl_sync(0xffffffffu, wts[k], hd);
+        if (idx >= G * kD4) continue;
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+          const int ws = static_cast<int>((static_cast<uint32_t>(inf.g0) + k) & (NC - 1));
+          const float4 a = *reinterpret_cast<const float4*>(&ms.acc[ws][hd][4 * d4]);
+          O.x = fmaf(a.x, wh[k], O.x);
+          O.y = fmaf(a.y, wh[k], O.y);
+          O.z = fmaf(a.z, wh[k], O.z);
+          O.w = fmaf(a.w, wh[k], O.w);
+        }
+        const int64_t row = static_cast<int64_t>(inf.b) * P.hq + head0 + hd;
+        if (single) {
+          uint2 pk;
+          pk.x = pack2<T>(O.x / Lh, O.y / Lh);
+          pk.y = pack2<T>(O.z / Lh, O.w / Lh);
+          *reinterpret_cast<uint2*>(static_cast<T*>(P.out) + row * D + 4 * d4) = pk;
+        } else {
+          const int64_t prow = static_cast<int64_t>(inf.part) * P.hq + head0 + hd;
+          *reinterpret_cast<float4*>(P.acc + prow * D + 4 * d4) = O;
+          if (d4 == 0) P.ml[prow] = make_float2(Mh, Lh);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&merge_empty[slot]);
+    }
+    return;
+  }
+
   // ---------------------------------------------------------------- consumers
   const int w = warp - 1 - Cfg::kIss;
   const int pt = *reinterpret_cast<volatile int32_t*>(&P.ws->part_tokens);
@@ -1129,13 +1209,14 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     if (inf.b < 0) break;
 
     bool alive = true;
-    // Block j of the item goes to consumer j % NC, so which warp sums which
-    // blocks does not depend on scheduling (outputs are bit-reproducible).
-    // With S a multiple of NC, the uses of a ring stage inside one item all
-    // belong to one warp, in order, and items are separated by the merge
-    // barrier below, so a parity wait can never be satisfied by an older
-    // phase of its stage (which would read the stage before its copy lands).
-    for (int j = w; j < inf.nblk; j += NC) {
+    // Block g of the CTA's stream goes to consumer g % NC: with S a multiple
+    // of NC every ring stage has one consumer, which waits for each of its
+    // rounds only after releasing the one before, so a parity wait can never
+    // be satisfied by an older phase of its stage, and no barrier between
+    // items is needed.  Within an item the blocks j with j % NC == k (one
+    // residue class) are summed by one warp in order, whichever warp it is.
+    const int j0 = static_cast<int>((static_cast<uint32_t>(w) - static_cast<uint32_t>(inf.g0)) & (NC - 1));
+    for (int j = j0; j < inf.nblk; j += NC) {
       const uint32_t gg = inf.g0 + j;
       const int s = gg % S;
       ok = mbar_wait(&full[s], (gg / S) & 1, abort_flag, err);
@@ -1151,45 +1232,19 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     }
     if (!alive) break;
 
-    MergeSlot<D, NC>& ms = merge[slot];
-    st.template store<NC>(ms, w, lane);
+    // hand the state to the combiner (double-buffered by item parity) and go on
+    ok = mbar_wait(&merge_empty[slot], ((it >> 1) & 1) ^ 1, abort_flag, err);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    st.template store<NC>(merge[slot], w, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(&merge_full[slot]);
-    ok = mbar_wait(&merge_full[slot], (it >> 1) & 1, abort_flag, err);
-    if (!__all_sync(0xffffffffu, ok)) break;
-
-    // Combine the NC warp states; this thread's share of the G*D outputs.
-    const int G = P.G;
-    const int head0 = inf.h * G;
-    const bool single = inf.nparts == 1;
-    for (int e = w * 32 + lane; e < G * D; e += NC * 32) {
-      const int hd = e / D, d = e - hd * D;
-      float M = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < NC; ++k) M = fmaxf(M, ms.m[k][hd]);
-      float Lsum = 0.f, O = 0.f;
-#pragma unroll
-      for (int k = 0; k < NC; ++k) {
-        const float wk = exp2f(ms.m[k][hd] - M);
-        Lsum = fmaf(ms.l[k][hd], wk, Lsum);
-        O = fmaf(ms.acc[k][hd][d], wk, O);
-      }
-      const int64_t row = static_cast<int64_t>(inf.b) * P.hq + head0 + hd;
-      if (single) {
-        static_cast<T*>(P.out)[row * D + d] = from_float<T>(O / Lsum);
-      } else {
-        const int64_t prow = static_cast<int64_t>(inf.part) * P.hq + head0 + hd;
-        P.acc[prow * D + d] = O;
-        if (d == 0) P.ml[prow] = make_float2(M, Lsum);
-      }
-    }
   }
 }
 
 // The tensor maps live in kernel parameter space (__grid_constant__); the body
 // takes their addresses for the copies.
 template <typename T, int D, int NC, int S, bool kFma, int HPG>
-__global__ void __launch_bounds__(32 * (NC + 2))
+__global__ void __launch_bounds__(32 * (NC + 3))
     attend_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const DecodeParams P) {
   attend_body<T, D, NC, S, kFma, HPG, false>(tm_k, tm_v, P);
@@ -1199,7 +1254,7 @@ __global__ void __launch_bounds__(32 * (NC + 2))
 // copy thread per CTA left the FP8 kernel short of copies in flight at this
 // tile size (316 vs 309 us on the Llama-3-70B-shaped batch).
 template <typename T, int D, int NC, int S>
-__global__ void __launch_bounds__(32 * (NC + 3), 2)
+__global__ void __launch_bounds__(32 * (NC + 4), 2)
     attend_fp8_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const DecodeParams P) {
   attend_body<T, D, NC, S, false, 1, true>(tm_k, tm_v, P);

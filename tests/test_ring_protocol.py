@@ -2,20 +2,30 @@
 
 The kernel's producer warp streams blocks into S stages; consumer warps wait
 on a per-stage "full" mbarrier with a parity bit and release the stage on an
-"empty" mbarrier; at the end of every work item the consumers meet at a
-merge barrier.  A parity wait only asks "has the phase of this parity
+"empty" mbarrier.  A parity wait only asks "has the phase of this parity
 completed", so if two consecutive uses of one stage could be consumed by
-different warps without a barrier between them, a warp waiting for round
+different warps without an ordering between them, a warp waiting for round
 r+1 could pass on round r-1's completed phase and read the stage before its
-copy lands.  The kernel gives block j of an item to consumer j % NC and
-requires S % NC == 0.  This test runs a randomised discrete-event model of
-the protocol with exact mbarrier parity semantics (try_wait.parity(P) is
-true iff the barrier's current phase parity differs from P) and checks that
-no consumer ever reads a stage holding another block: safe for every S that
-is a multiple of NC, unsafe (stale reads or deadlock) for S = 6 or 10 with
-NC = 4.  The alternative rule (block g of the CTA's whole stream to consumer
-g % NC) is safe too, but makes the per-warp grouping of sums depend on
-scheduling, so outputs would not be bit-reproducible.
+copy lands.
+
+The kernel gives block g of the CTA's whole block stream to consumer
+g % NC and requires S % NC == 0, so every stage has one consumer and no
+barrier is needed between work items: at the end of an item each consumer
+hands its state to a combiner warp and goes on with the next item.  (Which
+warp sums which blocks of an item then depends on where the item starts in
+the stream, but the blocks of one residue class j % NC are always summed
+together and in order, and the combiner folds the classes in class order,
+so the outputs stay bit-reproducible.)  The earlier rule, block j of an item
+to consumer j % NC, is safe only with a barrier between items; without one
+it reads stale stages, which the model shows too.
+
+This test runs a randomised discrete-event model of the protocol with exact
+mbarrier parity semantics (try_wait.parity(P) is true iff the barrier's
+current phase parity differs from P) and checks that no consumer ever reads
+a stage holding another block: safe for every S that is a multiple of NC
+under the kernel's rule without a merge barrier, unsafe (stale reads or
+deadlock) for S = 6 or 10 with NC = 4, and unsafe for the item-relative rule
+without the barrier.
 
 The FP8 kernel has two copy threads: thread p refills the stages of the
 blocks g with g % 2 == p, in order, each independently of the other (one
@@ -54,9 +64,10 @@ class Barrier:
             self.pending = self.count
 
 
-def simulate(S, NC, rule, items, seed, producers=1):
+def simulate(S, NC, rule, items, seed, producers=1, merge_barrier=True):
     """Returns the number of stale reads (0 = protocol safe), or -1 if the
-    protocol deadlocks (nobody can move for a long time)."""
+    protocol deadlocks (nobody can move for a long time).  merge_barrier:
+    consumers wait for each other at the end of every item."""
     rng = random.Random(seed)
     full = [Barrier(1) for _ in range(S)]
     empty = [Barrier(1) for _ in range(S)]
@@ -119,7 +130,14 @@ def simulate(S, NC, rule, items, seed, producers=1):
             continue
         if c["pos"] == len(c["list"]):
             merge_arrived[c["it"]] += 1
-            c["at_merge"] = True
+            if merge_barrier:
+                c["at_merge"] = True
+            else:                       # hand the state over and go on
+                c["it"] += 1
+                if c["it"] == len(items):
+                    done[actor] = True
+                else:
+                    c["list"], c["pos"] = blocks_of(actor, c["it"]), 0
             continue
         blk = c["list"][c["pos"]]
         s, r = blk % S, blk // S
@@ -158,3 +176,21 @@ def test_two_producers_on_alternate_stages_never_read_a_stale_stage(S, NC, rule)
     rng = random.Random(S * 1000 + NC)
     for seed in range(40):
         assert simulate(S, NC, rule, random_items(rng, 12), seed, producers=2) == 0
+
+
+@pytest.mark.parametrize("producers", [1, 2])
+@pytest.mark.parametrize("S,NC", [(4, 4), (8, 4), (16, 4), (8, 2), (8, 8)])
+def test_stage_owned_consumers_need_no_barrier_between_items(S, NC, producers):
+    """The kernel's protocol: block g to consumer g % NC, no merge barrier."""
+    rng = random.Random(S * 10 + NC + producers)
+    for seed in range(40):
+        assert simulate(S, NC, "global", random_items(rng, 12), seed, producers,
+                        merge_barrier=False) == 0
+
+
+def test_item_relative_consumers_without_barrier_are_unsafe():
+    """Block j of an item to consumer j % NC is safe only with the barrier."""
+    rng = random.Random(11)
+    results = [simulate(8, 4, "item", random_items(rng, 12), seed, merge_barrier=False)
+               for seed in range(40)]
+    assert any(r != 0 for r in results)
