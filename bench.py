@@ -1184,12 +1184,16 @@ def time_graph(step, steps, warmup, stream, barrier, dist, dev, units, world):
 # the ncu captures summarised in profiles/ (file named below), keyed by the
 # hash of the kernel sources they were taken on: a changed kernel reports null.
 TRAFFIC = {
-    ("llama70b", "auto"): {"bytes": 3773.80e6 + 16.26e6, "kernel_src": "9753814105dbec76",
+    ("llama70b", "auto"): {"bytes": 3773.90e6 + 17.71e6, "kernel_src": "7dc38db4d303159b",
                            "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "mma"): {"bytes": 3773.80e6 + 16.26e6, "kernel_src": "9753814105dbec76",
+    ("llama70b", "mma"): {"bytes": 3773.90e6 + 17.71e6, "kernel_src": "7dc38db4d303159b",
                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "fp8"): {"bytes": 1889.40e6 + 15.25e6, "kernel_src": "9753814105dbec76",
+    ("llama70b", "fp8"): {"bytes": 1889.37e6 + 16.41e6, "kernel_src": "7dc38db4d303159b",
                           "profile": "profiles/decode_step_llama70b_fp8_launches.md"},
+    ("fullstep", "auto"): {"bytes": 1979.17e6 + 12.46e6, "kernel_src": "7dc38db4d303159b",
+                           "profile": "profiles/attend_kernel_fullstep_shared_prefix_l2.md"},
+    ("fullstep", "grouped"): {"bytes": 1937.92e6 + 10.35e6, "kernel_src": "7dc38db4d303159b",
+                              "profile": "profiles/attend_kernel_fullstep_shared_prefix_l2.md"},
     ("cow", "auto"): {"bytes": 268.52e6 + 216.53e6, "kernel_src": "ba3a77c251cf3178",
                       "profile": "profiles/copy_blocks_kernel_cow.md"},
     # the 8 prefill launches of one step (iterations 1..8), summed
