@@ -925,7 +925,6 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
   }
   __syncthreads();
   pdl_wait();               // the plan, q and the caches are ready from here on
-  pdl_launch_dependents();  // the merge kernel may be scheduled (it waits for this grid)
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler
@@ -995,6 +994,11 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
         if (lane == 0) {
           info[slot].b = -1;
           mbar_arrive(&item_full[slot]);
+          // The merge kernel may be scheduled once every CTA's queue is empty
+          // (it waits for this grid before reading anything).  Not earlier:
+          // its CTAs would sit resident beside this kernel's CTAs through the
+          // whole stream and slow them down.
+          pdl_launch_dependents();
         }
         break;
       }
@@ -1152,6 +1156,7 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
       }
       const int head0 = inf.h * G;
       const bool single = inf.nparts == 1;
+      const uint64_t pol_last = l2_policy_evict_last();  // the merge reads the partials back
       constexpr int kD4 = D / 4;
       for (int base = 0; base < G * kD4; base += 32) {  // whole warp each round (shuffles)
         const int idx = base + lane;
@@ -1180,7 +1185,7 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
           *reinterpret_cast<uint2*>(static_cast<T*>(P.out) + row * D + 4 * d4) = pk;
         } else {
           const int64_t prow = static_cast<int64_t>(inf.part) * P.hq + head0 + hd;
-          *reinterpret_cast<float4*>(P.acc + prow * D + 4 * d4) = O;
+          st_global_hint(reinterpret_cast<float4*>(P.acc + prow * D + 4 * d4), O, pol_last);
           if (d4 == 0) P.ml[prow] = make_float2(Mh, Lh);
         }
       }
@@ -1274,9 +1279,9 @@ __global__ void __launch_bounds__(32 * (NC + 4), 2)
 // rounds of a long sequence (64 partials at G = 4: 8 rounds -> 2).
 
 template <typename T, int D, int kCols, int kThreads>
-__global__ void __launch_bounds__(kThreads, 1024 / kThreads)
+__global__ void __launch_bounds__(kThreads, kThreads >= 512 ? 2 : 512 / kThreads)
     merge_kernel(const DecodeParams P) {
-  constexpr int U = 6;
+  constexpr int U = kThreads >= 512 ? 6 : 8;  // partials in flight per thread (no spills)
   constexpr int kMergeSplit = kThreads / kCols;
   __shared__ float4 s_o[kMergeSplit][kCols];
   __shared__ float2 s_ml[kMergeSplit][kCols];
@@ -1951,7 +1956,8 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   const bool split = (static_cast<int64_t>(a.max_seq_len) + kPartTokens - 1) / kPartTokens > 8;
   const int mthreads = split ? kMergeThreads : (wide ? 256 : 128);
   int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  if (mgrid > sms * (1024 / mthreads)) mgrid = sms * (1024 / mthreads);
+  const int mres = mthreads >= 512 ? 2 : 512 / mthreads;  // resident merge CTAs per SM
+  if (mgrid > sms * mres) mgrid = sms * mres;
   if (mgrid < 1) mgrid = 1;
   const dim3 mg(static_cast<unsigned>(mgrid)), mb(static_cast<unsigned>(mthreads));
   cudaError_t e;
