@@ -12,21 +12,23 @@
 //   1. prep   (1 CTA)    clamps lengths, cuts every sequence into 512-token
 //                        partitions, lists them (full partitions first) in
 //                        the workspace and resets the work counters;
-//   2. attend (persistent, two or three CTAs per SM)
+//   2. attend (persistent, two CTAs per SM)
 //                        one work item = (partition, KV head).  Warp 0
-//                        schedules: it takes items from an atomic counter
-//                        (one ahead) and stages each item's partition record
-//                        and block ids in a two-slot item ring.  Warp 1 (one
-//                        thread; FP8: warps 1 and 2, alternate stages)
-//                        streams each block's K and V tiles into a
-//                        ring of shared-memory stages with TMA (128-byte
-//                        swizzle), completion on mbarriers, without ever
-//                        waiting on global memory.  The other warps consume blocks
-//                        round-robin, each keeping an online softmax (running
+//                        schedules: it takes items from an atomic counter as
+//                        slots of a two-slot item ring free up and stages each
+//                        item's partition record, block ids and query rows
+//                        there.  Warp 1 (one thread; FP8: warps 1 and 2,
+//                        alternate stages) streams each block's K and V tiles
+//                        into a ring of shared-memory stages with TMA
+//                        (128-byte swizzle), completion on mbarriers, without
+//                        ever waiting on global memory.  Four consumer warps
+//                        own the ring stages (block g of the CTA's stream to
+//                        warp g % 4), each keeping an online softmax (running
 //                        max and sum, fp32) for the G heads; at the end of an
-//                        item they merge their states through shared memory
-//                        and write either the final output (one partition)
-//                        or the partition's (max, sum, unnormalised output);
+//                        item each hands its state to a combiner warp, which
+//                        folds the four and writes either the final output
+//                        (one partition) or the partition's (max, sum,
+//                        unnormalised output), while the consumers go on;
 //   3. merge  (grid-stride) combines the partitions of split sequences:
 //                        one CTA per (sequence, KV head), slices of
 //                        partitions merged with a running maximum.
@@ -928,9 +930,9 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler
-    // Takes work items from the atomic counter one item ahead and stages each
-    // item's partition record and block ids in the item ring, so the TMA warp
-    // never waits on global memory between items.  The plan may be one a
+    // Takes work items from the atomic counter as item-ring slots free up and
+    // stages each item's partition record, block ids and query rows there, so
+    // the TMA warp never waits on global memory between items.  The plan may be one a
     // caller reuses from an earlier call (PA_DECODE_REUSE_PLAN), so it is not
     // trusted: an item count beyond the workspace's capacity is cut, a record
     // that is not a partition of this call's sequences is skipped, and a
@@ -953,7 +955,7 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
     uint32_t g = 0;  // blocks of this CTA's stream before the next item
     // Item blockIdx.x is this CTA's first (no atomic on the critical path of
     // the kernel's start); the work counter hands out the rest from gridDim.x.
-    int next = static_cast<int>(blockIdx.x);
+    bool first = true;
     for (uint32_t it = 0;; ++it) {
       const int slot = it & 1;
       bool ok = true;
@@ -962,17 +964,25 @@ __device__ __forceinline__ void attend_body(const CUtensorMap& tm_k, const CUten
       int item, part = 0, h = 0, first_tok = 0, nblk = 0;
       PartInfo pi;
       for (;;) {  // the next item whose record is a partition of this call
-        item = __shfl_sync(0xffffffffu, next, 0);
+        // claimed only now that its slot is free: near the end of the queue a
+        // CTA then holds one item fewer than it would claiming one ahead
+        int claimed = 0;
+        if (lane == 0) {
+          if (first) {
+            claimed = static_cast<int>(blockIdx.x);
+          } else {
+            const int r = atomicAdd(&P.ws->next_item, 1);
+            // a counter the last call did not leave at 0 never yields a
+            // wrapped index (a negative one is flagged below)
+            claimed = r < 0 ? -1 : (r > INT32_MAX - static_cast<int>(gridDim.x) ? n_items
+                                                                             : static_cast<int>(gridDim.x) + r);
+          }
+        }
+        first = false;
+        item = __shfl_sync(0xffffffffu, claimed, 0);
         if (item < 0) {  // the work counter itself was not reset: no item is taken
           if (lane == 0) atomicOr(err, kErrPlan);
           item = n_items;
-        }
-        if (lane == 0 && item < n_items) {
-          const int r = atomicAdd(&P.ws->next_item, 1);
-          // a counter the last call did not leave at 0 (a negative one is
-          // flagged above on its next use) never yields a wrapped index
-          next = r < 0 ? -1 : (r > INT32_MAX - static_cast<int>(gridDim.x) ? n_items
-                                                                          : static_cast<int>(gridDim.x) + r);
         }
         if (item >= n_items) break;
         part = item / P.hkv;
