@@ -422,17 +422,6 @@ def run_prefill(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = run_prefill_e2e(args, pa, its, w, dev, barrier, dist, world, flops)
-    # ---- every decode config of the workload table, measured the same way ---------
-    per_config = None
-    if args.per_config and world == 1 and not args.fp8 and not grouped:
-        per_config = {}
-        for name in PER_CONFIG:
-            try:
-                per_config[name] = measure_config(pa, W, name, args.steps, args.warmup, dev,
-                                                  measured_peaks()[0],
-                                                  with_oracle=not args.no_cpu_baseline)
-            except Exception as ex:   # report, do not hide
-                per_config[name] = {"error": repr(ex)}
 
     if rank != 0:
         return 0
@@ -666,17 +655,6 @@ def run_cow(args, rank, world, local_rank):
                "steps": steps, "ms_per_step": sec * 1e3,
                "path": "per step: H2D (pinned) source and destination ids -> pa_copy_blocks -> "
                        "D2H of one copied K block; synchronised after the last step"}
-    # ---- every decode config of the workload table, measured the same way ---------
-    per_config = None
-    if args.per_config and world == 1 and not args.fp8 and not grouped:
-        per_config = {}
-        for name in PER_CONFIG:
-            try:
-                per_config[name] = measure_config(pa, W, name, args.steps, args.warmup, dev,
-                                                  measured_peaks()[0],
-                                                  with_oracle=not args.no_cpu_baseline)
-            except Exception as ex:   # report, do not hide
-                per_config[name] = {"error": repr(ex)}
 
     if rank != 0:
         return 0
