@@ -1162,20 +1162,20 @@ def time_graph(step, steps, warmup, stream, barrier, dist, dev, units, world):
 # the ncu captures summarised in profiles/ (file named below), keyed by the
 # hash of the kernel sources they were taken on: a changed kernel reports null.
 TRAFFIC = {
-    ("llama70b", "auto"): {"bytes": 3773.90e6 + 17.71e6, "kernel_src": "7dc38db4d303159b",
+    ("llama70b", "auto"): {"bytes": 3773.74e6 + 9.37e6, "kernel_src": "c08ad2ab15eee90b",
                            "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "mma"): {"bytes": 3773.90e6 + 17.71e6, "kernel_src": "7dc38db4d303159b",
+    ("llama70b", "mma"): {"bytes": 3773.74e6 + 9.37e6, "kernel_src": "c08ad2ab15eee90b",
                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "fp8"): {"bytes": 1889.37e6 + 16.41e6, "kernel_src": "7dc38db4d303159b",
+    ("llama70b", "fp8"): {"bytes": 1889.37e6 + 3.25e6, "kernel_src": "c08ad2ab15eee90b",
                           "profile": "profiles/decode_step_llama70b_fp8_launches.md"},
-    ("fullstep", "auto"): {"bytes": 1979.17e6 + 12.46e6, "kernel_src": "7dc38db4d303159b",
+    ("fullstep", "auto"): {"bytes": 1978.32e6 + 4.05e6, "kernel_src": "c08ad2ab15eee90b",
                            "profile": "profiles/attend_kernel_fullstep_shared_prefix_l2.md"},
-    ("fullstep", "grouped"): {"bytes": 1937.92e6 + 10.35e6, "kernel_src": "7dc38db4d303159b",
+    ("fullstep", "grouped"): {"bytes": 1937.91e6 + 3.81e6, "kernel_src": "c08ad2ab15eee90b",
                               "profile": "profiles/attend_kernel_fullstep_shared_prefix_l2.md"},
-    ("cow", "auto"): {"bytes": 268.52e6 + 216.53e6, "kernel_src": "ba3a77c251cf3178",
+    ("cow", "auto"): {"bytes": 268.52e6 + 216.58e6, "kernel_src": "2f48210de8b75c2c",
                       "profile": "profiles/copy_blocks_kernel_cow.md"},
     # the 8 prefill launches of one step (iterations 1..8), summed
-    ("chunked", "auto"): {"bytes": 1285.08e6 + 286.55e6, "kernel_src": "771ab884a675a98c",
+    ("chunked", "auto"): {"bytes": 1285.57e6 + 286.94e6, "kernel_src": "3609587c3737d282",
                           "profile": "profiles/prefill_tc_kernel_chunked.md"},
 }
 
