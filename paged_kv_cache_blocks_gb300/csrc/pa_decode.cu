@@ -1289,7 +1289,7 @@ __global__ void __launch_bounds__(32 * (NC + 4), 2)
 // rounds of a long sequence (64 partials at G = 4: 8 rounds -> 2).
 
 template <typename T, int D, int kCols, int kThreads>
-__global__ void __launch_bounds__(kThreads, kThreads >= 512 ? 2 : 512 / kThreads)
+__global__ void __launch_bounds__(kThreads, kThreads >= 1024 ? 1 : (kThreads >= 512 ? 2 : 512 / kThreads))
     merge_kernel(const DecodeParams P) {
   constexpr int U = kThreads >= 512 ? 6 : 8;  // partials in flight per thread (no spills)
   constexpr int kMergeSplit = kThreads / kCols;
@@ -1842,6 +1842,15 @@ bool launch_prefix(const CUtensorMap& tk, const CUtensorMap& tv, const DecodePar
   return true;
 }
 
+// Merge kernel for kThreads = one group of kCols threads, 512 or 1024.
+template <typename T, int D, int kCols>
+cudaError_t launch_merge(int threads, dim3 grid, cudaStream_t s, const DecodeParams& P) {
+  if (threads == 1024) return launch_pdl(merge_kernel<T, D, kCols, 1024>, grid, dim3(1024), 0, s, P);
+  if (threads == kMergeThreads)
+    return launch_pdl(merge_kernel<T, D, kCols, kMergeThreads>, grid, dim3(kMergeThreads), 0, s, P);
+  return launch_pdl(merge_kernel<T, D, kCols, kCols>, grid, dim3(kCols), 0, s, P);
+}
+
 int decode_launch(const DecodeArgs& a, std::string* why) {
   const bool grouped = a.num_groups > 0;
   const WsLayout L = ws_layout(a.num_seqs, a.num_q_heads, a.head_dim, a.max_seq_len, grouped);
@@ -1964,37 +1973,29 @@ int decode_launch(const DecodeArgs& a, std::string* why) {
   // 512-thread CTAs whose groups share the partials.
   const bool wide = P.G * a.head_dim / 4 > 128;
   const bool split = (static_cast<int64_t>(a.max_seq_len) + kPartTokens - 1) / kPartTokens > 8;
-  const int mthreads = split ? kMergeThreads : (wide ? 256 : 128);
-  int64_t mgrid = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  const int mres = mthreads >= 512 ? 2 : 512 / mthreads;  // resident merge CTAs per SM
+  // Long sequences: 512 threads, the thread groups sharing a sequence's
+  // partials; 1024 (twice the groups: one round of loads for 64 partials)
+  // when the (sequence, KV head) units fit one CTA per SM.
+  const int64_t units = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+  const int mthreads = split ? (units <= sms ? 1024 : kMergeThreads) : (wide ? 256 : 128);
+  int64_t mgrid = units;
+  const int mres = mthreads >= 1024 ? 1 : (mthreads >= 512 ? 2 : 512 / mthreads);  // resident per SM
   if (mgrid > sms * mres) mgrid = sms * mres;
   if (mgrid < 1) mgrid = 1;
-  const dim3 mg(static_cast<unsigned>(mgrid)), mb(static_cast<unsigned>(mthreads));
+  const dim3 mg(static_cast<unsigned>(mgrid));
   cudaError_t e;
   if (a.dtype == 1) {
-    if (a.head_dim == 128) {
-      if (wide)
-        e = split ? launch_pdl(merge_kernel<__nv_bfloat16, 128, 256, kMergeThreads>, mg, mb, 0, s, P)
-                  : launch_pdl(merge_kernel<__nv_bfloat16, 128, 256, 256>, mg, mb, 0, s, P);
-      else
-        e = split ? launch_pdl(merge_kernel<__nv_bfloat16, 128, 128, kMergeThreads>, mg, mb, 0, s, P)
-                  : launch_pdl(merge_kernel<__nv_bfloat16, 128, 128, 128>, mg, mb, 0, s, P);
-    } else {
-      e = split ? launch_pdl(merge_kernel<__nv_bfloat16, 64, 128, kMergeThreads>, mg, mb, 0, s, P)
-                : launch_pdl(merge_kernel<__nv_bfloat16, 64, 128, 128>, mg, mb, 0, s, P);
-    }
+    if (a.head_dim == 128)
+      e = wide ? launch_merge<__nv_bfloat16, 128, 256>(mthreads, mg, s, P)
+               : launch_merge<__nv_bfloat16, 128, 128>(mthreads, mg, s, P);
+    else
+      e = launch_merge<__nv_bfloat16, 64, 128>(mthreads, mg, s, P);
   } else {
-    if (a.head_dim == 128) {
-      if (wide)
-        e = split ? launch_pdl(merge_kernel<__half, 128, 256, kMergeThreads>, mg, mb, 0, s, P)
-                  : launch_pdl(merge_kernel<__half, 128, 256, 256>, mg, mb, 0, s, P);
-      else
-        e = split ? launch_pdl(merge_kernel<__half, 128, 128, kMergeThreads>, mg, mb, 0, s, P)
-                  : launch_pdl(merge_kernel<__half, 128, 128, 128>, mg, mb, 0, s, P);
-    } else {
-      e = split ? launch_pdl(merge_kernel<__half, 64, 128, kMergeThreads>, mg, mb, 0, s, P)
-                : launch_pdl(merge_kernel<__half, 64, 128, 128>, mg, mb, 0, s, P);
-    }
+    if (a.head_dim == 128)
+      e = wide ? launch_merge<__half, 128, 256>(mthreads, mg, s, P)
+               : launch_merge<__half, 128, 128>(mthreads, mg, s, P);
+    else
+      e = launch_merge<__half, 64, 128>(mthreads, mg, s, P);
   }
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
