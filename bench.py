@@ -1162,15 +1162,15 @@ def time_graph(step, steps, warmup, stream, barrier, dist, dev, units, world):
 # the ncu captures summarised in profiles/ (file named below), keyed by the
 # hash of the kernel sources they were taken on: a changed kernel reports null.
 TRAFFIC = {
-    ("llama70b", "auto"): {"bytes": 3773.74e6 + 9.37e6, "kernel_src": "c08ad2ab15eee90b",
+    ("llama70b", "auto"): {"bytes": 3773.76e6 + 9.35e6, "kernel_src": "e0b3982bd76effc8",
                            "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "mma"): {"bytes": 3773.74e6 + 9.37e6, "kernel_src": "c08ad2ab15eee90b",
+    ("llama70b", "mma"): {"bytes": 3773.76e6 + 9.35e6, "kernel_src": "e0b3982bd76effc8",
                           "profile": "profiles/attend_kernel_llama70b_dram.md"},
-    ("llama70b", "fp8"): {"bytes": 1889.37e6 + 3.25e6, "kernel_src": "c08ad2ab15eee90b",
+    ("llama70b", "fp8"): {"bytes": 1889.38e6 + 3.37e6, "kernel_src": "e0b3982bd76effc8",
                           "profile": "profiles/decode_step_llama70b_fp8_launches.md"},
-    ("fullstep", "auto"): {"bytes": 1978.32e6 + 4.05e6, "kernel_src": "c08ad2ab15eee90b",
+    ("fullstep", "auto"): {"bytes": 1978.47e6 + 4.28e6, "kernel_src": "e0b3982bd76effc8",
                            "profile": "profiles/attend_kernel_fullstep_shared_prefix_l2.md"},
-    ("fullstep", "grouped"): {"bytes": 1937.91e6 + 3.81e6, "kernel_src": "c08ad2ab15eee90b",
+    ("fullstep", "grouped"): {"bytes": 1937.99e6 + 3.73e6, "kernel_src": "e0b3982bd76effc8",
                               "profile": "profiles/attend_kernel_fullstep_shared_prefix_l2.md"},
     ("cow", "auto"): {"bytes": 268.52e6 + 216.58e6, "kernel_src": "2f48210de8b75c2c",
                       "profile": "profiles/copy_blocks_kernel_cow.md"},
