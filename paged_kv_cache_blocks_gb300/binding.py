@@ -464,3 +464,10 @@ class Allocator:
         return {"num_blocks": st.num_blocks, "free": st.free_blocks, "used": st.used_blocks,
                 "shared": st.shared_blocks, "refs": st.refs, "seqs": st.seqs,
                 "frag_tokens": st.frag_tokens}
+
+
+# The two calls of the decode step under their short names as well:
+# cache_write(k, v, slot_mapping, k_cache, v_cache) and
+# decode(q, k_cache, v_cache, block_tables, seq_lens, scale) -> out.
+cache_write = pa_cache_write
+decode = pa_decode

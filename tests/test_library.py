@@ -201,3 +201,9 @@ def test_noalloc_binding_checks_index_types(monkeypatch):
         with pytest.raises(TypeError, match="int32"):
             b.pa_decode_fp8(q, kc, kc, torch.ones(2), torch.ones(2), tab, lens, 0.1, out=q,
                             workspace=torch.zeros(256, dtype=torch.uint8))
+
+
+def test_binding_short_names_are_the_c_calls():
+    from paged_kv_cache_blocks_gb300 import binding
+    assert binding.cache_write is binding.pa_cache_write
+    assert binding.decode is binding.pa_decode
