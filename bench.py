@@ -1172,7 +1172,7 @@ TRAFFIC = {
                            "profile": "profiles/attend_kernel_fullstep_shared_prefix_l2.md"},
     ("fullstep", "grouped"): {"bytes": 1937.99e6 + 3.73e6, "kernel_src": "e0b3982bd76effc8",
                               "profile": "profiles/attend_kernel_fullstep_shared_prefix_l2.md"},
-    ("cow", "auto"): {"bytes": 268.52e6 + 216.58e6, "kernel_src": "2f48210de8b75c2c",
+    ("cow", "auto"): {"bytes": 268.53e6 + 216.54e6, "kernel_src": "52affb2a945dc192",
                       "profile": "profiles/copy_blocks_kernel_cow.md"},
     # the 8 prefill launches of one step (iterations 1..8), summed
     ("chunked", "auto"): {"bytes": 1285.57e6 + 286.94e6, "kernel_src": "3609587c3737d282",

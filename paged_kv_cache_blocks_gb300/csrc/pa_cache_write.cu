@@ -27,17 +27,16 @@ __global__ void __launch_bounds__(256)
   const int rem = static_cast<int>(i - t * chunks_per_token);
   const int h = rem / chunks_per_row;
   const int c = rem - h * chunks_per_row;
+  // the chunk is loaded together with its token's slot (its index does not
+  // depend on the slot): one round trip to global memory, not two
+  const uint4 val = blockIdx.y == 0 ? k[i] : v[i];
   const int64_t s = slot_mapping[t];
   if (s < 0) return;                      // padding token
   const int64_t blk = s / kBlock;
   if (blk >= num_blocks) return;          // outside the pool: not written
   const int64_t off = s - blk * kBlock;
   const int64_t dst = ((blk * hkv + h) * kBlock + off) * chunks_per_row + c;
-  if (blockIdx.y == 0) {
-    k_cache[dst] = k[i];
-  } else {
-    v_cache[dst] = v[i];
-  }
+  (blockIdx.y == 0 ? k_cache : v_cache)[dst] = val;
 }
 
 int cache_write_launch(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
