@@ -30,7 +30,13 @@ without the barrier.
 The FP8 kernel has two copy threads: thread p refills the stages of the
 blocks g with g % 2 == p, in order, each independently of the other (one
 may run ahead).  The model runs P independent producers the same way and
-checks that the protocol stays safe with them."""
+checks that the protocol stays safe with them.
+
+The consumers hand their per-item states to the combiner warp through two
+merge slots guarded by a full and an empty mbarrier each; a second model
+runs that hand-off with random timing and checks that the combiner only
+ever reads the states of the item it is folding (and that the empty wait
+needs its parity flipped on first use)."""
 import random
 
 import pytest
@@ -193,4 +199,57 @@ def test_item_relative_consumers_without_barrier_are_unsafe():
     rng = random.Random(11)
     results = [simulate(8, 4, "item", random_items(rng, 12), seed, merge_barrier=False)
                for seed in range(40)]
+    assert any(r != 0 for r in results)
+
+
+def simulate_merge_slots(NC, n_items, seed, slots=2, empty_parity_flip=True):
+    """The hand-off between the consumer warps and the combiner warp: at the
+    end of item `it` each consumer waits merge_empty[it % slots] (parity
+    ((it // slots) & 1) ^ 1), stores its state into merge slot it % slots
+    and arrives merge_full[it % slots]; the combiner, item by item, waits
+    merge_full[it % slots] (parity (it // slots) & 1), reads the NC states
+    and arrives merge_empty[it % slots].  Returns the number of reads that
+    saw a state of another item (0 = safe), or -1 on deadlock."""
+    rng = random.Random(seed)
+    full = [Barrier(NC) for _ in range(slots)]
+    empty = [Barrier(1) for _ in range(slots)]
+    slot_state = [[None] * NC for _ in range(slots)]
+    cons_it = [0] * NC            # next item each consumer finishes
+    comb_it = 0
+    bad = 0
+    steps = 0
+    while comb_it < n_items:
+        steps += 1
+        if steps > 200 * n_items * (NC + 1) + 10000:
+            return -1
+        actor = rng.randrange(NC + 1)
+        if actor < NC:
+            it = cons_it[actor]
+            if it >= n_items:
+                continue
+            s, r = it % slots, it // slots
+            parity = ((r & 1) ^ 1) if empty_parity_flip else (r & 1)
+            if empty[s].try_wait(parity):
+                slot_state[s][actor] = it
+                full[s].arrive()
+                cons_it[actor] += 1
+        else:
+            s, r = comb_it % slots, comb_it // slots
+            if full[s].try_wait(r & 1):
+                bad += sum(1 for w in range(NC) if slot_state[s][w] != comb_it)
+                empty[s].arrive()
+                comb_it += 1
+    return bad
+
+
+@pytest.mark.parametrize("NC", [1, 2, 4])
+def test_combiner_hand_off_never_reads_another_items_state(NC):
+    for seed in range(60):
+        assert simulate_merge_slots(NC, 25, seed) == 0
+
+
+def test_combiner_hand_off_without_the_empty_parity_flip_is_unsafe():
+    """Waiting merge_empty on the full barrier's parity (no flip) lets the
+    first uses of a slot block forever or overwrite: the flip is needed."""
+    results = [simulate_merge_slots(4, 25, seed, empty_parity_flip=False) for seed in range(20)]
     assert any(r != 0 for r in results)
